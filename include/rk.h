@@ -1,0 +1,221 @@
+/*
+ * rk.h -- C ABI of the GB300 recurrent-layer library (ONNX LSTM / GRU / RNN
+ * forward pass on one GPU, sm_103a).
+ *
+ * The operation is the one defined on the web page "Recurrent layers"
+ * (onegpu docs):
+ *   - first paragraph: cells RNN, GRU, LSTM; directions forward, reverse,
+ *     bidirectional; layouts 0 and 1; sequence_lens; initial states;
+ *     peepholes; clip; input_forget; linear_before_reset; the eleven ONNX
+ *     activations with alpha / beta resolved by the caller; all tensors
+ *     float32 or all Half, with float32 accumulation and float32 state;
+ *   - the C# example and the paragraph after it: a problem description
+ *     (RecurrentProblem) and an operand list X, W, R, B, sequence_lens,
+ *     initial_h, initial_c, P, Y, Y_h, Y_c, each a buffer plus an element
+ *     offset (GpuTensorRef); W, R, B, P used as stored, gate order i, o, f, c
+ *     (LSTM) and z, r, h (GRU); null outputs are not written;
+ *   - section "How a layer runs": the input projection Xw = X . W^T for all
+ *     steps and directions, the state setup, the steps, the outputs;
+ *   - section "Arithmetic and determinism": pre = ((xw + rec) + Wb) + Rb,
+ *     then peepholes, clip, activation, state update; runs are bit-identical;
+ *   - section "Semantics": sequence_lens, Seq = 0, Batch = 0, clip, options
+ *     legal per cell (anything else is an error);
+ *   - the "Scratch" paragraph: XwLength / StateLength floats, kept by the
+ *     library and grown on demand, or placed by the caller with element
+ *     offsets (both may sit in one arena); checks in safe arithmetic before
+ *     anything is launched, with an error that names the cell and argument.
+ *
+ * Shapes (D = 2 for bidirectional, else 1; G = 4 LSTM, 3 GRU, 1 RNN;
+ * S seq, N batch, I input, H hidden), all dense row-major:
+ *   X            [S, N, I] (layout 0)   or [N, S, I] (layout 1)
+ *   W            [D, G*H, I]
+ *   R            [D, G*H, H]
+ *   B            [D, 2*G*H]   (Wb then Rb)               optional, else 0
+ *   sequence_lens[N] int32                                optional, else S
+ *   initial_h    [D, N, H]   (layout 0) or [N, D, H]      optional, else 0
+ *   initial_c    same as initial_h, LSTM only             optional, else 0
+ *   P            [D, 3*H]    (i, o, f), LSTM only         optional, else 0
+ *   Y            [S, D, N, H] (layout 0) or [N, S, D, H]  optional output
+ *   Y_h          [D, N, H]   (layout 0) or [N, D, H]      optional output
+ *   Y_c          same as Y_h, LSTM only                   optional output
+ * Every tensor other than sequence_lens has the problem's dtype (float32 or
+ * IEEE binary16).  Outputs are rounded to nearest even when Half.
+ *
+ * Ownership: every tensor pointer is caller-owned DEVICE memory (except in
+ * rk_encode_host, which takes host memory).  The library never frees or
+ * rewrites an input.  Handles are not thread-safe: one host thread at a time.
+ * Errors: every function returns an rk_status; nothing is launched when a
+ * check fails; rk_last_error() then names the cell and the argument.
+ */
+#ifndef RK_H_
+#define RK_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t rk_status;
+#define RK_OK 0
+#define RK_ERR_SHAPE 1       /* bad size, offset, option for the cell, overflow */
+#define RK_ERR_UNSUPPORTED 2 /* legal but not runnable here (residency, size)  */
+#define RK_ERR_CUDA 3        /* a CUDA call failed; message has the error name  */
+#define RK_ERR_TIMEOUT 4     /* a bounded device wait gave up                   */
+#define RK_ERR_OOM 5         /* device scratch allocation failed                */
+#define RK_ERR_ARG 6         /* null handle / problem / operand list            */
+
+enum rk_cell { RK_LSTM = 0, RK_GRU = 1, RK_RNN = 2 };
+enum rk_direction { RK_FORWARD = 0, RK_REVERSE = 1, RK_BIDIRECTIONAL = 2 };
+enum rk_dtype { RK_F32 = 0, RK_F16 = 1 };
+enum rk_activation_kind {
+  RK_ACT_SIGMOID = 0,
+  RK_ACT_TANH = 1,
+  RK_ACT_RELU = 2,
+  RK_ACT_AFFINE = 3,           /* alpha*x + beta */
+  RK_ACT_LEAKY_RELU = 4,       /* x >= 0 ? x : alpha*x */
+  RK_ACT_THRESHOLDED_RELU = 5, /* x > alpha ? x : 0 */
+  RK_ACT_SCALED_TANH = 6,      /* alpha*tanh(beta*x) */
+  RK_ACT_HARD_SIGMOID = 7,     /* clamp(alpha*x + beta, 0, 1) */
+  RK_ACT_ELU = 8,              /* x >= 0 ? x : alpha*(exp(x) - 1) */
+  RK_ACT_SOFTSIGN = 9,         /* x / (1 + |x|) */
+  RK_ACT_SOFTPLUS = 10         /* log(1 + exp(x)) */
+};
+
+/* rk_create flags */
+#define RK_FORCE_SIMT_PROJECTION 1u /* Half problems: SIMT projection, no tensor cores */
+#define RK_FORCE_GRID_STEP 2u       /* use the grid-wide step kernel even where a cluster fits */
+
+/* One activation slot (GpuRecurrentActivation): kind plus resolved alpha/beta. */
+typedef struct rk_activation {
+  int32_t kind;
+  float alpha;
+  float beta;
+} rk_activation;
+
+/* The layer (RecurrentProblem). */
+typedef struct rk_problem {
+  int32_t cell;                /* rk_cell */
+  int32_t direction;           /* rk_direction */
+  int32_t dtype;               /* rk_dtype, shared by all tensors */
+  int32_t layout;              /* 0 or 1 */
+  int64_t seq, batch, input, hidden;
+  float clip;                  /* > 0 clamps pre-activations to [-clip, clip]; else off */
+  int32_t input_forget;        /* LSTM only: f = 1 - i */
+  int32_t linear_before_reset; /* GRU only */
+  int32_t num_acts;            /* 0: ONNX defaults; else G' * D (G' = 3 LSTM, 2 GRU, 1 RNN) */
+  rk_activation act[6];        /* slots f, g, h of direction 0, then of direction 1 */
+  int64_t max_length;          /* 0: seq.  Else a promise that no sequence_lens
+                                  entry exceeds it; shortens the step loop.
+                                  Needs sequence_lens when < seq. */
+} rk_problem;
+
+/* A tensor (GpuTensorRef): base pointer, element offset from it, and the
+ * number of elements available from the base (the buffer's length), so the
+ * library can check offset + extent <= length.  ptr == NULL means absent. */
+typedef struct rk_tensor {
+  void* ptr;
+  int64_t offset;
+  int64_t length;
+} rk_tensor;
+
+/* The operand list (RecurrentOperands).  X, W, R are required. */
+typedef struct rk_operands {
+  rk_tensor X, W, R, B, sequence_lens, initial_h, initial_c, P, Y, Y_h, Y_c;
+} rk_operands;
+
+/* Caller-placed scratch (float32 device memory).  Either pointer may be NULL,
+ * in which case the library uses its own grown-on-demand allocation.  The two
+ * regions may lie in one arena buffer but must not overlap.  state + offset
+ * must be 16-byte aligned (it is read as float4); xw has no alignment rule. */
+typedef struct rk_scratch {
+  float* xw;
+  int64_t xw_offset;
+  int64_t xw_length;
+  float* state;
+  int64_t state_offset;
+  int64_t state_length;
+} rk_scratch;
+
+typedef struct rk_handle rk_handle;
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int32_t rk_version(void);
+
+/* Create a handle.  No CUDA call is made until the first encode, so this
+ * works without a GPU.  flags: RK_FORCE_* bits.  *out receives the handle. */
+rk_status rk_create(rk_handle** out, uint32_t flags);
+
+/* Wait for the handle's work on the streams it used, free its scratch and the
+ * handle.  NULL is accepted. */
+rk_status rk_destroy(rk_handle* h);
+
+/* Floats of projection scratch the problem needs (XwLength): D * S * N * G * H
+ * for S, N > 0, else 0.  Returns -1 for an invalid problem. */
+int64_t rk_xw_length(const rk_problem* p);
+
+/* Floats of state scratch the problem needs (StateLength): the double-buffered
+ * hidden state exchanged between blocks of the step kernel plus its barrier
+ * and status words.  Returns -1 for an invalid problem. */
+int64_t rk_state_length(const rk_problem* p);
+
+/* Host-only validation of a problem and its operands (sizes, offsets,
+ * extents, options legal for the cell); makes no CUDA call.  Returns RK_OK or
+ * the error encode would return, with rk_last_error set. */
+rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops);
+
+/* Enqueue the whole layer on `stream` (a cudaStream_t; NULL = legacy default
+ * stream): input projection, then one persistent step kernel that runs every
+ * step and writes Y, Y_h, Y_c.  Asynchronous: returns after enqueueing.
+ * scratch may be NULL.  All operand pointers are device pointers. */
+rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops,
+                    const rk_scratch* scratch, void* stream);
+
+/* Same layer with HOST operand pointers: copies the inputs to device buffers
+ * owned by the handle (grown on demand), encodes on `stream`, copies the
+ * requested outputs back and synchronises the stream before returning. */
+rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* host_ops,
+                         void* stream);
+
+/* Synchronise `stream`, read and clear the device status word of the handle:
+ * RK_OK, or RK_ERR_TIMEOUT if a bounded barrier wait of the grid step kernel
+ * gave up during a previous encode. */
+rk_status rk_status_poll(rk_handle* h, void* stream);
+
+/* Nanoseconds (measured on the GPU's global timer) a device-side wait of the
+ * step kernel may spin before it gives up, sets the status word and lets the
+ * kernel wind down; default 2e9 (2 s).  limit must be >= 1. */
+rk_status rk_set_wait_limit(rk_handle* h, int64_t limit);
+
+/* Run the step kernels' bounded device waits against a grid barrier and an
+ * mbarrier that nothing completes (one CTA, no other memory touched): each
+ * must give up after timeout_ns and set the handle's status word.  Returns
+ * RK_OK once the check kernel is enqueued on `stream`; rk_status_poll then
+ * returns RK_ERR_TIMEOUT.  Used to test the give-up path without a hang. */
+rk_status rk_selftest_timeout(rk_handle* h, void* stream, int64_t timeout_ns);
+
+/* Kernel timing for measurement: with enabled != 0 every later encode records
+ * CUDA events (on its stream) around its projection launch and its step
+ * launch; rk_last_timings then waits for them and returns the two durations
+ * of the most recent encode in milliseconds (-1 for a launch that did not
+ * happen).  Disabled by default. */
+rk_status rk_set_profiling(rk_handle* h, int32_t enabled);
+rk_status rk_last_timings(rk_handle* h, float* projection_ms, float* step_ms);
+
+/* Message of the last failed call on this handle ("" if none).  The string
+ * belongs to the handle. */
+const char* rk_last_error(const rk_handle* h);
+
+/* Number of kernels this handle has launched so far (all encodes). */
+uint64_t rk_launch_count(const rk_handle* h);
+
+/* Describe the plan encode would use for a problem (for logs and tests): a
+ * NUL-terminated text such as "proj=simt_f32 step=cluster16 nb=1 ..." written
+ * into buf (at most len bytes).  Host only. */
+rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RK_H_ */

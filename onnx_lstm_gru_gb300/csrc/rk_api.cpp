@@ -1,0 +1,696 @@
+// rk_api.cpp -- host side of the C ABI declared in include/rk.h: argument
+// checks in 64-bit arithmetic, the launch plan, scratch management and the
+// two launches of a layer (projection, then the persistent step kernel).
+//
+// Behaviour follows the web page "Recurrent layers" (onegpu docs): the
+// "Scratch" paragraph (XwLength / StateLength floats, library-owned and grown
+// on demand or caller-placed with element offsets; sizes, offsets and shapes
+// checked in safe arithmetic before anything is recorded, errors naming
+// LSTM/GRU/RNN and the argument) and section "Semantics" (Batch = 0 records
+// nothing; Seq = 0 returns the initial states; peepholes, input_forget,
+// initial_c and Y_c only for an LSTM, linear_before_reset only for a GRU).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "rk.h"
+#include "rk_internal.h"
+
+struct rk_handle {
+  uint32_t flags = 0;
+  std::string last_error;
+  uint64_t launches = 0;
+  long long timeout_ns = 2000000000LL;  // 2 s
+  bool dev_ready = false;
+  int device = -1;
+  int sms = 152;
+  int smem_optin = 232448;
+  int* status = nullptr;
+  float* xw = nullptr;
+  size_t xw_cap = 0;
+  float* state = nullptr;
+  size_t state_cap = 0;
+  unsigned char* host_arena = nullptr;  // device buffers for rk_encode_host
+  size_t host_arena_cap = 0;
+  bool profiling = false;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // proj start/end, step start/end
+  bool ev_proj = false, ev_step = false;
+};
+
+namespace {
+
+using rk::StepPlan;
+using rk::StepParams;
+
+const char* cell_name(int32_t c) {
+  switch (c) {
+    case RK_LSTM: return "LSTM";
+    case RK_GRU: return "GRU";
+    case RK_RNN: return "RNN";
+    default: return "recurrent";
+  }
+}
+
+rk_status fail(rk_handle* h, rk_status code, const char* fmt, ...) {
+  if (h != nullptr) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    h->last_error = buf;
+  }
+  return code;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+int gates_of(int32_t cell) { return cell == RK_LSTM ? 4 : (cell == RK_GRU ? 3 : 1); }
+int acts_per_dir(int32_t cell) { return cell == RK_LSTM ? 3 : (cell == RK_GRU ? 2 : 1); }
+int dirs_of(const rk_problem* p) { return p->direction == RK_BIDIRECTIONAL ? 2 : 1; }
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Element counts of every operand; -1 where a product overflows.
+struct Extents {
+  int64_t X, W, R, B, lens, state, P, Y;
+};
+
+bool extents_of(const rk_problem* p, Extents* e) {
+  const int64_t G = gates_of(p->cell), D = dirs_of(p);
+  int64_t GH, t1, t2;
+  if (!mul_ok(G, p->hidden, &GH)) return false;
+  if (!mul_ok(p->seq, p->batch, &t1) || !mul_ok(t1, p->input, &e->X)) return false;
+  if (!mul_ok(D, GH, &t1) || !mul_ok(t1, p->input, &e->W)) return false;
+  if (!mul_ok(t1, p->hidden, &e->R)) return false;
+  if (!mul_ok(t1, 2, &e->B)) return false;
+  e->lens = p->batch;
+  if (!mul_ok(D, p->batch, &t2) || !mul_ok(t2, p->hidden, &e->state)) return false;
+  if (!mul_ok(D, 3, &t1) || !mul_ok(t1, p->hidden, &e->P)) return false;
+  if (!mul_ok(p->seq, e->state, &e->Y)) return false;
+  return true;
+}
+
+rk_status check_tensor(rk_handle* h, const rk_problem* p, const char* name, const rk_tensor& t, int64_t extent,
+                       bool required) {
+  const char* cn = cell_name(p->cell);
+  if (t.ptr == nullptr) {
+    if (required && extent > 0) return fail(h, RK_ERR_SHAPE, "%s: %s: required tensor is null", cn, name);
+    return RK_OK;
+  }
+  if (t.offset < 0) return fail(h, RK_ERR_SHAPE, "%s: %s: negative offset %lld", cn, name, (long long)t.offset);
+  if (t.length < 0) return fail(h, RK_ERR_SHAPE, "%s: %s: negative length %lld", cn, name, (long long)t.length);
+  int64_t end;
+  if (!add_ok(t.offset, extent, &end))
+    return fail(h, RK_ERR_SHAPE, "%s: %s: offset %lld + extent %lld overflows", cn, name, (long long)t.offset,
+                (long long)extent);
+  if (end > t.length)
+    return fail(h, RK_ERR_SHAPE, "%s: %s: offset %lld + extent %lld exceeds buffer length %lld", cn, name,
+                (long long)t.offset, (long long)extent, (long long)t.length);
+  return RK_OK;
+}
+
+rk_status validate_problem(rk_handle* h, const rk_problem* p) {
+  if (p == nullptr) return fail(h, RK_ERR_ARG, "recurrent: problem is null");
+  if (p->cell < RK_LSTM || p->cell > RK_RNN) return fail(h, RK_ERR_SHAPE, "recurrent: cell: unknown value %d", p->cell);
+  const char* cn = cell_name(p->cell);
+  if (p->direction < RK_FORWARD || p->direction > RK_BIDIRECTIONAL)
+    return fail(h, RK_ERR_SHAPE, "%s: direction: unknown value %d", cn, p->direction);
+  if (p->dtype != RK_F32 && p->dtype != RK_F16) return fail(h, RK_ERR_SHAPE, "%s: dtype: unknown value %d", cn, p->dtype);
+  if (p->layout != 0 && p->layout != 1) return fail(h, RK_ERR_SHAPE, "%s: layout: must be 0 or 1, got %d", cn, p->layout);
+  const int64_t lim = 0x7fffffffLL;
+  if (p->seq < 0 || p->seq > lim) return fail(h, RK_ERR_SHAPE, "%s: seq: %lld out of range", cn, (long long)p->seq);
+  if (p->batch < 0 || p->batch > lim)
+    return fail(h, RK_ERR_SHAPE, "%s: batch: %lld out of range", cn, (long long)p->batch);
+  if (p->input < 0 || p->input > lim)
+    return fail(h, RK_ERR_SHAPE, "%s: input: %lld out of range", cn, (long long)p->input);
+  if (p->hidden < 0 || p->hidden > lim)
+    return fail(h, RK_ERR_SHAPE, "%s: hidden: %lld out of range", cn, (long long)p->hidden);
+  if (p->input_forget != 0 && p->cell != RK_LSTM)
+    return fail(h, RK_ERR_SHAPE, "%s: input_forget: only an LSTM has it", cn);
+  if (p->linear_before_reset != 0 && p->cell != RK_GRU)
+    return fail(h, RK_ERR_SHAPE, "%s: linear_before_reset: only a GRU has it", cn);
+  const int want = acts_per_dir(p->cell) * dirs_of(p);
+  if (p->num_acts != 0 && p->num_acts != want)
+    return fail(h, RK_ERR_SHAPE, "%s: activations: expected 0 or %d, got %d", cn, want, p->num_acts);
+  for (int i = 0; i < p->num_acts; ++i)
+    if (p->act[i].kind < RK_ACT_SIGMOID || p->act[i].kind > RK_ACT_SOFTPLUS)
+      return fail(h, RK_ERR_SHAPE, "%s: activations[%d]: unknown kind %d", cn, i, p->act[i].kind);
+  if (p->max_length < 0 || p->max_length > p->seq)
+    return fail(h, RK_ERR_SHAPE, "%s: max_length: %lld not in [0, seq=%lld]", cn, (long long)p->max_length,
+                (long long)p->seq);
+  Extents e;
+  if (!extents_of(p, &e)) return fail(h, RK_ERR_SHAPE, "%s: sizes overflow 64-bit element counts", cn);
+  int64_t m, gh;
+  if (!mul_ok(p->seq, p->batch, &m) || m > lim || !mul_ok(gates_of(p->cell), p->hidden, &gh) || gh > lim)
+    return fail(h, RK_ERR_UNSUPPORTED, "%s: seq*batch or gates*hidden exceeds 2^31 - 1", cn);
+  return RK_OK;
+}
+
+rk_status validate_all(rk_handle* h, const rk_problem* p, const rk_operands* o) {
+  rk_status st = validate_problem(h, p);
+  if (st != RK_OK) return st;
+  if (o == nullptr) return fail(h, RK_ERR_ARG, "%s: operands: null", cell_name(p->cell));
+  const char* cn = cell_name(p->cell);
+  Extents e;
+  extents_of(p, &e);
+  const bool lstm = p->cell == RK_LSTM;
+  if (!lstm) {
+    if (o->P.ptr) return fail(h, RK_ERR_SHAPE, "%s: P: peepholes exist only for an LSTM", cn);
+    if (o->initial_c.ptr) return fail(h, RK_ERR_SHAPE, "%s: initial_c: exists only for an LSTM", cn);
+    if (o->Y_c.ptr) return fail(h, RK_ERR_SHAPE, "%s: Y_c: exists only for an LSTM", cn);
+  }
+  if (p->max_length > 0 && p->max_length < p->seq && o->sequence_lens.ptr == nullptr)
+    return fail(h, RK_ERR_SHAPE, "%s: max_length: %lld < seq needs sequence_lens", cn, (long long)p->max_length);
+  if ((st = check_tensor(h, p, "X", o->X, e.X, true)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "W", o->W, e.W, true)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "R", o->R, e.R, true)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "B", o->B, e.B, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "sequence_lens", o->sequence_lens, e.lens, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "initial_h", o->initial_h, e.state, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "initial_c", o->initial_c, e.state, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "P", o->P, e.P, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "Y", o->Y, e.Y, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "Y_h", o->Y_h, e.state, false)) != RK_OK) return st;
+  if ((st = check_tensor(h, p, "Y_c", o->Y_c, e.state, false)) != RK_OK) return st;
+  return RK_OK;
+}
+
+int64_t xw_len(const rk_problem* p) {
+  if (p->seq == 0 || p->batch == 0) return 0;
+  return (int64_t)dirs_of(p) * p->seq * p->batch * gates_of(p->cell) * p->hidden;
+}
+int64_t kp_of(const rk_problem* p) { return round_up(std::max<int64_t>(p->hidden, 1), rk::kKChunk); }
+int64_t state_len(const rk_problem* p) {
+  return rk::kStateHeader + 3 * (int64_t)dirs_of(p) * p->batch * kp_of(p);
+}
+
+rk_status ensure_device(rk_handle* h) {
+  if (h->dev_ready) return RK_OK;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+  if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
+  if (e != cudaSuccess) return fail(h, RK_ERR_CUDA, "recurrent: device setup failed: %s", cudaGetErrorName(e));
+  h->dev_ready = true;
+  return RK_OK;
+}
+
+void fill_params_problem(const rk_problem* p, StepParams* sp) {
+  std::memset(sp, 0, sizeof(*sp));
+  sp->cell = p->cell;
+  sp->dtype = p->dtype;
+  sp->direction = p->direction;
+  sp->layout = p->layout;
+  sp->S = (int)p->seq;
+  sp->N = (int)p->batch;
+  sp->I = (int)p->input;
+  sp->H = (int)p->hidden;
+  sp->D = dirs_of(p);
+  sp->G = gates_of(p->cell);
+  sp->T = (int)(p->max_length > 0 ? p->max_length : p->seq);
+  sp->clip = p->clip;
+  sp->input_forget = p->input_forget != 0;
+  sp->lbr = p->linear_before_reset != 0;
+  const int want = acts_per_dir(p->cell) * sp->D;
+  if (p->num_acts == 0) {
+    sp->generic_acts = 0;
+    const int defk[3][3] = {{RK_ACT_SIGMOID, RK_ACT_TANH, RK_ACT_TANH}, {RK_ACT_SIGMOID, RK_ACT_TANH, 0}, {RK_ACT_TANH, 0, 0}};
+    for (int i = 0; i < want; ++i) sp->acts[i] = {defk[p->cell][i % acts_per_dir(p->cell)], 0.0f, 0.0f};
+  } else {
+    sp->generic_acts = 1;
+    for (int i = 0; i < want; ++i) sp->acts[i] = {p->act[i].kind, p->act[i].alpha, p->act[i].beta};
+  }
+  sp->KP = (int)kp_of(p);
+}
+
+// Step-kernel plan.  Cluster kernel when R fits one cluster's shared memory,
+// else the grid kernel.  `check` asks the occupancy API (needs a device).
+rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
+  const int G = sp->G, D = sp->D, N = sp->N, H = sp->H, KP = sp->KP;
+  const int eb = p->dtype == RK_F32 ? 4 : 2;
+  const bool lbr0 = p->cell == RK_GRU && !p->linear_before_reset;
+  (void)lbr0;
+  const int smem_cap = h->smem_optin - 1024;  // room for the kernel's static shared memory
+  auto finish = [&](StepPlan& pl) -> bool {
+    sp->team_ctas = pl.team_ctas;
+    sp->J = pl.J;
+    sp->nb = pl.nb;
+    sp->teams_per_dir = pl.teams_per_dir;
+    sp->rows_pad = pl.rows_pad;
+    sp->nbc = pl.nbc;
+    pl.KP = KP;
+    pl.smem = rk::step_smem_for(*sp, pl);
+    return pl.smem > 0 && (int)pl.smem <= smem_cap;
+  };
+  auto resident = [&](const StepPlan& pl) -> int {
+    int teams = 0;
+    StepParams probe = *sp;
+    cudaError_t e;
+    switch (p->cell) {
+      case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(probe, pl, nullptr, &teams)
+                                                    : rk::step_entry<0, true>(probe, pl, nullptr, &teams); break;
+      case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(probe, pl, nullptr, &teams)
+                                                   : rk::step_entry<1, true>(probe, pl, nullptr, &teams); break;
+      default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(probe, pl, nullptr, &teams)
+                                               : rk::step_entry<2, true>(probe, pl, nullptr, &teams); break;
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return teams;
+  };
+
+  if (!(h->flags & RK_FORCE_GRID_STEP)) {
+    const int nb = N == 1 ? 1 : std::min(N, 8);
+    const rk::StepShape shape = nb == 1 ? rk::kShapeR8B1 : rk::kShapeR4B8;
+    const int rpw = shape == rk::kShapeR8B1 ? 8 : 4;
+    const int maxt = shape == rk::kShapeR8B1 ? 512 : 768;
+    for (int C = 1; C <= 16; C *= 2) {
+      StepPlan pl{};
+      pl.kind = rk::kStepCluster;
+      pl.shape = shape;
+      pl.team_ctas = C;
+      pl.J = (int)((H + C - 1) / C);
+      pl.nb = nb;
+      pl.nbc = nb == 1 ? 1 : 8;
+      pl.teams_per_dir = (N + nb - 1) / nb;
+      const int Jp = (int)round_up(pl.J, rpw);
+      pl.rows_pad = G * Jp;
+      const int warps = pl.rows_pad / rpw;
+      pl.threads = (int)std::max<int64_t>(32 * warps, round_up((int64_t)pl.J * nb, 32));
+      pl.threads = std::max(pl.threads, 64);
+      pl.grid = D * pl.teams_per_dir * C;
+      const int64_t rbytes = (int64_t)pl.rows_pad * KP * eb;
+      if (pl.threads > maxt) continue;
+      if (rbytes > 64 * 1024 && C < 16) continue;  // spread R until a slice is <= 64 KB
+      if (!finish(pl)) continue;
+      if (check && resident(pl) < 1) continue;
+      *out = pl;
+      return RK_OK;
+    }
+  }
+  // grid kernel: all SMs, one CTA each, teams of up to 64 batch rows
+  {
+    StepPlan pl{};
+    pl.kind = rk::kStepGrid;
+    const int nb = std::min(N, 64);
+    pl.nb = nb;
+    pl.teams_per_dir = (N + nb - 1) / nb;
+    pl.shape = nb <= 4 ? rk::kShapeR8B4 : rk::kShapeR4B8;
+    pl.nbc = nb <= 4 ? 4 : 8;
+    const int rpw = nb <= 4 ? 8 : 4;
+    const int teams = D * pl.teams_per_dir;
+    if (teams > rk::kStateHeader)
+      return fail(h, RK_ERR_UNSUPPORTED, "%s: batch %d needs too many grid teams", cell_name(p->cell), N);
+    int per_team = h->sms / teams;
+    if (per_team < 1)
+      return fail(h, RK_ERR_UNSUPPORTED, "%s: %d teams exceed %d SMs", cell_name(p->cell), teams, h->sms);
+    pl.J = (H + per_team - 1) / per_team;
+    pl.team_ctas = (H + pl.J - 1) / pl.J;
+    const int Jp = (int)round_up(pl.J, rpw);
+    pl.rows_pad = G * Jp;
+    pl.threads = (int)std::min<int64_t>(768, std::max<int64_t>(256, 32 * (pl.rows_pad / rpw)));
+    pl.grid = teams * pl.team_ctas;
+    if (!finish(pl))
+      return fail(h, RK_ERR_UNSUPPORTED, "%s: R slice of %d rows x %d does not fit shared memory", cell_name(p->cell),
+                  pl.rows_pad, KP);
+    if (check) {
+      // every CTA of the launch must be resident at once
+      const int r = resident(pl);
+      if (r * pl.team_ctas < pl.grid)
+        return fail(h, RK_ERR_UNSUPPORTED, "%s: grid step kernel needs %d co-resident CTAs", cell_name(p->cell), pl.grid);
+    }
+    *out = pl;
+    return RK_OK;
+  }
+}
+
+rk_status cuda_fail(rk_handle* h, const rk_problem* p, const char* what, cudaError_t e) {
+  return fail(h, RK_ERR_CUDA, "%s: %s: %s (%s)", cell_name(p->cell), what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+rk_status grow(rk_handle* h, float** buf, size_t* cap, size_t need, const rk_problem* p, const char* what) {
+  if (*cap >= need) return RK_OK;
+  if (*buf) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, p, what, e);
+    cudaFree(*buf);
+    *buf = nullptr;
+    *cap = 0;
+  }
+  cudaError_t e = cudaMalloc(buf, need * sizeof(float));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *buf = nullptr;
+    return fail(h, RK_ERR_OOM, "%s: %s: cannot allocate %zu bytes of scratch", cell_name(p->cell), what,
+                need * sizeof(float));
+  }
+  *cap = need;
+  return RK_OK;
+}
+
+const void* tptr(const rk_tensor& t, int eb) {
+  return t.ptr ? static_cast<const void*>(static_cast<const char*>(t.ptr) + t.offset * eb) : nullptr;
+}
+void* tptr_mut(const rk_tensor& t, int eb) {
+  return t.ptr ? static_cast<void*>(static_cast<char*>(t.ptr) + t.offset * eb) : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t rk_version(void) { return 100; }
+
+rk_status rk_create(rk_handle** out, uint32_t flags) {
+  if (out == nullptr) return RK_ERR_ARG;
+  *out = new (std::nothrow) rk_handle();
+  if (*out == nullptr) return RK_ERR_OOM;
+  (*out)->flags = flags;
+  return RK_OK;
+}
+
+rk_status rk_destroy(rk_handle* h) {
+  if (h == nullptr) return RK_OK;
+  if (h->dev_ready) {
+    cudaDeviceSynchronize();
+    for (auto& ev : h->ev)
+      if (ev) cudaEventDestroy(ev);
+    cudaFree(h->status);
+    cudaFree(h->xw);
+    cudaFree(h->state);
+    cudaFree(h->host_arena);
+  }
+  delete h;
+  return RK_OK;
+}
+
+int64_t rk_xw_length(const rk_problem* p) {
+  if (validate_problem(nullptr, p) != RK_OK) return -1;
+  return xw_len(p);
+}
+
+int64_t rk_state_length(const rk_problem* p) {
+  if (validate_problem(nullptr, p) != RK_OK) return -1;
+  return state_len(p);
+}
+
+rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops) {
+  if (h == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  return validate_all(h, p, ops);
+}
+
+rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t len) {
+  if (h == nullptr || buf == nullptr || len <= 0) return RK_ERR_ARG;
+  rk_status st = validate_problem(h, p);
+  if (st != RK_OK) return st;
+  StepParams sp;
+  fill_params_problem(p, &sp);
+  StepPlan pl{};
+  int dev = 0;
+  const bool have_dev = cudaGetDevice(&dev) == cudaSuccess;
+  if (!have_dev) cudaGetLastError();
+  if (have_dev) {
+    if ((st = ensure_device(h)) != RK_OK) return st;
+  }
+  if (p->batch == 0 || p->hidden == 0) {
+    snprintf(buf, (size_t)len, "noop");
+    return RK_OK;
+  }
+  if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
+  snprintf(buf, (size_t)len, "proj=simt step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
+           pl.kind == rk::kStepCluster ? "cluster" : "grid", (int)pl.shape, pl.team_ctas, pl.J, pl.nb,
+           pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
+  return RK_OK;
+}
+
+rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, const rk_scratch* scratch,
+                    void* stream_ptr) {
+  if (h == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  rk_status st = validate_all(h, p, ops);
+  if (st != RK_OK) return st;
+  if (p->batch == 0 || p->hidden == 0) return RK_OK;  // nothing is recorded
+  if ((st = ensure_device(h)) != RK_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int eb = p->dtype == RK_F32 ? 4 : 2;
+
+  StepParams sp;
+  fill_params_problem(p, &sp);
+  StepPlan pl{};
+  if ((st = plan_step(h, p, &sp, &pl, true)) != RK_OK) return st;
+
+  // scratch: caller-placed or grown on demand
+  const int64_t need_xw = xw_len(p), need_state = state_len(p);
+  float* xw = nullptr;
+  float* state = nullptr;
+  if (scratch != nullptr && scratch->xw != nullptr) {
+    if (scratch->xw_offset < 0 || scratch->xw_offset > scratch->xw_length ||
+        scratch->xw_length - scratch->xw_offset < need_xw)
+      return fail(h, RK_ERR_SHAPE, "%s: xw scratch: offset %lld + %lld floats exceeds length %lld", cell_name(p->cell),
+                  (long long)scratch->xw_offset, (long long)need_xw, (long long)scratch->xw_length);
+    xw = scratch->xw + scratch->xw_offset;
+  } else {
+    if ((st = grow(h, &h->xw, &h->xw_cap, (size_t)std::max<int64_t>(need_xw, 1), p, "xw scratch")) != RK_OK) return st;
+    xw = h->xw;
+  }
+  if (scratch != nullptr && scratch->state != nullptr) {
+    if (scratch->state_offset < 0 || scratch->state_offset > scratch->state_length ||
+        scratch->state_length - scratch->state_offset < need_state)
+      return fail(h, RK_ERR_SHAPE, "%s: state scratch: offset %lld + %lld floats exceeds length %lld",
+                  cell_name(p->cell), (long long)scratch->state_offset, (long long)need_state,
+                  (long long)scratch->state_length);
+    state = scratch->state + scratch->state_offset;
+    if (reinterpret_cast<uintptr_t>(state) % 16 != 0)
+      return fail(h, RK_ERR_SHAPE, "%s: state scratch: base + offset must be 16-byte aligned", cell_name(p->cell));
+  } else {
+    if ((st = grow(h, &h->state, &h->state_cap, (size_t)need_state, p, "state scratch")) != RK_OK) return st;
+    state = h->state;
+  }
+
+  // 1. input projection of every step and direction
+  if (sp.T > 0 && need_xw > 0) {
+    rk::ProjParams pp{};
+    pp.M = (int)(p->seq * p->batch);
+    pp.N = sp.G * sp.H;
+    pp.K = (int)p->input;
+    pp.D = sp.D;
+    pp.X = tptr(ops->X, eb);
+    pp.W = tptr(ops->W, eb);
+    pp.Xw = xw;
+    pp.dtype = p->dtype;
+    if (h->profiling) cudaEventRecord(h->ev[0], stream);
+    cudaError_t e = rk::launch_projection_simt(pp, stream);
+    if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);
+    if (h->profiling) cudaEventRecord(h->ev[1], stream);
+    h->ev_proj = h->profiling;
+    h->launches += 1;
+  } else {
+    h->ev_proj = false;
+  }
+
+  // 2-4. state setup, steps and outputs in one persistent launch
+  sp.R = tptr(ops->R, eb);
+  sp.Bias = tptr(ops->B, eb);
+  sp.lens = static_cast<const int*>(tptr(ops->sequence_lens, 4));
+  sp.h0 = tptr(ops->initial_h, eb);
+  sp.c0 = tptr(ops->initial_c, eb);
+  sp.P = tptr(ops->P, eb);
+  sp.Y = tptr_mut(ops->Y, eb);
+  sp.Yh = tptr_mut(ops->Y_h, eb);
+  sp.Yc = tptr_mut(ops->Y_c, eb);
+  sp.xw = xw;
+  sp.counters = reinterpret_cast<unsigned*>(state);
+  sp.hglob = state + rk::kStateHeader;
+  sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
+  sp.status = h->status;
+  sp.timeout_ns = h->timeout_ns;
+  if (pl.kind == rk::kStepGrid) {
+    cudaError_t e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
+    if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
+  }
+  if (h->profiling) cudaEventRecord(h->ev[2], stream);
+  cudaError_t e;
+  switch (p->cell) {
+    case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(sp, pl, stream, nullptr)
+                                                  : rk::step_entry<0, true>(sp, pl, stream, nullptr); break;
+    case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(sp, pl, stream, nullptr)
+                                                 : rk::step_entry<1, true>(sp, pl, stream, nullptr); break;
+    default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(sp, pl, stream, nullptr)
+                                             : rk::step_entry<2, true>(sp, pl, stream, nullptr); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (e == cudaErrorCooperativeLaunchTooLarge)
+      return fail(h, RK_ERR_UNSUPPORTED, "%s: step kernel cannot be resident: %s", cell_name(p->cell),
+                  cudaGetErrorName(e));
+    return cuda_fail(h, p, "step kernel launch", e);
+  }
+  if (h->profiling) cudaEventRecord(h->ev[3], stream);
+  h->ev_step = h->profiling;
+  h->launches += 1;
+  return RK_OK;
+}
+
+rk_status rk_set_profiling(rk_handle* h, int32_t enabled) {
+  if (h == nullptr) return RK_ERR_ARG;
+  if (enabled) {
+    rk_status st = ensure_device(h);
+    if (st != RK_OK) return st;
+    for (auto& ev : h->ev) {
+      if (ev == nullptr) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) return fail(h, RK_ERR_CUDA, "recurrent: event create: %s", cudaGetErrorName(e));
+      }
+    }
+  }
+  h->profiling = enabled != 0;
+  h->ev_proj = h->ev_step = false;
+  return RK_OK;
+}
+
+rk_status rk_last_timings(rk_handle* h, float* projection_ms, float* step_ms) {
+  if (h == nullptr || projection_ms == nullptr || step_ms == nullptr) return RK_ERR_ARG;
+  *projection_ms = -1.0f;
+  *step_ms = -1.0f;
+  cudaError_t e = cudaSuccess;
+  if (h->ev_proj) {
+    e = cudaEventSynchronize(h->ev[1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(projection_ms, h->ev[0], h->ev[1]);
+  }
+  if (e == cudaSuccess && h->ev_step) {
+    e = cudaEventSynchronize(h->ev[3]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(step_ms, h->ev[2], h->ev[3]);
+  }
+  if (e != cudaSuccess) return fail(h, RK_ERR_CUDA, "recurrent: timings: %s", cudaGetErrorName(e));
+  return RK_OK;
+}
+
+rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* host_ops, void* stream_ptr) {
+  if (h == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  rk_status st = validate_all(h, p, host_ops);
+  if (st != RK_OK) return st;
+  if (p->batch == 0 || p->hidden == 0) return RK_OK;
+  if ((st = ensure_device(h)) != RK_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int eb = p->dtype == RK_F32 ? 4 : 2;
+  Extents ex;
+  extents_of(p, &ex);
+  struct Item {
+    const rk_tensor* src;
+    rk_tensor* dst;
+    int64_t bytes;
+    bool input;
+  };
+  rk_operands dev = {};
+  Item items[11] = {
+      {&host_ops->X, &dev.X, ex.X * eb, true},
+      {&host_ops->W, &dev.W, ex.W * eb, true},
+      {&host_ops->R, &dev.R, ex.R * eb, true},
+      {&host_ops->B, &dev.B, ex.B * eb, true},
+      {&host_ops->sequence_lens, &dev.sequence_lens, ex.lens * 4, true},
+      {&host_ops->initial_h, &dev.initial_h, ex.state * eb, true},
+      {&host_ops->initial_c, &dev.initial_c, ex.state * eb, true},
+      {&host_ops->P, &dev.P, ex.P * eb, true},
+      {&host_ops->Y, &dev.Y, ex.Y * eb, false},
+      {&host_ops->Y_h, &dev.Y_h, ex.state * eb, false},
+      {&host_ops->Y_c, &dev.Y_c, ex.state * eb, false},
+  };
+  size_t total = 0;
+  size_t offs[11];
+  for (int i = 0; i < 11; ++i) {
+    offs[i] = total;
+    if (items[i].src->ptr) total += (size_t)round_up(std::max<int64_t>(items[i].bytes, 1), 256);
+  }
+  if (h->host_arena_cap < total) {
+    if (h->host_arena) {
+      cudaDeviceSynchronize();
+      cudaFree(h->host_arena);
+      h->host_arena = nullptr;
+      h->host_arena_cap = 0;
+    }
+    cudaError_t e = cudaMalloc(&h->host_arena, total);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, RK_ERR_OOM, "%s: cannot allocate %zu bytes for host operands", cell_name(p->cell), total);
+    }
+    h->host_arena_cap = total;
+  }
+  for (int i = 0; i < 11; ++i) {
+    if (!items[i].src->ptr) continue;
+    const int elem = (i == 4) ? 4 : eb;
+    items[i].dst->ptr = h->host_arena + offs[i];
+    items[i].dst->offset = 0;
+    items[i].dst->length = items[i].bytes / elem;
+    if (items[i].input && items[i].bytes > 0) {
+      const char* src = static_cast<const char*>(items[i].src->ptr) + items[i].src->offset * elem;
+      cudaError_t e = cudaMemcpyAsync(items[i].dst->ptr, src, (size_t)items[i].bytes, cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) return cuda_fail(h, p, "host-to-device copy", e);
+    }
+  }
+  if ((st = rk_encode(h, p, &dev, nullptr, stream_ptr)) != RK_OK) return st;
+  for (int i = 8; i < 11; ++i) {
+    if (!items[i].src->ptr || items[i].bytes == 0) continue;
+    char* dstp = static_cast<char*>(items[i].src->ptr) + items[i].src->offset * eb;
+    cudaError_t e = cudaMemcpyAsync(dstp, items[i].dst->ptr, (size_t)items[i].bytes, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(h, p, "device-to-host copy", e);
+  }
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(h, p, "stream synchronize", e);
+  return RK_OK;
+}
+
+rk_status rk_status_poll(rk_handle* h, void* stream_ptr) {
+  if (h == nullptr) return RK_ERR_ARG;
+  if (!h->dev_ready) return RK_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int v = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
+  if (e != cudaSuccess) {
+    h->last_error = std::string("recurrent: status poll: ") + cudaGetErrorName(e);
+    return RK_ERR_CUDA;
+  }
+  if (v & 3) {
+    h->last_error = "recurrent: a bounded device wait timed out";
+    return RK_ERR_TIMEOUT;
+  }
+  return RK_OK;
+}
+
+rk_status rk_set_wait_limit(rk_handle* h, int64_t limit) {
+  if (h == nullptr || limit < 1) return RK_ERR_ARG;
+  h->timeout_ns = limit;
+  return RK_OK;
+}
+
+rk_status rk_selftest_timeout(rk_handle* h, void* stream_ptr, int64_t timeout_ns) {
+  if (h == nullptr || timeout_ns < 1) return RK_ERR_ARG;
+  rk_status st = ensure_device(h);
+  if (st != RK_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  rk_problem dummy = {};
+  if ((st = grow(h, &h->state, &h->state_cap, rk::kStateHeader, &dummy, "state scratch")) != RK_OK) return st;
+  cudaError_t e = cudaMemsetAsync(h->state, 0, sizeof(unsigned), stream);
+  if (e == cudaSuccess) e = rk::launch_selftest_timeout(reinterpret_cast<unsigned*>(h->state), h->status, timeout_ns, stream);
+  if (e != cudaSuccess) return fail(h, RK_ERR_CUDA, "recurrent: self-test launch: %s", cudaGetErrorName(e));
+  h->launches += 1;
+  return RK_OK;
+}
+
+const char* rk_last_error(const rk_handle* h) { return h ? h->last_error.c_str() : "null handle"; }
+
+uint64_t rk_launch_count(const rk_handle* h) { return h ? h->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// rk_internal.h -- structures shared between the host side of the library
+// (validation, planning, scratch) and the CUDA kernels.  Not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rk {
+
+constexpr int kMaxActs = 6;
+constexpr int kKChunk = 128;      // k is padded to a multiple of 32 lanes x 4 floats
+constexpr int kStateHeader = 256; // floats reserved at the start of the state scratch
+                                  // for the grid step kernel's barrier counters
+
+struct ActSlot {
+  int kind;
+  float alpha, beta;
+};
+
+// Which persistent step kernel runs the recurrence.
+enum StepKind : int {
+  kStepCluster = 0,  // a team is one thread-block cluster; h exchanged through DSMEM
+  kStepGrid = 1,     // a team spans many SMs; h exchanged through L2 and a bounded barrier
+};
+
+// Register tile of the step kernel's R.h product: rows per warp x batch rows.
+enum StepShape : int {
+  kShapeR8B1 = 0,  // 8 rows x 1 batch row
+  kShapeR4B8 = 1,  // 4 rows x 8 batch rows
+  kShapeR8B4 = 2,  // 8 rows x 4 batch rows
+};
+
+struct StepParams {
+  // problem
+  int cell, dtype, direction, layout;
+  int S, N, I, H, D, G;
+  int T;               // steps the loop runs (max_length or seq)
+  float clip;          // > 0: on
+  int input_forget, lbr;
+  int generic_acts;    // 0: ONNX defaults compiled in
+  ActSlot acts[kMaxActs];
+  // operands (element offsets already applied)
+  const void* R;
+  const void* Bias;    // may be null
+  const int* lens;     // may be null
+  const void* h0;      // may be null
+  const void* c0;      // may be null
+  const void* P;       // may be null
+  void* Y;             // may be null
+  void* Yh;            // may be null
+  void* Yc;            // may be null
+  const float* xw;     // [D, S*N, G*H]
+  // plan
+  int team_ctas;       // CTAs per team (cluster size for kStepCluster)
+  int J;               // hidden units per CTA
+  int KP;              // H padded to a multiple of kKChunk
+  int nb;              // batch rows per team
+  int teams_per_dir;
+  int rows_pad;        // rows of R held per CTA (warps x rows per warp)
+  int nbc;             // batch rows per h chunk in shared memory
+  // grid exchange (kStepGrid) and status
+  float* hglob;        // [2][D*N][KP]
+  float* rhglob;       // [D*N][KP]
+  unsigned* counters;  // one per team, zero at launch
+  int* status;         // device status word (bit 1: timeout)
+  long long timeout_ns;
+};
+
+struct ProjParams {
+  int M, N, K, D;      // Xw[d] (M x N) = X (M x K) . W[d]^T (W[d] is N x K)
+  const void* X;
+  const void* W;
+  float* Xw;
+  int dtype;
+};
+
+struct StepPlan {
+  StepKind kind;
+  StepShape shape;
+  int threads;
+  int team_ctas, J, KP, nb, teams_per_dir, rows_pad, nbc;
+  size_t smem;
+  int grid;
+};
+
+// Launchers (defined in the .cu files).  Each returns a cudaError_t.
+cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s);
+// Step kernel for one cell and exchange kind.  With resident_teams != nullptr
+// nothing is launched: the kernel is opted into the plan's shared memory /
+// cluster size and the number of teams that can be resident at once is
+// returned through the pointer.
+template <int CELL, bool GRID>
+cudaError_t step_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
+// Dynamic shared memory (bytes) the step kernel needs for a plan.
+size_t step_smem_for(const StepParams& p, const StepPlan& plan);
+// Self-test of the bounded waits (see rk_selftest_timeout).
+cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);
+
+}  // namespace rk

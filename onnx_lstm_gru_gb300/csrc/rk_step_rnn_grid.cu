@@ -1,0 +1,6 @@
+// Step-kernel instantiations: RNN cell, grid exchange.
+#include "rk_step_launch.cuh"
+
+namespace rk {
+template cudaError_t step_entry<2, true>(const StepParams&, const StepPlan&, cudaStream_t, int*);
+}  // namespace rk

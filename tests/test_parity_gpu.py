@@ -1,0 +1,361 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Every case compares Y, Y_h and Y_c element by element on the same seeded
+inputs: |gpu - oracle| <= tol or <= tol * |oracle| with tol 1e-4 for float32
+and 5e-3 for Half tensors (float32 accumulation and state, outputs rounded to
+half).  Positions past a row's length must be exactly 0, bytes around every
+output (sentinels) must be untouched, and two runs must give the same bits.
+
+The test matrix follows the one the recurrent-layers page lists: every cell x
+direction x layout with option sets (bias, lengths including 0, initial state,
+peepholes, clip, input_forget, linear_before_reset), every activation in every
+slot of both directions, odd offsets with sentinels around every output, empty
+sequence and batch, hidden sizes that do not divide the tiles, batches above
+eight, and both step kernels (cluster and grid).  The named workloads run at
+full size; the largest one is checked on sampled batch rows (rows are
+independent, so the oracle can run on those rows alone).
+"""
+import numpy as np
+import pytest
+import torch
+
+import onnx_lstm_gru_gb300 as rk
+import oracle
+from onnx_lstm_gru_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "f16": 5e-3}
+SENTINEL = 1234.5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    rk.build()
+    rk.load()
+    yield
+    torch.cuda.synchronize()
+
+
+_layers = {}
+
+
+def layer(flags=0):
+    if flags not in _layers:
+        _layers[flags] = rk.RecurrentLayer(flags)
+    return _layers[flags]
+
+
+def torch_dtype(pr):
+    return torch.float32 if pr.dtype == "f32" else torch.float16
+
+
+def to_device(arr, offset, dtype):
+    """Place arr at element `offset` inside a larger device buffer."""
+    flat = torch.from_numpy(np.ascontiguousarray(arr).reshape(-1))
+    if dtype is not None:
+        flat = flat.to(dtype)
+    if offset == 0:
+        return flat.cuda()
+    buf = torch.full((flat.numel() + offset + 3,), 7.0 if flat.is_floating_point() else 7, dtype=flat.dtype)
+    buf[offset:offset + flat.numel()] = flat
+    return (buf.cuda(), offset)
+
+
+def run_gpu(pr, inputs, outputs=("Y", "Y_h", "Y_c"), in_off=0, out_off=0, flags=0, scratch=None):
+    dt = torch_dtype(pr)
+    shp = pr.shapes()
+    args = {}
+    for k, v in inputs.items():
+        args[k] = to_device(v, in_off, None if k == "sequence_lens" else dt)
+    outs = {}
+    pad = max(out_off, 8)
+    for name in outputs:
+        if name == "Y_c" and pr.cell != "lstm":
+            continue
+        n = int(np.prod(shp[name]))
+        buf = torch.full((n + 2 * pad,), SENTINEL, dtype=dt, device="cuda")
+        outs[name] = (buf, pad, n)
+        args[name] = (buf, pad)
+    L = layer(flags)
+    L.encode(pr, scratch=scratch, **args)
+    torch.cuda.synchronize()
+    L.poll()
+    res = {}
+    for name, (buf, off, n) in outs.items():
+        host = buf.float().cpu().numpy().astype(np.float64)
+        assert np.all(host[:off] == SENTINEL) and np.all(host[off + n:] == SENTINEL), f"{name}: sentinel overwritten"
+        res[name] = host[off:off + n].reshape(shp[name])
+        res[name + "_raw"] = buf[off:off + n].clone()
+    return res
+
+
+def spec_of(pr):
+    return dict(cell=pr.cell, direction=pr.direction, layout=pr.layout, seq=pr.seq, batch=pr.batch,
+                input=pr.input, hidden=pr.hidden, clip=pr.clip, input_forget=pr.input_forget,
+                linear_before_reset=pr.linear_before_reset,
+                activations=list(pr.activations) if pr.activations else None)
+
+
+def run_oracle(pr, inputs):
+    args = {k: (v.astype(np.float64) if k != "sequence_lens" else v) for k, v in inputs.items()}
+    return oracle.layer(spec_of(pr), **args)
+
+
+def past_length_mask(pr, lens):
+    """True at Y positions t >= len (or t >= max_length) of their row."""
+    S, N, D, H = pr.seq, pr.batch, pr.num_directions, pr.hidden
+    L = np.full(N, S) if lens is None else np.clip(lens, 0, S)
+    t = np.arange(S)[:, None]
+    m = t >= L[None, :]                              # [S, N]
+    m = np.broadcast_to(m[:, None, :, None], (S, D, N, H))
+    return m if pr.layout == 0 else m.transpose(2, 0, 1, 3)
+
+
+def compare(pr, got, ref, lens=None):
+    tol = TOL[pr.dtype]
+    for name in ref:
+        if name not in got:
+            continue
+        g, r = got[name], ref[name]
+        assert g.shape == r.shape, name
+        nan_g, nan_r = np.isnan(g), np.isnan(r)
+        assert np.array_equal(nan_g, nan_r), f"{name}: NaN positions differ"
+        d = np.abs(g - r)[~nan_r]
+        rr = np.abs(r)[~nan_r]
+        ok = (d <= tol) | (d <= tol * rr)
+        if not ok.all():
+            i = np.argmax(np.where(ok, 0, d))
+            raise AssertionError(f"{name}: {int((~ok).sum())} of {ok.size} elements off; worst |d|={d.flat[i]:.3g} "
+                                 f"at ref={r[~nan_r].flat[i]:.6g}")
+    if "Y" in got and pr.seq > 0:
+        m = past_length_mask(pr, lens)
+        assert np.all(got["Y"][m] == 0.0), "Y must be exactly 0 past the length"
+
+
+def rand_inputs(pr, seed, lens=None, init=True, peep=False, bias=True, scale=0.5):
+    rng = np.random.default_rng(seed)
+    shp = pr.shapes()
+    dt = np.float32 if pr.dtype == "f32" else np.float16
+    a = {"X": rng.uniform(-1, 1, shp["X"]).astype(dt),
+         "W": rng.uniform(-scale, scale, shp["W"]).astype(dt),
+         "R": rng.uniform(-scale, scale, shp["R"]).astype(dt)}
+    if bias:
+        a["B"] = rng.uniform(-scale, scale, shp["B"]).astype(dt)
+    if peep and pr.cell == "lstm":
+        a["P"] = rng.uniform(-scale, scale, shp["P"]).astype(dt)
+    if init:
+        a["initial_h"] = rng.uniform(-1, 1, shp["initial_h"]).astype(dt)
+        if pr.cell == "lstm":
+            a["initial_c"] = rng.uniform(-1, 1, shp["initial_c"]).astype(dt)
+    if lens is not None:
+        a["sequence_lens"] = np.asarray(lens, dtype=np.int32)
+    return a
+
+
+# ------------------------------------------------------------------ the named workloads
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if n != "bilstm_s512_b64_i1024_h1024_f16"])
+def test_workload_full_size(name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    got = run_gpu(w.problem, inp, outputs=w.outputs)
+    ref = run_oracle(w.problem, inp)
+    compare(w.problem, got, ref, inp.get("sequence_lens"))
+    again = run_gpu(w.problem, inp, outputs=w.outputs)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
+
+
+def test_large_half_workload_sampled_rows():
+    """bi-LSTM 512 x 64 x 1024 x 1024 Half, run whole on the GPU; batch rows
+    0, 29 and 63 re-run through the oracle alone (rows are independent)."""
+    w = workloads.WORKLOADS["bilstm_s512_b64_i1024_h1024_f16"]
+    pr = w.problem
+    inp = workloads.make_inputs(w)
+    got = run_gpu(pr, inp)
+    rows = [0, 29, 63]
+    sub = rk.Problem(pr.cell, seq=pr.seq, batch=len(rows), input=pr.input, hidden=pr.hidden,
+                     direction=pr.direction, dtype=pr.dtype, layout=pr.layout)
+    sinp = dict(inp)
+    sinp["X"] = inp["X"][:, rows]
+    sinp["sequence_lens"] = inp["sequence_lens"][rows]
+    ref = run_oracle(sub, sinp)
+    gsub = {"Y": got["Y"][:, :, rows], "Y_h": got["Y_h"][:, rows], "Y_c": got["Y_c"][:, rows]}
+    compare(sub, gsub, ref, sinp["sequence_lens"])
+    assert np.all(np.isfinite(got["Y"]))
+
+
+# ------------------------------------------------------------------ the option matrix
+
+CASES = []
+for cell in ("lstm", "gru", "rnn"):
+    for direction in ("forward", "reverse", "bidirectional"):
+        for layout in (0, 1):
+            for opts in ("plain", "full"):
+                CASES.append((cell, direction, layout, opts))
+
+
+@pytest.mark.parametrize("kernel", ["cluster", "grid"])
+@pytest.mark.parametrize("cell,direction,layout,opts", CASES)
+def test_option_matrix(cell, direction, layout, opts, kernel):
+    S, N, I, H = 7, 3, 5, 40
+    kw = {}
+    lens = None
+    if opts == "full":
+        lens = [7, 0, 4]
+        kw = dict(clip=0.9)
+        if cell == "lstm":
+            kw["input_forget"] = 1
+    pr = rk.Problem(cell, seq=S, batch=N, input=I, hidden=H, direction=direction, layout=layout, **kw)
+    for lbr in ((0, 1) if cell == "gru" else (0,)):
+        pr.linear_before_reset = lbr
+        inp = rand_inputs(pr, seed=100 + len(cell) + layout, lens=lens, init=opts == "full",
+                          peep=opts == "full", bias=opts == "full")
+        flags = rk.RK_FORCE_GRID_STEP if kernel == "grid" else 0
+        got = run_gpu(pr, inp, flags=flags)
+        ref = run_oracle(pr, inp)
+        compare(pr, got, ref, lens)
+
+
+ALL_ACTS = [("sigmoid", 0, 0), ("tanh", 0, 0), ("relu", 0, 0), ("affine", 0.7, -0.2), ("leakyrelu", 0.15, 0),
+            ("thresholdedrelu", 0.3, 0), ("scaledtanh", 1.3, 0.6), ("hardsigmoid", 0.25, 0.45), ("elu", 0.8, 0),
+            ("softsign", 0, 0), ("softplus", 0, 0)]
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "rnn"])
+@pytest.mark.parametrize("act", ALL_ACTS, ids=[a[0] for a in ALL_ACTS])
+def test_every_activation_in_every_slot(cell, act):
+    A = {"lstm": 3, "gru": 2, "rnn": 1}[cell]
+    defaults = {"lstm": [("sigmoid", 0, 0), ("tanh", 0, 0), ("tanh", 0, 0)],
+                "gru": [("sigmoid", 0, 0), ("tanh", 0, 0)], "rnn": [("tanh", 0, 0)]}[cell] * 2
+    for slot in range(2 * A):
+        acts = list(defaults)
+        acts[slot] = act
+        pr = rk.Problem(cell, seq=5, batch=2, input=3, hidden=12, direction="bidirectional",
+                        activations=acts, clip=4.0)
+        inp = rand_inputs(pr, seed=7 + slot, lens=[5, 3], peep=True)
+        got = run_gpu(pr, inp)
+        compare(pr, got, run_oracle(pr, inp), [5, 3])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_odd_offsets_and_sentinels(dtype):
+    pr = rk.Problem("lstm", seq=6, batch=3, input=7, hidden=36, direction="bidirectional", dtype=dtype, layout=1)
+    inp = rand_inputs(pr, seed=3, lens=[6, 2, 5], peep=True)
+    got = run_gpu(pr, inp, in_off=3, out_off=5)
+    compare(pr, got, run_oracle(pr, inp), [6, 2, 5])
+
+
+def test_empty_sequence_and_batch():
+    pr = rk.Problem("lstm", seq=0, batch=3, input=4, hidden=20, direction="bidirectional")
+    inp = rand_inputs(pr, seed=5)
+    got = run_gpu(pr, inp, outputs=("Y_h", "Y_c"))
+    np.testing.assert_array_equal(got["Y_h"], inp["initial_h"].astype(np.float64))
+    np.testing.assert_array_equal(got["Y_c"], inp["initial_c"].astype(np.float64))
+    pr0 = rk.Problem("gru", seq=5, batch=0, input=4, hidden=20)
+    before = layer().launches()
+    run_gpu(pr0, rand_inputs(pr0, seed=6, init=False))  # sentinels checked inside
+    assert layer().launches() == before  # Batch = 0 records nothing
+
+
+@pytest.mark.parametrize("kernel", ["cluster", "grid"])
+@pytest.mark.parametrize("H,N", [(100, 11), (37, 9), (130, 2), (513, 1)])
+def test_ragged_hidden_and_large_batch(H, N, kernel):
+    pr = rk.Problem("gru", seq=6, batch=N, input=9, hidden=H, direction="bidirectional", linear_before_reset=0)
+    lens = list(np.random.default_rng(H).integers(0, 7, N))
+    inp = rand_inputs(pr, seed=H + N, lens=lens, scale=0.2)
+    flags = rk.RK_FORCE_GRID_STEP if kernel == "grid" else 0
+    compare(pr, run_gpu(pr, inp, flags=flags), run_oracle(pr, inp), lens)
+
+
+def test_max_length_shortens_loop():
+    pr = rk.Problem("lstm", seq=9, batch=3, input=4, hidden=24, direction="bidirectional", max_length=5)
+    inp = rand_inputs(pr, seed=9, lens=[5, 2, 0])
+    compare(pr, run_gpu(pr, inp), run_oracle(pr, inp), [5, 2, 0])
+
+
+def test_nan_passes_through_clip():
+    pr = rk.Problem("rnn", seq=1, batch=2, input=1, hidden=1, activations=[("affine", 1.0, 0.0)], clip=1.0)
+    inp = {"X": np.array([np.nan, 0.5], dtype=np.float32).reshape(1, 2, 1),
+           "W": np.ones((1, 1, 1), np.float32), "R": np.zeros((1, 1, 1), np.float32)}
+    got = run_gpu(pr, inp, outputs=("Y",))
+    assert np.isnan(got["Y"][0, 0, 0, 0]) and got["Y"][0, 0, 1, 0] == 0.5
+
+
+def test_getting_started_rows_exact():
+    """RNN with Affine(1, 0), R = 0: Y is the projection, the pages' example rows."""
+    A = np.arange(1, 9, dtype=np.float32).reshape(4, 1, 2)
+    Bm = np.array([[1, 0, 2], [0, 1, 3]], dtype=np.float32)
+    for dtype in ("f32", "f16"):
+        pr = rk.Problem("rnn", seq=4, batch=1, input=2, hidden=3, activations=[("affine", 1.0, 0.0)], dtype=dtype)
+        dt = np.float32 if dtype == "f32" else np.float16
+        inp = {"X": A.astype(dt), "W": Bm.T.copy()[None].astype(dt), "R": np.zeros((1, 3, 3), dt)}
+        got = run_gpu(pr, inp, outputs=("Y",))
+        np.testing.assert_array_equal(got["Y"].reshape(4, 3), [[1, 2, 8], [3, 4, 18], [5, 6, 28], [7, 8, 38]])
+
+
+# ------------------------------------------------------------------ boundary behaviour
+
+def test_launches_do_not_grow_with_seq():
+    L = layer()
+    for S in (4, 64):
+        pr = rk.Problem("lstm", seq=S, batch=1, input=8, hidden=32)
+        inp = rand_inputs(pr, seed=S)
+        before = L.launches()
+        run_gpu(pr, inp)
+        assert L.launches() - before == 2  # projection + one persistent step kernel
+
+
+def test_caller_scratch_in_one_arena_is_bitwise_equal():
+    w = workloads.WORKLOADS["bilstm_s80_b1_i256_h256_f32"]
+    inp = workloads.make_inputs(w)
+    base = run_gpu(w.problem, inp)
+    c = w.problem.to_c()
+    nx, ns = rk.rk_xw_length(c), rk.rk_state_length(c)
+    arena = torch.empty(nx + ns + 64, dtype=torch.float32, device="cuda")
+    sc = rk.rk_scratch(arena.data_ptr(), 17, nx + 17, arena.data_ptr(), nx + 40, nx + ns + 64)
+    got = run_gpu(w.problem, inp, scratch=sc)
+    for k in ("Y_raw", "Y_h_raw", "Y_c_raw"):
+        assert torch.equal(base[k], got[k])
+
+
+def test_host_buffer_entry_matches_device_entry():
+    w = workloads.WORKLOADS["bigru_s128_b8_i512_h512_f16_lbr0"]
+    pr = w.problem
+    inp = workloads.make_inputs(w)
+    dev = run_gpu(pr, inp, outputs=("Y", "Y_h"))
+    shp = pr.shapes()
+    Y = np.zeros(shp["Y"], np.float16)
+    Yh = np.zeros(shp["Y_h"], np.float16)
+    layer().encode_host(pr, Y=Y, Y_h=Yh, **inp)
+    np.testing.assert_array_equal(Y.astype(np.float64), dev["Y"])
+    np.testing.assert_array_equal(Yh.astype(np.float64), dev["Y_h"])
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    L = rk.RecurrentLayer()
+    s = torch.cuda.current_stream()
+    assert rk.rk_selftest_timeout(L.handle, s.cuda_stream, 200_000) == rk.RK_OK
+    assert rk.rk_status_poll(L.handle, s.cuda_stream) == rk.RK_ERR_TIMEOUT
+    assert rk.rk_status_poll(L.handle, s.cuda_stream) == rk.RK_OK  # cleared
+    # the context is still usable
+    pr = rk.Problem("rnn", seq=3, batch=2, input=2, hidden=8)
+    inp = rand_inputs(pr, seed=1)
+    L.encode(pr, X=torch.from_numpy(inp["X"]).cuda(), W=torch.from_numpy(inp["W"]).cuda(),
+             R=torch.from_numpy(inp["R"]).cuda(), B=torch.from_numpy(inp["B"]).cuda())
+    L.poll()
+    L.close()
+
+
+def test_validation_error_launches_nothing():
+    L = layer()
+    pr = rk.Problem("gru", seq=3, batch=2, input=2, hidden=8)
+    X = torch.zeros(3 * 2 * 2, device="cuda")
+    before = L.launches()
+    with pytest.raises(rk.RkError) as e:
+        L.encode(pr, X=X, W=torch.zeros(3 * 8 * 2, device="cuda"), R=torch.zeros(5, device="cuda"))
+    assert e.value.code == rk.RK_ERR_SHAPE and "GRU: R:" in e.value.message
+    assert L.launches() == before
