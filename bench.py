@@ -114,7 +114,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, uuid=None):
-        self.uuid = uuid
+        self.uuid = str(uuid) if uuid is not None else None
         self.proc = None
 
     def start(self):
@@ -138,11 +138,13 @@ class ClockSampler:
         rows = []
         for line in out.splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            if self.uuid and self.uuid not in parts[1]:
-                continue
-            rows.append(parts)
+            if len(parts) >= 10:
+                rows.append(parts)
+        mine = [r for r in rows if self.uuid and self.uuid in r[1]]
+        if mine:
+            rows = mine
+        elif len({r[0] for r in rows}) > 1:
+            rows = [r for r in rows if r[0] == rows[0][0]]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]

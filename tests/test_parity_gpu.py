@@ -26,7 +26,7 @@ from onnx_lstm_gru_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "f16": 5e-3}
-SENTINEL = 1234.5
+SENTINEL = -777.0  # exactly representable in float32 and in binary16
 
 
 @pytest.fixture(scope="module", autouse=True)
