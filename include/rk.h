@@ -194,6 +194,31 @@ rk_status rk_set_wait_limit(rk_handle* h, int64_t limit);
  * returns RK_ERR_TIMEOUT.  Used to test the give-up path without a hang. */
 rk_status rk_selftest_timeout(rk_handle* h, void* stream, int64_t timeout_ns);
 
+/* The layer of rk_encode, for callers that cannot allocate device memory:
+ * a runtime whose memory planner owns every device allocation and allows no
+ * new one after start-up, a process with a fixed device-memory budget, or
+ * code that must not pay the device-wide synchronisation cudaFree can imply.
+ * The pages have no counterpart of this entry point.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Its scratch
+ * (projection Xw plus the step kernel's exchange buffers, barrier counters
+ * and status word) is a fixed 16 MiB float32 array inside the library, which
+ * every GPU that loads the library holds until the process exits.  A layer
+ * needing more than 4 Mi floats (rk_state_length rounded up to 64, plus
+ * rk_xw_length) is rejected with RK_ERR_UNSUPPORTED and a message giving both
+ * numbers; nothing is launched then.  The caller passes inputs and outputs as
+ * for rk_encode (device pointers); h holds only host-side state.
+ *
+ * The first call on each device takes the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * which keeps the previous call's contents: the call clears what must start
+ * at zero (barrier counters, status word).  Calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on the array and give
+ * undefined results: order them on one stream.  A device wait that gives up
+ * is not reported to rk_status_poll on this path. */
+rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands* ops, void* stream);
+
 /* Kernel timing for measurement: with enabled != 0 every later encode records
  * CUDA events (on its stream) around its projection launch and its step
  * launch; rk_last_timings then waits for them and returns the two durations

@@ -22,7 +22,7 @@ __all__ = [
     "rk_create", "rk_destroy", "rk_encode", "rk_encode_host", "rk_validate", "rk_xw_length",
     "rk_state_length", "rk_status_poll", "rk_set_wait_limit", "rk_last_error", "rk_launch_count",
     "rk_describe_plan", "rk_version", "rk_selftest_timeout", "rk_set_profiling", "rk_last_timings",
-    "RK_OK", "RK_ERR_SHAPE", "RK_ERR_UNSUPPORTED", "RK_ERR_CUDA", "RK_ERR_TIMEOUT", "RK_ERR_OOM", "RK_ERR_ARG",
+    "rk_encode_noalloc", "RK_OK", "RK_ERR_SHAPE", "RK_ERR_UNSUPPORTED", "RK_ERR_CUDA", "RK_ERR_TIMEOUT", "RK_ERR_OOM", "RK_ERR_ARG",
     "RK_FORCE_SIMT_PROJECTION", "RK_FORCE_GRID_STEP", "EXPORTED_SYMBOLS",
 ]
 
@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = [
     "rk_version", "rk_create", "rk_destroy", "rk_xw_length", "rk_state_length", "rk_validate",
     "rk_encode", "rk_encode_host", "rk_status_poll", "rk_set_wait_limit", "rk_last_error",
     "rk_launch_count", "rk_describe_plan", "rk_selftest_timeout", "rk_set_profiling", "rk_last_timings",
+    "rk_encode_noalloc",
 ]
 
 
@@ -118,6 +119,7 @@ def load(path: Optional[str] = None):
         "rk_describe_plan": (ctypes.c_int32, [H, P, ctypes.c_char_p, ctypes.c_int64]),
         "rk_selftest_timeout": (ctypes.c_int32, [H, ctypes.c_void_p, ctypes.c_int64]),
         "rk_set_profiling": (ctypes.c_int32, [H, ctypes.c_int32]),
+        "rk_encode_noalloc": (ctypes.c_int32, [H, P, O, ctypes.c_void_p]),
         "rk_last_timings": (ctypes.c_int32, [H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
@@ -162,6 +164,12 @@ def rk_encode(handle: int, problem: rk_problem, ops: rk_operands, scratch: Optio
               stream: int) -> int:
     return load().rk_encode(handle, ctypes.byref(problem), ctypes.byref(ops),
                             ctypes.byref(scratch) if scratch is not None else None, stream)
+
+
+def rk_encode_noalloc(handle: int, problem: rk_problem, ops: rk_operands, stream: int) -> int:
+    """rk_encode with the scratch in the library's fixed 16 MiB device array:
+    for callers that cannot allocate device memory.  No allocation happens."""
+    return load().rk_encode_noalloc(handle, ctypes.byref(problem), ctypes.byref(ops), stream)
 
 
 def rk_encode_host(handle: int, problem: rk_problem, ops: rk_operands, stream: int) -> int:

@@ -541,6 +541,93 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
   return RK_OK;
 }
 
+// The layer with its scratch in the library's fixed device array instead of
+// memory from cudaMalloc, for callers that cannot allocate (see rk.h).
+rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands* ops, void* stream_ptr) {
+  if (h == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  rk_status st = validate_all(h, p, ops);
+  if (st != RK_OK) return st;
+  if (p->batch == 0 || p->hidden == 0) return RK_OK;  // nothing is recorded
+  const int64_t need_state = round_up(state_len(p), 64), need_xw = xw_len(p);
+  if (need_state + need_xw > rk::kNoAllocScratchFloats)
+    return fail(h, RK_ERR_UNSUPPORTED,
+                "%s: no-alloc scratch holds %lld floats (16 MiB); this layer needs %lld (state %lld + xw %lld)",
+                cell_name(p->cell), (long long)rk::kNoAllocScratchFloats, (long long)(need_state + need_xw),
+                (long long)need_state, (long long)need_xw);
+  float* scratch = nullptr;
+  int* status = nullptr;
+  cudaError_t e = rk::noalloc_scratch(&scratch, &status);
+  if (e != cudaSuccess) return cuda_fail(h, p, "no-alloc scratch set-up", e);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int eb = p->dtype == RK_F32 ? 4 : 2;
+  // planning needs the device's SM count and shared-memory limit, not a status word
+  rk_handle plan_h;
+  plan_h.flags = h->flags;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan_h.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan_h.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return cuda_fail(h, p, "device query", e);
+  StepParams sp;
+  fill_params_problem(p, &sp);
+  StepPlan pl{};
+  if ((st = plan_step(&plan_h, p, &sp, &pl, true)) != RK_OK) {
+    h->last_error = plan_h.last_error;
+    return st;
+  }
+  float* state = scratch;            // 256-byte aligned start of the array
+  float* xw = scratch + need_state;  // after the state region
+  if (sp.T > 0 && need_xw > 0) {
+    rk::ProjParams pp{};
+    pp.M = (int)(p->seq * p->batch);
+    pp.N = sp.G * sp.H;
+    pp.K = (int)p->input;
+    pp.D = sp.D;
+    pp.X = tptr(ops->X, eb);
+    pp.W = tptr(ops->W, eb);
+    pp.Xw = xw;
+    pp.dtype = p->dtype;
+    e = rk::launch_projection_simt(pp, stream);
+    if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);
+    h->launches += 1;
+  }
+  sp.R = tptr(ops->R, eb);
+  sp.Bias = tptr(ops->B, eb);
+  sp.lens = static_cast<const int*>(tptr(ops->sequence_lens, 4));
+  sp.h0 = tptr(ops->initial_h, eb);
+  sp.c0 = tptr(ops->initial_c, eb);
+  sp.P = tptr(ops->P, eb);
+  sp.Y = tptr_mut(ops->Y, eb);
+  sp.Yh = tptr_mut(ops->Y_h, eb);
+  sp.Yc = tptr_mut(ops->Y_c, eb);
+  sp.xw = xw;
+  sp.counters = reinterpret_cast<unsigned*>(state);
+  sp.hglob = state + rk::kStateHeader;
+  sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
+  sp.status = status;
+  sp.timeout_ns = h->timeout_ns;
+  // the array keeps the previous call's contents: the barrier counters and
+  // the status word must start at zero
+  e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return cuda_fail(h, p, "scratch reset", e);
+  switch (p->cell) {
+    case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(sp, pl, stream, nullptr)
+                                                  : rk::step_entry<0, true>(sp, pl, stream, nullptr); break;
+    case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(sp, pl, stream, nullptr)
+                                                 : rk::step_entry<1, true>(sp, pl, stream, nullptr); break;
+    default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(sp, pl, stream, nullptr)
+                                             : rk::step_entry<2, true>(sp, pl, stream, nullptr); break;
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(h, p, "step kernel launch", e);
+  }
+  h->launches += 1;
+  return RK_OK;
+}
+
 rk_status rk_set_profiling(rk_handle* h, int32_t enabled) {
   if (h == nullptr) return RK_ERR_ARG;
   if (enabled) {

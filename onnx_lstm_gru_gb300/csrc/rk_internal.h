@@ -93,6 +93,11 @@ template <int CELL, bool GRID>
 cudaError_t step_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
 // Dynamic shared memory (bytes) the step kernel needs for a plan.
 size_t step_smem_for(const StepParams& p, const StepPlan& plan);
+// Fixed scratch of rk_encode_noalloc: floats per GPU, and the device
+// addresses of the array and its status word for the current device (taken
+// with cudaGetSymbolAddress on the first call for each device).
+constexpr long long kNoAllocScratchFloats = 4LL << 20;  // 16 MiB
+cudaError_t noalloc_scratch(float** scratch, int** status);
 // Self-test of the bounded waits (see rk_selftest_timeout).
 cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);
 
