@@ -349,6 +349,8 @@ def run_gb300(args):
     tot_len = pr.seq * pr.batch if lens is None else int(_np.clip(lens, 0, pr.seq).sum())
     step_flops = 2.0 * tot_len * G * H * H * D
     proj_flops = 2.0 * pr.seq * pr.batch * pr.input * G * H * D
+    if proj_ms <= 0.0:  # projection fused into the step kernel
+        step_flops += proj_flops
     dominant = "step" if step_ms >= proj_ms else "projection"
     kflops, kms = (step_flops, step_ms) if dominant == "step" else (proj_flops, proj_ms)
     achieved = kflops / (kms * 1e-3) / 1e12

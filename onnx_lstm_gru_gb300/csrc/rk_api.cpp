@@ -230,8 +230,28 @@ void fill_params_problem(const rk_problem* p, StepParams* sp) {
   sp->KP = (int)kp_of(p);
 }
 
-// Step-kernel plan.  Cluster kernel when R fits one cluster's shared memory,
-// else the grid kernel.  `check` asks the occupancy API (needs a device).
+// Launch (or, with resident != nullptr, size) the step kernel of a plan.
+cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl, cudaStream_t stream, int* resident) {
+  if (pl.kind == rk::kStepClusterFast) {
+    switch (cell) {
+      case RK_LSTM: return rk::step_fast_entry<0>(sp, pl, stream, resident);
+      case RK_GRU: return rk::step_fast_entry<1>(sp, pl, stream, resident);
+      default: return rk::step_fast_entry<2>(sp, pl, stream, resident);
+    }
+  }
+  const bool grid = pl.kind == rk::kStepGrid;
+  switch (cell) {
+    case RK_LSTM: return grid ? rk::step_entry<0, true>(sp, pl, stream, resident) : rk::step_entry<0, false>(sp, pl, stream, resident);
+    case RK_GRU: return grid ? rk::step_entry<1, true>(sp, pl, stream, resident) : rk::step_entry<1, false>(sp, pl, stream, resident);
+    default: return grid ? rk::step_entry<2, true>(sp, pl, stream, resident) : rk::step_entry<2, false>(sp, pl, stream, resident);
+  }
+}
+
+// Step-kernel plan, in order of preference: the fused one-row-per-cluster
+// kernel (R in registers) when a row's hidden units fit 16 CTAs of <= 32
+// units and R's chunks fit the registers; else the cluster kernel when R
+// fits one cluster's shared memory; else the grid kernel.  `check` asks the
+// occupancy API (needs a device).
 rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
   const int G = sp->G, D = sp->D, N = sp->N, H = sp->H, KP = sp->KP;
   const int eb = p->dtype == RK_F32 ? 4 : 2;
@@ -251,23 +271,42 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   };
   auto resident = [&](const StepPlan& pl) -> int {
     int teams = 0;
-    StepParams probe = *sp;
-    cudaError_t e;
-    switch (p->cell) {
-      case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(probe, pl, nullptr, &teams)
-                                                    : rk::step_entry<0, true>(probe, pl, nullptr, &teams); break;
-      case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(probe, pl, nullptr, &teams)
-                                                   : rk::step_entry<1, true>(probe, pl, nullptr, &teams); break;
-      default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(probe, pl, nullptr, &teams)
-                                               : rk::step_entry<2, true>(probe, pl, nullptr, &teams); break;
-    }
+    cudaError_t e = step_dispatch(p->cell, *sp, pl, nullptr, &teams);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
     return teams;
   };
+  sp->IP = (int)round_up(std::max<int64_t>(p->input, 1), rk::kKChunk);
 
+  const int KV = KP / rk::kKChunk;
+  const bool kv_ok = (p->dtype == RK_F32 ? KV <= 2 : KV <= 4) && KV != 3;
+  if (!(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP)) && kv_ok) {
+    for (int C = 1; C <= 16; C *= 2) {
+      StepPlan pl{};
+      pl.kind = rk::kStepClusterFast;
+      pl.shape = rk::kShapeR8B1;
+      pl.team_ctas = C;
+      pl.J = (H + C - 1) / C;
+      if (pl.J > 32) continue;
+      if (C > 1 && (int64_t)(C - 1) * pl.J >= H) continue;  // no CTA without units
+      pl.nb = 1;
+      pl.nbc = 1;
+      pl.teams_per_dir = N;
+      pl.rows_pad = G * (int)round_up(pl.J, 8);
+      pl.kv = KV;
+      pl.fused = !(h->flags & RK_FORCE_UNFUSED_PROJECTION) &&
+                 (int64_t)pl.rows_pad * sp->IP * eb <= 160 * 1024;
+      pl.threads = (pl.rows_pad / 8 + (pl.fused ? 4 : 0)) * 32;
+      if (pl.threads > 512) continue;
+      pl.grid = D * N * C;
+      if (!finish(pl)) continue;
+      if (check && resident(pl) < 1) continue;
+      *out = pl;
+      return RK_OK;
+    }
+  }
   if (!(h->flags & RK_FORCE_GRID_STEP)) {
     const int nb = N == 1 ? 1 : std::min(N, 8);
     const rk::StepShape shape = nb == 1 ? rk::kShapeR8B1 : rk::kShapeR4B8;
@@ -427,9 +466,11 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
     return RK_OK;
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
-  snprintf(buf, (size_t)len, "proj=simt step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
-           pl.kind == rk::kStepCluster ? "cluster" : "grid", (int)pl.shape, pl.team_ctas, pl.J, pl.nb,
-           pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
+  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
+  snprintf(buf, (size_t)len, "proj=%s step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
+           fused ? "fused" : "simt",
+           pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid"),
+           (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
   return RK_OK;
 }
 
@@ -477,8 +518,10 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     state = h->state;
   }
 
-  // 1. input projection of every step and direction
-  if (sp.T > 0 && need_xw > 0) {
+  // 1. input projection of every step and direction (inside the step kernel
+  //    when the plan fuses it)
+  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
+  if (sp.T > 0 && need_xw > 0 && !fused) {
     rk::ProjParams pp{};
     pp.M = (int)(p->seq * p->batch);
     pp.N = sp.G * sp.H;
@@ -509,6 +552,8 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
+  sp.X = tptr(ops->X, eb);
+  sp.W = tptr(ops->W, eb);
   sp.counters = reinterpret_cast<unsigned*>(state);
   sp.hglob = state + rk::kStateHeader;
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
@@ -519,15 +564,7 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
   }
   if (h->profiling) cudaEventRecord(h->ev[2], stream);
-  cudaError_t e;
-  switch (p->cell) {
-    case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(sp, pl, stream, nullptr)
-                                                  : rk::step_entry<0, true>(sp, pl, stream, nullptr); break;
-    case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(sp, pl, stream, nullptr)
-                                                 : rk::step_entry<1, true>(sp, pl, stream, nullptr); break;
-    default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(sp, pl, stream, nullptr)
-                                             : rk::step_entry<2, true>(sp, pl, stream, nullptr); break;
-  }
+  cudaError_t e = step_dispatch(p->cell, sp, pl, stream, nullptr);
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (e == cudaErrorCooperativeLaunchTooLarge)
@@ -578,7 +615,8 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   }
   float* state = scratch;            // 256-byte aligned start of the array
   float* xw = scratch + need_state;  // after the state region
-  if (sp.T > 0 && need_xw > 0) {
+  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
+  if (sp.T > 0 && need_xw > 0 && !fused) {
     rk::ProjParams pp{};
     pp.M = (int)(p->seq * p->batch);
     pp.N = sp.G * sp.H;
@@ -602,6 +640,8 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
+  sp.X = tptr(ops->X, eb);
+  sp.W = tptr(ops->W, eb);
   sp.counters = reinterpret_cast<unsigned*>(state);
   sp.hglob = state + rk::kStateHeader;
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
@@ -612,14 +652,7 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), stream);
   if (e != cudaSuccess) return cuda_fail(h, p, "scratch reset", e);
-  switch (p->cell) {
-    case RK_LSTM: e = pl.kind == rk::kStepCluster ? rk::step_entry<0, false>(sp, pl, stream, nullptr)
-                                                  : rk::step_entry<0, true>(sp, pl, stream, nullptr); break;
-    case RK_GRU: e = pl.kind == rk::kStepCluster ? rk::step_entry<1, false>(sp, pl, stream, nullptr)
-                                                 : rk::step_entry<1, true>(sp, pl, stream, nullptr); break;
-    default: e = pl.kind == rk::kStepCluster ? rk::step_entry<2, false>(sp, pl, stream, nullptr)
-                                             : rk::step_entry<2, true>(sp, pl, stream, nullptr); break;
-  }
+  e = step_dispatch(p->cell, sp, pl, stream, nullptr);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(h, p, "step kernel launch", e);

@@ -19,8 +19,9 @@ struct ActSlot {
 
 // Which persistent step kernel runs the recurrence.
 enum StepKind : int {
-  kStepCluster = 0,  // a team is one thread-block cluster; h exchanged through DSMEM
-  kStepGrid = 1,     // a team spans many SMs; h exchanged through L2 and a bounded barrier
+  kStepCluster = 0,      // a team is one thread-block cluster; h exchanged through DSMEM
+  kStepGrid = 1,         // a team spans many SMs; h exchanged through L2 and a bounded barrier
+  kStepClusterFast = 2,  // one batch row per cluster, R in registers, projection fused in
 };
 
 // Register tile of the step kernel's R.h product: rows per warp x batch rows.
@@ -49,7 +50,10 @@ struct StepParams {
   void* Y;             // may be null
   void* Yh;            // may be null
   void* Yc;            // may be null
-  const float* xw;     // [D, S*N, G*H]
+  const float* xw;     // [D, S*N, G*H] (unused by the fused kernel)
+  const void* X;       // fused projection: X and W as stored
+  const void* W;
+  int IP;              // input padded to a multiple of kKChunk (fused kernel)
   // plan
   int team_ctas;       // CTAs per team (cluster size for kStepCluster)
   int J;               // hidden units per CTA
@@ -81,6 +85,8 @@ struct StepPlan {
   int team_ctas, J, KP, nb, teams_per_dir, rows_pad, nbc;
   size_t smem;
   int grid;
+  int kv;     // kStepClusterFast: KP / kKChunk (R chunks per lane and row)
+  int fused;  // kStepClusterFast: projection computed inside the step kernel
 };
 
 // Launchers (defined in the .cu files).  Each returns a cudaError_t.
@@ -91,6 +97,10 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s);
 // returned through the pointer.
 template <int CELL, bool GRID>
 cudaError_t step_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
+// The fused batch-row-per-cluster step kernel (kStepClusterFast), same
+// contract as step_entry.
+template <int CELL>
+cudaError_t step_fast_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
 // Dynamic shared memory (bytes) the step kernel needs for a plan.
 size_t step_smem_for(const StepParams& p, const StepPlan& plan);
 // Fixed scratch of rk_encode_noalloc: floats per GPU, and the device

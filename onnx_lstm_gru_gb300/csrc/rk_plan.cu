@@ -1,11 +1,12 @@
 // rk_plan.cu -- shared-memory size of a step-kernel plan (computed from the
 // same layout function the kernel uses to carve its shared memory), and the
 // self-test of the step kernels' bounded waits.
-#include "rk_step.cuh"
+#include "rk_step_fast.cuh"
 
 namespace rk {
 
 size_t step_smem_for(const StepParams& p, const StepPlan& plan) {
+  if (plan.kind == kStepClusterFast) return fast_smem_layout(p, plan.rows_pad, plan.fused != 0, p.dtype == 0 ? 4 : 2).total;
   const bool grid = plan.kind == kStepGrid;
   const int eb = p.dtype == 0 ? 4 : 2;
   const int nb_ld = grid ? ((plan.nb + plan.nbc - 1) / plan.nbc) * plan.nbc : plan.nbc;  // as in the kernel

@@ -168,9 +168,10 @@ def test_plans_without_device(handle):
     """With no GPU the planner assumes a GB300 (152 SMs, 227 KB shared memory
     per block) and skips the occupancy check."""
     plans = {name: rk.rk_describe_plan(handle, w.problem.to_c()) for name, w in workloads.WORKLOADS.items()}
-    assert "step=cluster" in plans["lstm_fwd_s8_b1_i16_h16_f32"]
-    assert "step=cluster" in plans["bilstm_s80_b1_i256_h256_f32"] and "ctas=16" in plans["bilstm_s80_b1_i256_h256_f32"]
-    assert "step=cluster" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]
+    assert "step=fast" in plans["lstm_fwd_s8_b1_i16_h16_f32"]
+    assert "step=fast" in plans["bilstm_s80_b1_i256_h256_f32"] and "ctas=16" in plans["bilstm_s80_b1_i256_h256_f32"]
+    assert "proj=fused" in plans["bilstm_s80_b1_i256_h256_f32"]
+    assert "step=fast" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]
     assert "step=grid" in plans["revlstm_peep_clip_s200_b4_i128_h1024_f32"]
     assert "step=grid" in plans["bilstm_s512_b64_i1024_h1024_f16"]
     for name, text in plans.items():
@@ -178,11 +179,14 @@ def test_plans_without_device(handle):
         assert smem <= 232448 - 1024, (name, text)
     empty = rk.Problem("lstm", seq=3, batch=0, input=2, hidden=4)
     assert rk.rk_describe_plan(handle, empty.to_c()) == "noop"
-    h2 = rk.rk_create(rk.RK_FORCE_GRID_STEP)
-    try:
-        assert "step=grid" in rk.rk_describe_plan(h2, workloads.WORKLOADS["bilstm_s80_b1_i256_h256_f32"].problem.to_c())
-    finally:
-        rk.rk_destroy(h2)
+    c2 = workloads.WORKLOADS["bilstm_s80_b1_i256_h256_f32"].problem.to_c()
+    for flags, want in [(rk.RK_FORCE_GRID_STEP, "step=grid"), (rk.RK_FORCE_GENERAL_STEP, "step=cluster"),
+                        (rk.RK_FORCE_UNFUSED_PROJECTION, "proj=simt step=fast")]:
+        h2 = rk.rk_create(flags)
+        try:
+            assert want in rk.rk_describe_plan(h2, c2), flags
+        finally:
+            rk.rk_destroy(h2)
 
 
 def test_workload_inputs_are_seeded_and_shaped():

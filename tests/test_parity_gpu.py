@@ -198,7 +198,11 @@ for cell in ("lstm", "gru", "rnn"):
                 CASES.append((cell, direction, layout, opts))
 
 
-@pytest.mark.parametrize("kernel", ["cluster", "grid"])
+KERNELS = {"fused": 0, "fast_unfused": rk.RK_FORCE_UNFUSED_PROJECTION, "cluster": rk.RK_FORCE_GENERAL_STEP,
+           "grid": rk.RK_FORCE_GRID_STEP}
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("cell,direction,layout,opts", CASES)
 def test_option_matrix(cell, direction, layout, opts, kernel):
     S, N, I, H = 7, 3, 5, 40
@@ -214,8 +218,7 @@ def test_option_matrix(cell, direction, layout, opts, kernel):
         pr.linear_before_reset = lbr
         inp = rand_inputs(pr, seed=100 + len(cell) + layout, lens=lens, init=opts == "full",
                           peep=opts == "full", bias=opts == "full")
-        flags = rk.RK_FORCE_GRID_STEP if kernel == "grid" else 0
-        got = run_gpu(pr, inp, flags=flags)
+        got = run_gpu(pr, inp, flags=KERNELS[kernel])
         ref = run_oracle(pr, inp)
         compare(pr, got, ref, lens)
 
@@ -261,14 +264,24 @@ def test_empty_sequence_and_batch():
     assert layer().launches() == before  # Batch = 0 records nothing
 
 
-@pytest.mark.parametrize("kernel", ["cluster", "grid"])
-@pytest.mark.parametrize("H,N", [(100, 11), (37, 9), (130, 2), (513, 1)])
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("H,N", [(100, 11), (37, 9), (130, 2), (513, 1), (250, 3)])
 def test_ragged_hidden_and_large_batch(H, N, kernel):
-    pr = rk.Problem("gru", seq=6, batch=N, input=9, hidden=H, direction="bidirectional", linear_before_reset=0)
-    lens = list(np.random.default_rng(H).integers(0, 7, N))
-    inp = rand_inputs(pr, seed=H + N, lens=lens, scale=0.2)
-    flags = rk.RK_FORCE_GRID_STEP if kernel == "grid" else 0
-    compare(pr, run_gpu(pr, inp, flags=flags), run_oracle(pr, inp), lens)
+    for lbr in (0, 1):
+        pr = rk.Problem("gru", seq=6, batch=N, input=9, hidden=H, direction="bidirectional", linear_before_reset=lbr)
+        lens = list(np.random.default_rng(H).integers(0, 7, N))
+        inp = rand_inputs(pr, seed=H + N, lens=lens, scale=0.2)
+        compare(pr, run_gpu(pr, inp, flags=KERNELS[kernel]), run_oracle(pr, inp), lens)
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_kernels_agree_on_lstm_with_every_option(kernel, dtype):
+    pr = rk.Problem("lstm", seq=9, batch=2, input=70, hidden=96, direction="bidirectional", dtype=dtype, layout=1,
+                    clip=2.5, input_forget=1,
+                    activations=[("hardsigmoid", 0.2, 0.5), ("scaledtanh", 1.0, 1.0), ("softsign", 0, 0)] * 2)
+    inp = rand_inputs(pr, seed=31, lens=[9, 4], peep=True, scale=0.3)
+    compare(pr, run_gpu(pr, inp, flags=KERNELS[kernel]), run_oracle(pr, inp), [9, 4])
 
 
 def test_max_length_shortens_loop():
@@ -299,14 +312,17 @@ def test_getting_started_rows_exact():
 
 # ------------------------------------------------------------------ boundary behaviour
 
-def test_launches_do_not_grow_with_seq():
-    L = layer()
+@pytest.mark.parametrize("flags,per_layer", [(0, 1), (rk.RK_FORCE_GENERAL_STEP, 2), (rk.RK_FORCE_GRID_STEP, 2)])
+def test_launches_do_not_grow_with_seq(flags, per_layer):
+    """One persistent step kernel per layer (plus the projection when it is
+    not fused into it), whatever the sequence length."""
+    L = layer(flags)
     for S in (4, 64):
         pr = rk.Problem("lstm", seq=S, batch=1, input=8, hidden=32)
         inp = rand_inputs(pr, seed=S)
         before = L.launches()
-        run_gpu(pr, inp)
-        assert L.launches() - before == 2  # projection + one persistent step kernel
+        run_gpu(pr, inp, flags=flags)
+        assert L.launches() - before == per_layer
 
 
 def test_caller_scratch_in_one_arena_is_bitwise_equal():
