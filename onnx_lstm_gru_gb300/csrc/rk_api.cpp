@@ -247,7 +247,7 @@ cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl
   }
 }
 
-// Step-kernel plan, in order of preference: the fused one-row-per-cluster
+// Step-kernel plan, in order of preference: the one-row-per-cluster
 // kernel (R in registers) when a row's hidden units fit 16 CTAs of <= 32
 // units and R's chunks fit the registers; else the cluster kernel when R
 // fits one cluster's shared memory; else the grid kernel.  `check` asks the
@@ -278,28 +278,27 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     }
     return teams;
   };
-  sp->IP = (int)round_up(std::max<int64_t>(p->input, 1), rk::kKChunk);
-
+  // fast kernel: one batch row per cluster, R rows in registers.  Largest
+  // cluster (<= 16 CTAs) whose clusters all fit the GPU at once, with 16 to
+  // 32 hidden units per CTA (fewer when H itself is smaller).
   const int KV = KP / rk::kKChunk;
   const bool kv_ok = (p->dtype == RK_F32 ? KV <= 2 : KV <= 4) && KV != 3;
+  const int U = p->cell == RK_RNN ? 8 : 2;
   if (!(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP)) && kv_ok) {
-    for (int C = 1; C <= 16; C *= 2) {
+    for (int C = 16; C >= 1; C /= 2) {
       StepPlan pl{};
       pl.kind = rk::kStepClusterFast;
       pl.shape = rk::kShapeR8B1;
       pl.team_ctas = C;
       pl.J = (H + C - 1) / C;
-      if (pl.J > 32) continue;
+      if (pl.J > 32 || pl.J < std::min(H, 16)) continue;
       if (C > 1 && (int64_t)(C - 1) * pl.J >= H) continue;  // no CTA without units
+      if ((int64_t)D * N * C > h->sms) continue;            // all clusters at once
       pl.nb = 1;
       pl.nbc = 1;
       pl.teams_per_dir = N;
-      pl.rows_pad = G * (int)round_up(pl.J, 8);
       pl.kv = KV;
-      pl.fused = !(h->flags & RK_FORCE_UNFUSED_PROJECTION) &&
-                 (int64_t)pl.rows_pad * sp->IP * eb <= 160 * 1024;
-      pl.threads = (pl.rows_pad / 8 + (pl.fused ? 4 : 0)) * 32;
-      if (pl.threads > 512) continue;
+      pl.threads = (pl.J + U - 1) / U * 32;
       pl.grid = D * N * C;
       if (!finish(pl)) continue;
       if (check && resident(pl) < 1) continue;
@@ -466,9 +465,7 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
     return RK_OK;
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
-  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
-  snprintf(buf, (size_t)len, "proj=%s step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
-           fused ? "fused" : "simt",
+  snprintf(buf, (size_t)len, "proj=simt step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
            pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid"),
            (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
   return RK_OK;
@@ -518,10 +515,8 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     state = h->state;
   }
 
-  // 1. input projection of every step and direction (inside the step kernel
-  //    when the plan fuses it)
-  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
-  if (sp.T > 0 && need_xw > 0 && !fused) {
+  // 1. input projection of every step and direction
+  if (sp.T > 0 && need_xw > 0) {
     rk::ProjParams pp{};
     pp.M = (int)(p->seq * p->batch);
     pp.N = sp.G * sp.H;
@@ -552,8 +547,6 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
-  sp.X = tptr(ops->X, eb);
-  sp.W = tptr(ops->W, eb);
   sp.counters = reinterpret_cast<unsigned*>(state);
   sp.hglob = state + rk::kStateHeader;
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
@@ -615,8 +608,7 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   }
   float* state = scratch;            // 256-byte aligned start of the array
   float* xw = scratch + need_state;  // after the state region
-  const bool fused = pl.kind == rk::kStepClusterFast && pl.fused;
-  if (sp.T > 0 && need_xw > 0 && !fused) {
+  if (sp.T > 0 && need_xw > 0) {
     rk::ProjParams pp{};
     pp.M = (int)(p->seq * p->batch);
     pp.N = sp.G * sp.H;
@@ -640,8 +632,6 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
-  sp.X = tptr(ops->X, eb);
-  sp.W = tptr(ops->W, eb);
   sp.counters = reinterpret_cast<unsigned*>(state);
   sp.hglob = state + rk::kStateHeader;
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;

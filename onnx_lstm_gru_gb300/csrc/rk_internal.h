@@ -21,7 +21,7 @@ struct ActSlot {
 enum StepKind : int {
   kStepCluster = 0,      // a team is one thread-block cluster; h exchanged through DSMEM
   kStepGrid = 1,         // a team spans many SMs; h exchanged through L2 and a bounded barrier
-  kStepClusterFast = 2,  // one batch row per cluster, R in registers, projection fused in
+  kStepClusterFast = 2,  // one batch row per cluster, R in registers, no CTA-wide barrier
 };
 
 // Register tile of the step kernel's R.h product: rows per warp x batch rows.
@@ -50,10 +50,7 @@ struct StepParams {
   void* Y;             // may be null
   void* Yh;            // may be null
   void* Yc;            // may be null
-  const float* xw;     // [D, S*N, G*H] (unused by the fused kernel)
-  const void* X;       // fused projection: X and W as stored
-  const void* W;
-  int IP;              // input padded to a multiple of kKChunk (fused kernel)
+  const float* xw;     // [D, S*N, G*H]
   // plan
   int team_ctas;       // CTAs per team (cluster size for kStepCluster)
   int J;               // hidden units per CTA
@@ -86,7 +83,6 @@ struct StepPlan {
   size_t smem;
   int grid;
   int kv;     // kStepClusterFast: KP / kKChunk (R chunks per lane and row)
-  int fused;  // kStepClusterFast: projection computed inside the step kernel
 };
 
 // Launchers (defined in the .cu files).  Each returns a cudaError_t.
@@ -97,8 +93,8 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s);
 // returned through the pointer.
 template <int CELL, bool GRID>
 cudaError_t step_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
-// The fused batch-row-per-cluster step kernel (kStepClusterFast), same
-// contract as step_entry.
+// The batch-row-per-cluster step kernel (kStepClusterFast), same contract
+// as step_entry.
 template <int CELL>
 cudaError_t step_fast_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident_teams);
 // Dynamic shared memory (bytes) the step kernel needs for a plan.

@@ -6,7 +6,7 @@
 namespace rk {
 
 size_t step_smem_for(const StepParams& p, const StepPlan& plan) {
-  if (plan.kind == kStepClusterFast) return fast_smem_layout(p, plan.rows_pad, plan.fused != 0, p.dtype == 0 ? 4 : 2).total;
+  if (plan.kind == kStepClusterFast) return fast_smem_layout(p).total;
   const bool grid = plan.kind == kStepGrid;
   const int eb = p.dtype == 0 ? 4 : 2;
   const int nb_ld = grid ? ((plan.nb + plan.nbc - 1) / plan.nbc) * plan.nbc : plan.nbc;  // as in the kernel

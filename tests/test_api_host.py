@@ -170,8 +170,7 @@ def test_plans_without_device(handle):
     plans = {name: rk.rk_describe_plan(handle, w.problem.to_c()) for name, w in workloads.WORKLOADS.items()}
     assert "step=fast" in plans["lstm_fwd_s8_b1_i16_h16_f32"]
     assert "step=fast" in plans["bilstm_s80_b1_i256_h256_f32"] and "ctas=16" in plans["bilstm_s80_b1_i256_h256_f32"]
-    assert "proj=fused" in plans["bilstm_s80_b1_i256_h256_f32"]
-    assert "step=fast" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]
+    assert "step=cluster" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]  # 16 clusters of 16 would not fit at once
     assert "step=grid" in plans["revlstm_peep_clip_s200_b4_i128_h1024_f32"]
     assert "step=grid" in plans["bilstm_s512_b64_i1024_h1024_f16"]
     for name, text in plans.items():
@@ -180,8 +179,7 @@ def test_plans_without_device(handle):
     empty = rk.Problem("lstm", seq=3, batch=0, input=2, hidden=4)
     assert rk.rk_describe_plan(handle, empty.to_c()) == "noop"
     c2 = workloads.WORKLOADS["bilstm_s80_b1_i256_h256_f32"].problem.to_c()
-    for flags, want in [(rk.RK_FORCE_GRID_STEP, "step=grid"), (rk.RK_FORCE_GENERAL_STEP, "step=cluster"),
-                        (rk.RK_FORCE_UNFUSED_PROJECTION, "proj=simt step=fast")]:
+    for flags, want in [(rk.RK_FORCE_GRID_STEP, "step=grid"), (rk.RK_FORCE_GENERAL_STEP, "step=cluster")]:
         h2 = rk.rk_create(flags)
         try:
             assert want in rk.rk_describe_plan(h2, c2), flags

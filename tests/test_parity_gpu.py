@@ -198,8 +198,7 @@ for cell in ("lstm", "gru", "rnn"):
                 CASES.append((cell, direction, layout, opts))
 
 
-KERNELS = {"fused": 0, "fast_unfused": rk.RK_FORCE_UNFUSED_PROJECTION, "cluster": rk.RK_FORCE_GENERAL_STEP,
-           "grid": rk.RK_FORCE_GRID_STEP}
+KERNELS = {"fast": 0, "cluster": rk.RK_FORCE_GENERAL_STEP, "grid": rk.RK_FORCE_GRID_STEP}
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
@@ -312,10 +311,10 @@ def test_getting_started_rows_exact():
 
 # ------------------------------------------------------------------ boundary behaviour
 
-@pytest.mark.parametrize("flags,per_layer", [(0, 1), (rk.RK_FORCE_GENERAL_STEP, 2), (rk.RK_FORCE_GRID_STEP, 2)])
+@pytest.mark.parametrize("flags,per_layer", [(0, 2), (rk.RK_FORCE_GENERAL_STEP, 2), (rk.RK_FORCE_GRID_STEP, 2)])
 def test_launches_do_not_grow_with_seq(flags, per_layer):
-    """One persistent step kernel per layer (plus the projection when it is
-    not fused into it), whatever the sequence length."""
+    """The projection plus one persistent step kernel per layer, whatever the
+    sequence length."""
     L = layer(flags)
     for S in (4, 64):
         pr = rk.Problem("lstm", seq=S, batch=1, input=8, hidden=32)
