@@ -283,7 +283,7 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   // 32 hidden units per CTA (fewer when H itself is smaller).
   const int KV = KP / rk::kKChunk;
   const bool kv_ok = (p->dtype == RK_F32 ? KV <= 2 : KV <= 4) && KV != 3;
-  const int U = p->cell == RK_RNN ? 8 : 2;
+  const int U = p->cell == RK_RNN ? 8 : (KV <= 2 ? 4 : 2);  // units per warp, as the kernel uses
   if (!(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP)) && kv_ok) {
     for (int C = 16; C >= 1; C /= 2) {
       StepPlan pl{};

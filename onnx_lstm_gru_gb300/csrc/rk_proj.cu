@@ -9,10 +9,11 @@
 // multiply-add, one chain per output element in increasing k, so the result
 // does not depend on scheduling.
 //
-// Tiling: a 64 x 64 tile of Xw per 256-thread CTA, k in steps of 16 staged
-// through shared memory k-major (so each thread reads its 4 rows and 4
-// columns as float4), 4 x 4 outputs per thread.  Loads are bounds-checked and
-// element-wise, so any M, N, K and any element offset works.
+// Two kernels.  The pipelined one (below) serves 16-byte aligned operands.
+// The fallback serves any M, N, K and any element offset: a 64 x 64 tile of
+// Xw per 256-thread CTA, k in steps of 16 staged through shared memory
+// k-major (so each thread reads its 4 rows and 4 columns as float4), 4 x 4
+// outputs per thread, bounds-checked element-wise loads.
 #include <cuda_fp16.h>
 
 #include "rk_internal.h"
@@ -90,10 +91,157 @@ __global__ void __launch_bounds__(256) proj_simt_kernel(int M, int N, int K, con
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined variant for 16-byte aligned operands (X and W bases 16-byte
+// aligned, K * element size a multiple of 16): 4 stages of 32-deep k tiles
+// are kept in flight with cp.async (16-byte copies, zero-filled past M, N
+// and K), so the loads of later tiles overlap the arithmetic of earlier ones.
+// Tiles are PBM x 64 of Xw per 128-thread CTA; thread (tm, tn) owns rows
+// tm + 8 i and columns tn + 16 j (strided, so the 16-byte shared loads of a
+// quarter warp hit distinct banks and the stores are coalesced).  Each output
+// is still one fused-multiply-add chain in increasing k.
+constexpr int PBN = 64, PBK = 32, PSTAGES = 4, PTHREADS = 128;
+
+template <typename T>
+struct PipeElem {
+  static constexpr int per16 = 16 / (int)sizeof(T);  // elements per 16-byte copy
+  static constexpr int ld = PBK + per16;             // padded row length (elements)
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ float4 load4_row(const T* p);
+template <>
+__device__ __forceinline__ float4 load4_row<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4_row<__half>(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T, int PBM>
+__global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K, const T* __restrict__ X,
+                                                             const T* __restrict__ W, float* __restrict__ Xw) {
+  constexpr int E = PipeElem<T>::per16, LD = PipeElem<T>::ld;
+  constexpr int RM = PBM / 8;  // rows per thread
+  extern __shared__ __align__(16) unsigned char psm[];
+  T* As = reinterpret_cast<T*>(psm);                    // [PSTAGES][PBM][LD]
+  T* Bs = As + (size_t)PSTAGES * PBM * LD;              // [PSTAGES][PBN][LD]
+  const int d = blockIdx.z;
+  const int m0 = blockIdx.y * PBM, n0 = blockIdx.x * PBN;
+  const int tid = threadIdx.x, tn = tid & 15, tm = tid >> 4;
+  const T* Wd = W + (size_t)d * N * K;
+  const int KT = (K + PBK - 1) / PBK;
+  constexpr int CPR = PBK / E;                          // 16-byte chunks per tile row
+  constexpr int A_CH = PBM * CPR, B_CH = PBN * CPR;
+
+  auto issue = [&](int kt) {
+    const int st = kt % PSTAGES, k0 = kt * PBK;
+    for (int c = tid; c < A_CH + B_CH; c += PTHREADS) {
+      const bool isA = c < A_CH;
+      const int cc = isA ? c : c - A_CH;
+      const int r = cc / CPR, kc = (cc % CPR) * E;
+      const int gr = (isA ? m0 : n0) + r;
+      const bool ok = gr < (isA ? M : N) && k0 + kc < K;
+      const T* src = isA ? X + (size_t)(ok ? gr : 0) * K + (ok ? k0 + kc : 0) : Wd + (size_t)(ok ? gr : 0) * K + (ok ? k0 + kc : 0);
+      T* dst = (isA ? As + ((size_t)st * PBM + r) * LD : Bs + ((size_t)st * PBN + r) * LD) + kc;
+      cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(dst)), src, ok ? 16 : 0);
+    }
+  };
+
+  float acc[RM][4];
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+  for (int s = 0; s < PSTAGES - 1; ++s) {
+    if (s < KT) issue(s);
+    cp_async_commit();
+  }
+  for (int kt = 0; kt < KT; ++kt) {
+    cp_async_wait<PSTAGES - 2>();
+    __syncthreads();
+    if (kt + PSTAGES - 1 < KT) issue(kt + PSTAGES - 1);
+    cp_async_commit();
+    const int st = kt % PSTAGES;
+    const T* a = As + (size_t)st * PBM * LD;
+    const T* b = Bs + (size_t)st * PBN * LD;
+#pragma unroll
+    for (int kk = 0; kk < PBK; kk += 4) {
+      float4 av[RM], bv[4];
+#pragma unroll
+      for (int i = 0; i < RM; ++i) av[i] = load4_row<T>(a + (size_t)(tm + 8 * i) * LD + kk);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = load4_row<T>(b + (size_t)(tn + 16 * j) * LD + kk);
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float x = acc[i][j];
+          x = fmaf(av[i].x, bv[j].x, x);
+          x = fmaf(av[i].y, bv[j].y, x);
+          x = fmaf(av[i].z, bv[j].z, x);
+          x = fmaf(av[i].w, bv[j].w, x);
+          acc[i][j] = x;
+        }
+    }
+  }
+  cp_async_wait<0>();
+  float* out = Xw + (size_t)d * M * N;
+#pragma unroll
+  for (int i = 0; i < RM; ++i) {
+    const int m = m0 + tm + 8 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tn + 16 * j;
+      if (n < N) out[(size_t)m * N + n] = acc[i][j];
+    }
+  }
+}
+
+template <typename T, int PBM>
+cudaError_t launch_pipe(const ProjParams& p, cudaStream_t s) {
+  const size_t smem = (size_t)PSTAGES * (PBM + PBN) * PipeElem<T>::ld * sizeof(T);
+  auto kern = proj_pipe_kernel<T, PBM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.N + PBN - 1) / PBN), (unsigned)((p.M + PBM - 1) / PBM), (unsigned)p.D);
+  if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+  kern<<<grid, PTHREADS, smem, s>>>(p.M, p.N, p.K, static_cast<const T*>(p.X), static_cast<const T*>(p.W), p.Xw);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   if (p.M <= 0 || p.N <= 0) return cudaSuccess;
+  const int eb = p.dtype == 0 ? 4 : 2;
+  const bool aligned = (reinterpret_cast<uintptr_t>(p.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
+                       ((size_t)p.K * eb) % 16 == 0 && p.K > 0;
+  if (aligned) {
+    // 16-row tiles when 32-row tiles would leave SMs idle
+    const long long tiles32 = (long long)((p.N + PBN - 1) / PBN) * ((p.M + 31) / 32) * p.D;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool small = tiles32 < 2LL * sms;
+    if (p.dtype == 0) return small ? launch_pipe<float, 16>(p, s) : launch_pipe<float, 32>(p, s);
+    return small ? launch_pipe<__half, 16>(p, s) : launch_pipe<__half, 32>(p, s);
+  }
   dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.D);
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
   if (p.dtype == 0) {

@@ -11,8 +11,11 @@
 //
 // Layout: one cluster of C CTAs per (direction, batch row); CTA `rank` owns
 // hidden units [j0, j0 + J) with J <= 32.  Warp w owns U whole units
-// (U = 2 for LSTM and GRU, 8 for RNN): all G*U of their rows of R live in the
-// warp's registers for the whole layer (lanes hold k = 4*(32*chunk + lane)+e).
+// (U = 4 for LSTM and GRU when R's rows are short enough, else 2; 8 for
+// RNN): all G*U of their rows of R live in the warp's registers for the whole
+// layer (lanes hold k = 4*(32*chunk + lane) + e).  Each exchange message then
+// carries 4 units (16 bytes): the cost of an exchange grows with the number
+// of st.async messages a CTA receives, so fewer, larger messages matter.
 // Per step a warp
 //   1. waits on its CTA's mbarrier for h_prev (all H units, pushed by every
 //      CTA of the cluster with st.async),
@@ -33,20 +36,11 @@
 
 namespace rk {
 
-// Units per warp, per cell.
-template <int CELL>
-struct FastUnits;
-template <>
-struct FastUnits<0> {  // LSTM: rows g*2 + u, g in i, o, f, c
-  static constexpr int U = 2;
-};
-template <>
-struct FastUnits<1> {  // GRU: rows g*2 + u, g in z, r, h (rows 6, 7 unused)
-  static constexpr int U = 2;
-};
-template <>
-struct FastUnits<2> {  // RNN: rows u
-  static constexpr int U = 8;
+// Register rows a warp holds: G * U rounded up to a power of two (8 or 16).
+template <int CELL, int U>
+struct FastRows {
+  static constexpr int G = CELL == 0 ? 4 : (CELL == 1 ? 3 : 1);
+  static constexpr int value = (G * U <= 8) ? 8 : 16;
 };
 
 struct FastSmem {
@@ -96,11 +90,36 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uin
                : "memory");
 }
 
-// Sums of register rows R0 .. R0+NR-1 against h (KV float4 slices per lane),
-// folded by the shuffle tree: afterwards the sum of row R0 + i sits in lane
-// xreduce_lane<NR>(i).
-template <int R0, int NR, typename T, int KV>
-__device__ __forceinline__ float rowsums(const RFrag<T> (&R)[8][KV], const float* __restrict__ h, int lane) {
+// Row sums with a shuffle tree that needs no selects.  Lane l keeps the NR
+// rows of a block in the lane-dependent order i -> i ^ perm_mask<NR>(l) (the
+// rows' registers are loaded that way), so at every level each lane adds the
+// upper half of its partial sums, received from its partner lane, to its lower
+// half.  Afterwards lane l holds the full sum of row perm_mask<NR>(l) of the
+// block, i.e. row r sits in lanes r * (32 / NR) ... r * (32 / NR) + 32/NR - 1.
+template <int NR>
+__host__ __device__ constexpr int log2c() { return NR <= 1 ? 0 : 1 + log2c<NR / 2>(); }
+template <int NR>
+__device__ __forceinline__ int perm_mask(int lane) { return (lane >> (5 - log2c<NR>())) & (NR - 1); }
+template <int NR>
+__device__ __forceinline__ int row_lane(int r) { return r << (5 - log2c<NR>()); }
+
+template <int N, int O>
+__device__ __forceinline__ void fold(float* v) {
+  if constexpr (N > 1) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + N / 2], O);
+    if constexpr (O > 1) fold<N / 2, O / 2>(v);
+  } else {
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+    if constexpr (O > 1) fold<1, O / 2>(v);
+  }
+}
+
+// Sums of register rows R0 .. R0+NR-1 (a block stored in permuted order)
+// against h (KV float4 slices per lane); each lane chains its terms in
+// increasing k, then fold() combines the 32 lanes in a fixed order.
+template <int R0, int NR, typename T, int KV, int RW>
+__device__ __forceinline__ float rowsums(const RFrag<T> (&R)[RW][KV], const float* __restrict__ h, int lane) {
   float4 hv[KV];
 #pragma unroll
   for (int kc = 0; kc < KV; ++kc) hv[kc] = *reinterpret_cast<const float4*>(h + (kc * 32 + lane) * 4);
@@ -118,30 +137,17 @@ __device__ __forceinline__ float rowsums(const RFrag<T> (&R)[8][KV], const float
     }
     acc[r] = a;
   }
-  xreduce<NR, 16>(acc, lane);
+  fold<NR, 16>(acc);
   return acc[0];
 }
 
-// The lowest lane holding value index i after xreduce<N>.
-template <int N>
-__device__ __forceinline__ int xreduce_lane(int i) {
-  int lane = 0, half = N;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (half > 1) {
-      half >>= 1;
-      if (i & half) lane |= o;
-    }
-  }
-  return lane;
-}
-
-template <int CELL, typename T, bool GEN, int KV>
-__global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
+// PLAIN: no clip, no peepholes, no input_forget (the options compile out).
+template <int CELL, typename T, bool GEN, int KV, int U, bool PLAIN>
+__global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
-  constexpr int U = FastUnits<CELL>::U;
+  constexpr int RW = FastRows<CELL, U>::value;  // register rows per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = p.team_ctas;
   const int rank = (int)cluster_ctarank();
@@ -178,9 +184,19 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
   }
 
   // ---------------- prologue: R rows into registers, h_0, per-unit state
-  RFrag<T> Rr[8][KV];
+  // register i of this lane holds row row_of(i) of the warp's rows (g * U + u)
+  auto row_of = [&](int i) -> int {
+    if (lbr0) {
+      if (i < 2 * U) return i ^ perm_mask<2 * U>(lane);
+      if (i < 3 * U) return 2 * U + ((i - 2 * U) ^ perm_mask<U>(lane));
+      return i;
+    }
+    return i ^ perm_mask<RW>(lane);
+  };
+  RFrag<T> Rr[RW][KV];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
+  for (int i = 0; i < RW; ++i) {
+    const int r = row_of(i);
     const int g = r / U, u = r % U;
     const bool ok = g < G && u < Uc;
     const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
@@ -190,7 +206,7 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
       float e[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
-      Rr[r][kc].set(e);
+      Rr[i][kc].set(e);
     }
   }
   for (int e = tid; e < 2 * KP; e += blockDim.x) {
@@ -210,7 +226,9 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
 #pragma unroll
   for (int g = 0; g < 3; ++g)
     ppv[g] = (CELL == 0 && gl && P != nullptr) ? load_elem<T>(P + (size_t)d * 3 * H + (size_t)g * H + uj) : 0.0f;
-  const bool has_p = CELL == 0 && P != nullptr;
+  const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
+  const float clip = PLAIN ? 0.0f : p.clip;
+  const bool input_forget = !PLAIN && p.input_forget;
   if (gl) {
     const size_t si = state_index(p, d, b, uj);
     hreg = h0 != nullptr ? load_elem<T>(h0 + si) : 0.0f;
@@ -226,19 +244,20 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
   cluster_sync_all();
 
   // ---------------- the push of this warp's units into every CTA
-  // vector form: U = 2 -> one 8-byte st.async per peer (lanes q < C);
-  // U = 8 -> two 16-byte st.async per peer (lanes 2q + e < 2C); needs whole
-  // warps and aligned unit offsets.  Otherwise one 4-byte st.async per
-  // (peer, unit).
+  // vector form (whole warps, unit offsets aligned to the message size):
+  // U = 2 -> one 8-byte st.async per peer (lanes q < C); U = 4 -> one 16-byte
+  // st.async per peer; U = 8 -> two 16-byte st.async per peer (lanes 2q + e).
+  // Otherwise one 4-byte st.async per (peer, unit).
   const uint32_t hs_u = smem_u32(hs);
   const uint32_t bar_u = smem_u32(&bars[0]);
-  const bool vec = (Uc == U) && (((j0 + wu0) * 4) % (U == 2 ? 8 : 16) == 0);
-  const int vec_items = U == 2 ? C : 2 * C;
+  constexpr int kMsgUnits = U == 2 ? 2 : 4;
+  const bool vec = (Uc == U) && (((j0 + wu0) % kMsgUnits) == 0);
+  const int vec_items = U == 8 ? 2 * C : C;
   uint32_t my_dst = 0, my_bar = 0;
   int my_src = 0;
   if (vec && lane < vec_items) {
-    const int q = U == 2 ? lane : lane >> 1;
-    const int e = U == 2 ? 0 : (lane & 1);
+    const int q = U == 8 ? lane >> 1 : lane;
+    const int e = U == 8 ? (lane & 1) : 0;
     my_src = 4 * e;
     my_dst = map_to_rank(hs_u + (uint32_t)(j0 + wu0 + 4 * e) * 4u, (uint32_t)q);
     my_bar = map_to_rank(bar_u, (uint32_t)q);
@@ -287,12 +306,15 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
     return true;
   };
 
-  // xw of this lane's unit for step s (loaded one step ahead)
+  // xw of this lane's unit for step s (loaded one step ahead):
+  // element (t, g) = xw_base + t * xw_tstride + g * H
+  const size_t xw_tstride = p.layout == 0 ? (size_t)p.N * GH : GH;
+  const float* xw_base = p.xw + xw_index(p, d, 0, b, 0, uj);
   auto load_xw = [&](int s, float (&x)[G]) {
     const bool on = gl && s < len && s < Tn;
-    const int t = reverse ? len - 1 - s : s;
+    const float* q = xw_base + (size_t)(reverse ? len - 1 - s : s) * xw_tstride;
 #pragma unroll
-    for (int g = 0; g < G; ++g) x[g] = on ? __ldg(p.xw + xw_index(p, d, t, b, g, uj)) : 0.0f;
+    for (int g = 0; g < G; ++g) x[g] = on ? __ldg(q + (size_t)g * H) : 0.0f;
   };
 
   const uint32_t h_bytes = (uint32_t)H * 4u;
@@ -321,34 +343,34 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
     if constexpr (CELL == 1) {
       if (lbr0) {
         // z and r rows against h_prev; exchange r (.) h_prev; h rows against it
-        const float v1 = rowsums<0, 4, T, KV>(Rr, hs + (size_t)cur * KP, lane);
-        const float sz = __shfl_sync(0xffffffffu, v1, xreduce_lane<4>(0 * U + ul));
-        const float sr = __shfl_sync(0xffffffffu, v1, xreduce_lane<4>(1 * U + ul));
-        const float z = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, ((xv[0] + sz) + wbv[0]) + rbv[0]));
-        const float r = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, ((xv[1] + sr) + wbv[1]) + rbv[1]));
+        const float v1 = rowsums<0, 2 * U, T, KV>(Rr, hs + (size_t)cur * KP, lane);
+        const float sz = __shfl_sync(0xffffffffu, v1, row_lane<2 * U>(0 * U + ul));
+        const float sr = __shfl_sync(0xffffffffu, v1, row_lane<2 * U>(1 * U + ul));
+        const float z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[0] + sz) + wbv[0]) + rbv[0]));
+        const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[1] + sr) + wbv[1]) + rbv[1]));
         push(r * hreg, 1, cur);
         if (!wait(&bars[2 + cur], (uint32_t)((s >> 1) & 1))) break;
-        const float v2 = rowsums<4, 2, T, KV>(Rr, rhs + (size_t)cur * KP, lane);
-        const float sh = __shfl_sync(0xffffffffu, v2, xreduce_lane<2>(ul));
-        const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(p.clip, ((xv[2] + sh) + wbv[2]) + rbv[2]));
+        const float v2 = rowsums<2 * U, U, T, KV>(Rr, rhs + (size_t)cur * KP, lane);
+        const float sh = __shfl_sync(0xffffffffu, v2, row_lane<U>(ul));
+        const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, ((xv[2] + sh) + wbv[2]) + rbv[2]));
         if (active) hn = (1.0f - z) * hc + z * hreg;
       } else {
-        const float v = rowsums<0, 8, T, KV>(Rr, hs + (size_t)cur * KP, lane);
+        const float v = rowsums<0, RW, T, KV>(Rr, hs + (size_t)cur * KP, lane);
         float sum[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) sum[g] = __shfl_sync(0xffffffffu, v, xreduce_lane<8>(g * U + ul));
-        const float z = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, ((xv[0] + sum[0]) + wbv[0]) + rbv[0]));
-        const float r = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, ((xv[1] + sum[1]) + wbv[1]) + rbv[1]));
+        for (int g = 0; g < G; ++g) sum[g] = __shfl_sync(0xffffffffu, v, row_lane<RW>(g * U + ul));
+        const float z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[0] + sum[0]) + wbv[0]) + rbv[0]));
+        const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[1] + sum[1]) + wbv[1]) + rbv[1]));
         const float ph = (xv[2] + r * (sum[2] + rbv[2])) + wbv[2];
-        const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(p.clip, ph));
+        const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, ph));
         if (active) hn = (1.0f - z) * hc + z * hreg;
       }
     } else {
-      const float v = rowsums<0, 8, T, KV>(Rr, hs + (size_t)cur * KP, lane);
+      const float v = rowsums<0, RW, T, KV>(Rr, hs + (size_t)cur * KP, lane);
       float pre[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float sum = __shfl_sync(0xffffffffu, v, xreduce_lane<8>(g * U + ul));
+        const float sum = __shfl_sync(0xffffffffu, v, row_lane<RW>(g * U + ul));
         pre[g] = ((xv[g] + sum) + wbv[g]) + rbv[g];
       }
       if constexpr (CELL == 0) {
@@ -357,18 +379,18 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
           pi = pi + ppv[0] * creg;
           pf = pf + ppv[2] * creg;
         }
-        const float ig = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pi));
-        const float fg = p.input_forget ? 1.0f - ig : act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pf));
-        const float cg = act<GEN, 1>(p, d * A + 1, clip_pre(p.clip, pc));
+        const float ig = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pi));
+        const float fg = input_forget ? 1.0f - ig : act<GEN, 0>(p, d * A + 0, clip_pre(clip, pf));
+        const float cg = act<GEN, 1>(p, d * A + 1, clip_pre(clip, pc));
         const float cn = fg * creg + ig * cg;
         if (has_p) po = po + ppv[1] * cn;
-        const float og = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, po));
+        const float og = act<GEN, 0>(p, d * A + 0, clip_pre(clip, po));
         if (active) {
           hn = og * act<GEN, 1>(p, d * A + 2, cn);
           creg = cn;
         }
       } else {
-        if (active) hn = act<GEN, 1>(p, d * A + 0, clip_pre(p.clip, pre[0]));
+        if (active) hn = act<GEN, 1>(p, d * A + 0, clip_pre(clip, pre[0]));
       }
     }
     hreg = hn;
@@ -391,10 +413,10 @@ __global__ void __launch_bounds__(512, 1) step_fast_kernel(const StepParams p) {
 }
 
 // ------------------------------------------------------------------ launch
-template <int CELL, typename T, bool GEN, int KV>
+template <int CELL, typename T, bool GEN, int KV, int U, bool PLAIN>
 cudaError_t step_fast_launch_one(const StepParams& p, const StepPlan& plan, cudaStream_t stream, int* resident) {
-  auto kern = step_fast_kernel<CELL, T, GEN, KV>;
-  if (plan.threads > 512 || plan.threads % 32 != 0) return cudaErrorInvalidConfiguration;
+  auto kern = step_fast_kernel<CELL, T, GEN, KV, U, PLAIN>;
+  if (plan.threads > (U == 2 ? 512 : 256) || plan.threads % 32 != 0) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   if (plan.team_ctas > 8) {
@@ -422,25 +444,40 @@ cudaError_t step_fast_launch_one(const StepParams& p, const StepPlan& plan, cuda
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int CELL, typename T, bool GEN>
+// Units per warp: RNN 8; LSTM and GRU 4 when a warp's 16 rows of R fit its
+// registers (KV <= 2), else 2.
+template <int CELL, int KV>
+struct FastU {
+  static constexpr int value = CELL == 2 ? 8 : (KV <= 2 ? 4 : 2);
+};
+
+template <int CELL, typename T, bool GEN, bool PLAIN>
 cudaError_t step_fast_kv(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q) {
   switch (plan.kv) {
-    case 1: return step_fast_launch_one<CELL, T, GEN, 1>(p, plan, s, q);
-    case 2: return step_fast_launch_one<CELL, T, GEN, 2>(p, plan, s, q);
+    case 1: return step_fast_launch_one<CELL, T, GEN, 1, FastU<CELL, 1>::value, PLAIN>(p, plan, s, q);
+    case 2: return step_fast_launch_one<CELL, T, GEN, 2, FastU<CELL, 2>::value, PLAIN>(p, plan, s, q);
     case 4:
-      if constexpr (sizeof(T) == 2) return step_fast_launch_one<CELL, T, GEN, 4>(p, plan, s, q);
+      if constexpr (sizeof(T) == 2) return step_fast_launch_one<CELL, T, GEN, 4, FastU<CELL, 4>::value, PLAIN>(p, plan, s, q);
       break;
     default: break;
   }
   return cudaErrorInvalidConfiguration;
 }
 
+// Units per warp the kernel of a plan uses (for the planner's thread count).
+inline int fast_units_per_warp(int cell, int kv) { return cell == 2 ? 8 : (kv <= 2 ? 4 : 2); }
+
+template <int CELL, typename T>
+cudaError_t step_fast_dtype(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q) {
+  const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
+  if (p.generic_acts) return plain ? step_fast_kv<CELL, T, true, true>(p, plan, s, q) : step_fast_kv<CELL, T, true, false>(p, plan, s, q);
+  return plain ? step_fast_kv<CELL, T, false, true>(p, plan, s, q) : step_fast_kv<CELL, T, false, false>(p, plan, s, q);
+}
+
 template <int CELL>
 cudaError_t step_fast_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q) {
-  const bool gen = p.generic_acts != 0;
-  if (p.dtype == 0)
-    return gen ? step_fast_kv<CELL, float, true>(p, plan, s, q) : step_fast_kv<CELL, float, false>(p, plan, s, q);
-  return gen ? step_fast_kv<CELL, __half, true>(p, plan, s, q) : step_fast_kv<CELL, __half, false>(p, plan, s, q);
+  if (p.dtype == 0) return step_fast_dtype<CELL, float>(p, plan, s, q);
+  return step_fast_dtype<CELL, __half>(p, plan, s, q);
 }
 
 }  // namespace rk
