@@ -162,7 +162,7 @@ class ClockSampler:
 
 def step_kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("rk_step.cuh", "rk_step_launch.cuh"):
+    for name in ("rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh"):
         with open(os.path.join(ROOT, "onnx_lstm_gru_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
