@@ -465,8 +465,9 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
     return RK_OK;
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
-  snprintf(buf, (size_t)len, "proj=simt step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
-           pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid"),
+  const bool tc = p->dtype == RK_F16 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
+  snprintf(buf, (size_t)len, "proj=%s step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
+           tc ? "tc" : "simt", pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid"),
            (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
   return RK_OK;
 }
@@ -527,7 +528,9 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     pp.Xw = xw;
     pp.dtype = p->dtype;
     if (h->profiling) cudaEventRecord(h->ev[0], stream);
-    cudaError_t e = rk::launch_projection_simt(pp, stream);
+    const bool tc = !(h->flags & RK_FORCE_SIMT_PROJECTION) && rk::projection_tc_supported(pp);
+    cudaError_t e = tc ? rk::launch_projection_tc(pp, h->status, h->timeout_ns, stream)
+                       : rk::launch_projection_simt(pp, stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);
     if (h->profiling) cudaEventRecord(h->ev[1], stream);
     h->ev_proj = h->profiling;
@@ -618,7 +621,8 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
     pp.W = tptr(ops->W, eb);
     pp.Xw = xw;
     pp.dtype = p->dtype;
-    e = rk::launch_projection_simt(pp, stream);
+    const bool tc = !(h->flags & RK_FORCE_SIMT_PROJECTION) && rk::projection_tc_supported(pp);
+    e = tc ? rk::launch_projection_tc(pp, status, h->timeout_ns, stream) : rk::launch_projection_simt(pp, stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);
     h->launches += 1;
   }

@@ -87,6 +87,10 @@ struct StepPlan {
 
 // Launchers (defined in the .cu files).  Each returns a cudaError_t.
 cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s);
+// Half projection on tcgen05 tensor cores; cudaErrorNotSupported when the
+// operands do not meet its alignment rules (then the SIMT kernel runs).
+bool projection_tc_supported(const ProjParams& p);
+cudaError_t launch_projection_tc(const ProjParams& p, int* status, long long timeout_ns, cudaStream_t s);
 // Step kernel for one cell and exchange kind.  With resident_teams != nullptr
 // nothing is launched: the kernel is opted into the plan's shared memory /
 // cluster size and the number of teams that can be resident at once is

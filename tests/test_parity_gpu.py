@@ -374,3 +374,24 @@ def test_validation_error_launches_nothing():
         L.encode(pr, X=X, W=torch.zeros(3 * 8 * 2, device="cuda"), R=torch.zeros(5, device="cuda"))
     assert e.value.code == rk.RK_ERR_SHAPE and "GRU: R:" in e.value.message
     assert L.launches() == before
+
+
+@pytest.mark.parametrize("S,N,I,H", [(75, 4, 200, 600), (1, 1, 8, 16), (130, 1, 1024, 256)])
+def test_half_projection_tensor_cores(S, N, I, H):
+    """An RNN with Affine(1, 0), R = 0 and no bias outputs its projection:
+    Y[t] = x_t . W^T.  Half inputs take the tcgen05 projection; the result
+    matches the oracle's projection and the SIMT projection (same float32
+    products of Half values, different summation order)."""
+    pr = rk.Problem("rnn", seq=S, batch=N, input=I, hidden=H, direction="bidirectional", dtype="f16",
+                    activations=[("affine", 1.0, 0.0)] * 2)
+    assert "proj=tc" in layer().plan(pr)
+    rng = np.random.default_rng(S + I)
+    inp = {"X": rng.uniform(-1, 1, (S, N, I)).astype(np.float16),
+           "W": rng.uniform(-0.1, 0.1, (2, H, I)).astype(np.float16),
+           "R": np.zeros((2, H, H), np.float16)}
+    got = run_gpu(pr, inp, outputs=("Y",))
+    want = oracle.projection(inp["X"].astype(np.float64).reshape(S * N, I), inp["W"].astype(np.float64))
+    ref = {"Y": want.reshape(2, S, N, H).transpose(1, 0, 2, 3)}
+    compare(pr, got, ref)
+    simt = run_gpu(pr, inp, outputs=("Y",), flags=rk.RK_FORCE_SIMT_PROJECTION)
+    compare(pr, got, {"Y": simt["Y"]})
