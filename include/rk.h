@@ -86,6 +86,7 @@ enum rk_activation_kind {
 #define RK_FORCE_SIMT_PROJECTION 1u /* Half problems: SIMT projection, no tensor cores */
 #define RK_FORCE_GRID_STEP 2u       /* use the grid-wide step kernel even where a cluster fits */
 #define RK_FORCE_GENERAL_STEP 4u    /* never the one-row-per-cluster register-resident step kernel */
+#define RK_FORCE_SIMT_STEP 8u       /* Half problems: never the tensor-core step kernel */
 
 /* One activation slot (GpuRecurrentActivation): kind plus resolved alpha/beta. */
 typedef struct rk_activation {

@@ -232,6 +232,7 @@ void fill_params_problem(const rk_problem* p, StepParams* sp) {
 
 // Launch (or, with resident != nullptr, size) the step kernel of a plan.
 cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl, cudaStream_t stream, int* resident) {
+  if (pl.kind == rk::kStepTensor) return rk::step_tc_entry(sp, pl, stream, resident, sp.rhglob);
   if (pl.kind == rk::kStepClusterFast) {
     switch (cell) {
       case RK_LSTM: return rk::step_fast_entry<0>(sp, pl, stream, resident);
@@ -278,6 +279,31 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     }
     return teams;
   };
+  // tensor-core kernel: Half layers with a batch worth a dense product
+  // (R . h on tcgen05), every CTA of the launch resident at once
+  if (p->dtype == RK_F16 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
+      !(p->cell == RK_GRU && !p->linear_before_reset) && H % 8 == 0 && N >= 4) {
+    StepPlan pl{};
+    pl.kind = rk::kStepTensor;
+    pl.team_ctas = (H + 15) / 16;
+    pl.nb = std::min(N, 128);
+    pl.nbc = pl.nb <= 64 ? 64 : 128;  // rows of h per TMA box
+    pl.teams_per_dir = (N + 127) / 128;
+    pl.J = 16;
+    pl.threads = 320;
+    pl.grid = D * pl.teams_per_dir * pl.team_ctas;
+    pl.smem = rk::step_tc_smem(G, H);
+    const bool fits = (int)pl.smem <= smem_cap && pl.grid <= h->sms && D * pl.teams_per_dir <= rk::kStateHeader;
+    if (fits && (!check || resident(pl) * pl.team_ctas >= pl.grid)) {
+      sp->team_ctas = pl.team_ctas;
+      sp->J = pl.J;
+      sp->nb = pl.nb;
+      sp->teams_per_dir = pl.teams_per_dir;
+      sp->nbc = pl.nbc;
+      *out = pl;
+      return RK_OK;
+    }
+  }
   // fast kernel: one batch row per cluster, R rows in registers.  Largest
   // cluster (<= 16 CTAs) whose clusters all fit the GPU at once, with 16 to
   // 32 hidden units per CTA (fewer when H itself is smaller).
@@ -467,7 +493,9 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
   const bool tc = p->dtype == RK_F16 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
   snprintf(buf, (size_t)len, "proj=%s step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
-           tc ? "tc" : "simt", pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid"),
+           tc ? "tc" : "simt",
+           pl.kind == rk::kStepTensor ? "tensor"
+                                      : (pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid")),
            (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
   return RK_OK;
 }
@@ -555,7 +583,7 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
   sp.status = h->status;
   sp.timeout_ns = h->timeout_ns;
-  if (pl.kind == rk::kStepGrid) {
+  if (pl.kind == rk::kStepGrid || pl.kind == rk::kStepTensor) {
     cudaError_t e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
   }

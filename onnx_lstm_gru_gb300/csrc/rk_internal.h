@@ -22,6 +22,7 @@ enum StepKind : int {
   kStepCluster = 0,      // a team is one thread-block cluster; h exchanged through DSMEM
   kStepGrid = 1,         // a team spans many SMs; h exchanged through L2 and a bounded barrier
   kStepClusterFast = 2,  // one batch row per cluster, R in registers, no CTA-wide barrier
+  kStepTensor = 3,       // Half: R . h on tcgen05 tensor cores, teams across the grid
 };
 
 // Register tile of the step kernel's R.h product: rows per warp x batch rows.
@@ -108,6 +109,11 @@ size_t step_smem_for(const StepParams& p, const StepPlan& plan);
 // with cudaGetSymbolAddress on the first call for each device).
 constexpr long long kNoAllocScratchFloats = 4LL << 20;  // 16 MiB
 cudaError_t noalloc_scratch(float** scratch, int** status);
+// Tensor-core step kernel (kStepTensor): dynamic shared memory for G gates
+// and hidden H, and the launch (resident != nullptr: occupancy query only).
+// h16 is the Half copy of the exchanged hidden state, [2][D*N][H].
+size_t step_tc_smem(int G, int H);
+cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 // Self-test of the bounded waits (see rk_selftest_timeout).
 cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);
 

@@ -172,13 +172,20 @@ def test_plans_without_device(handle):
     assert "step=fast" in plans["bilstm_s80_b1_i256_h256_f32"] and "ctas=16" in plans["bilstm_s80_b1_i256_h256_f32"]
     assert "step=cluster" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]  # 16 clusters of 16 would not fit at once
     assert "step=grid" in plans["revlstm_peep_clip_s200_b4_i128_h1024_f32"]
-    assert "step=grid" in plans["bilstm_s512_b64_i1024_h1024_f16"]
+    assert "proj=tc step=tensor" in plans["bilstm_s512_b64_i1024_h1024_f16"]
+    assert "step=tensor" in plans["bigru_s128_b8_i512_h512_f16_lbr1"]
     for name, text in plans.items():
         smem = int(re.search(r"smem=(\d+)", text).group(1))
         assert smem <= 232448 - 1024, (name, text)
     empty = rk.Problem("lstm", seq=3, batch=0, input=2, hidden=4)
     assert rk.rk_describe_plan(handle, empty.to_c()) == "noop"
     c2 = workloads.WORKLOADS["bilstm_s80_b1_i256_h256_f32"].problem.to_c()
+    c5 = workloads.WORKLOADS["bilstm_s512_b64_i1024_h1024_f16"].problem.to_c()
+    h3 = rk.rk_create(rk.RK_FORCE_SIMT_STEP | rk.RK_FORCE_SIMT_PROJECTION)
+    try:
+        assert "proj=simt step=grid" in rk.rk_describe_plan(h3, c5)
+    finally:
+        rk.rk_destroy(h3)
     for flags, want in [(rk.RK_FORCE_GRID_STEP, "step=grid"), (rk.RK_FORCE_GENERAL_STEP, "step=cluster")]:
         h2 = rk.rk_create(flags)
         try:

@@ -395,3 +395,39 @@ def test_half_projection_tensor_cores(S, N, I, H):
     compare(pr, got, ref)
     simt = run_gpu(pr, inp, outputs=("Y",), flags=rk.RK_FORCE_SIMT_PROJECTION)
     compare(pr, got, {"Y": simt["Y"]})
+
+
+TC_STEP_CASES = [
+    ("lstm", 40, 5, "bidirectional", 0, "plain"),
+    ("lstm", 96, 130, "reverse", 1, "full"),
+    ("gru", 64, 9, "forward", 0, "full"),
+    ("rnn", 48, 17, "bidirectional", 1, "plain"),
+    ("lstm", 256, 64, "bidirectional", 0, "plain"),
+]
+
+
+@pytest.mark.parametrize("cell,H,N,direction,layout,opts", TC_STEP_CASES)
+def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts):
+    """Half layers with a batch of 4 or more run R . h on the tensor cores
+    (h rounded to Half for the product, state float32); results match the
+    oracle within the Half tolerance and the SIMT step kernel."""
+    kw = dict(clip=1.5) if opts == "full" else {}
+    if opts == "full" and cell == "lstm":
+        kw["input_forget"] = 1
+    if opts == "full":
+        A = {"lstm": 3, "gru": 2, "rnn": 1}[cell]
+        D = 2 if direction == "bidirectional" else 1
+        kw["activations"] = ([("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0), ("tanh", 0, 0)][:A]) * D
+    pr = rk.Problem(cell, seq=7, batch=N, input=24, hidden=H, direction=direction, dtype="f16", layout=layout,
+                    linear_before_reset=1 if cell == "gru" else 0, **kw)
+    assert "step=tensor" in layer().plan(pr)
+    lens = list(np.random.default_rng(N).integers(0, 8, N))
+    inp = rand_inputs(pr, seed=H + N, lens=lens, peep=(opts == "full"), scale=0.15)
+    got = run_gpu(pr, inp)
+    compare(pr, got, run_oracle(pr, inp), lens)
+    simt = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_STEP)
+    compare(pr, got, {k: v for k, v in simt.items() if not k.endswith("_raw")}, lens)
+    again = run_gpu(pr, inp)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
