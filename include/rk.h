@@ -156,9 +156,11 @@ rk_status rk_destroy(rk_handle* h);
  * for S, N > 0, else 0.  Returns -1 for an invalid problem. */
 int64_t rk_xw_length(const rk_problem* p);
 
-/* Floats of state scratch the problem needs (StateLength): the double-buffered
- * hidden state exchanged between blocks of the step kernel plus its barrier
- * and status words.  Returns -1 for an invalid problem. */
+/* Floats of state scratch the problem needs (StateLength): 256 barrier
+ * words, the double-buffered hidden state exchanged between blocks of the
+ * step kernel, 2 * D * N * KP, and a region for r (.) h or the Half copies of
+ * h used by the tensor cores, D * (N + 128) * KP (KP = hidden rounded up to a
+ * multiple of 128).  Returns -1 for an invalid problem. */
 int64_t rk_state_length(const rk_problem* p);
 
 /* Host-only validation of a problem and its operands (sizes, offsets,

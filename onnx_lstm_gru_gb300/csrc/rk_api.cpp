@@ -187,7 +187,10 @@ int64_t xw_len(const rk_problem* p) {
 }
 int64_t kp_of(const rk_problem* p) { return round_up(std::max<int64_t>(p->hidden, 1), rk::kKChunk); }
 int64_t state_len(const rk_problem* p) {
-  return rk::kStateHeader + 3 * (int64_t)dirs_of(p) * p->batch * kp_of(p);
+  // barrier counters, the double-buffered float32 h of the grid kernel, and a
+  // region for r.h (grid kernel) or the Half copies of h (tensor-core kernel)
+  return rk::kStateHeader + 2 * (int64_t)dirs_of(p) * p->batch * kp_of(p) +
+         (int64_t)dirs_of(p) * (p->batch + 128) * kp_of(p);
 }
 
 rk_status ensure_device(rk_handle* h) {

@@ -14,20 +14,24 @@
 // co-resident (cooperative launch).  A CTA keeps its 16 units' G rows of R in
 // shared memory, unit-major (row u*G + g), in the 128-byte swizzled K-major
 // layout the tensor cores read.  Per step:
-//   1. one lane streams h_t (Half, [128 batch rows][H], rows past the team
-//      read as anything and are never used) through a 4-stage ring with TMA,
-//      64 k at a time;
+//   1. one lane streams h_t through an 8-stage ring, one contiguous bulk copy
+//      per 64-wide k block: the Half copy of h is kept in global memory
+//      already in the swizzled K-major layout, one block of (team batch rows
+//      rounded up to 64) x 64 k per k block, written 16 bytes at a time by the
+//      gate threads;
 //   2. one lane issues tcgen05.mma kind::f16 with M = 128 (batch rows),
-//      N = 16 G (the CTA's gate rows), K = 16 per instruction, accumulating
-//      the whole K = H in one fp32 TMEM accumulator (lane = batch row,
-//      column = gate row), and commits to an mbarrier;
+//      N = 16 G (the CTA's gate rows), K = 16 per instruction, 64-wide k
+//      block kb into fp32 TMEM accumulator kb % 4 (lane = batch row, column =
+//      gate row): small-N MMAs into one accumulator would each wait for the
+//      previous one; then commits to an mbarrier;
 //   3. eight warps read the accumulator with tcgen05.ld: thread (warp w,
 //      lane l) takes batch row 32 (w % 4) + l and 8 units (half w / 4), does
 //      the gate arithmetic with its units' c and h in registers and the next
 //      step's xw prefetched, writes Y and the Half copy of the new h;
 //   4. the team passes a counter barrier with a bounded, timed wait.
-// The summation order is fixed by the shape (tensor-core k blocks of 16, in
-// increasing k), so runs are bit-identical.  Every wait is bounded; on
+// The summation order is fixed by the shape (tensor-core k blocks of 16 in
+// increasing k within each accumulator, then ((a0 + a1) + (a2 + a3))), so
+// runs are bit-identical.  Every wait is bounded; on
 // expiry the kernel sets the status word, drains its copies and MMAs, frees
 // its TMEM and returns.
 #include <cuda.h>
@@ -69,12 +73,6 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t par, long long tim
 }
 __device__ __forceinline__ void bar_expect(uint32_t b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -167,9 +165,23 @@ __host__ __device__ inline TcSmem tc_smem_layout(int G, int H) {
   return L;
 }
 
+// Half copy of the exchanged h, pre-arranged for the tensor cores: for every
+// (buffer, direction, team, 64-wide k block) a contiguous block of box rows
+// x 64 k in the 128-byte swizzled K-major layout, so one stage of the ring is
+// one contiguous bulk copy.  Element (row, k) of a block sits at
+// sw128_offset(row, k).
+__device__ __forceinline__ size_t h16_block(const StepParams& p, int buf, int d, int team_in_dir, int kb, int KB,
+                                            int box_rows) {
+  return ((((size_t)buf * p.D + d) * p.teams_per_dir + team_in_dir) * KB + kb) * (size_t)box_rows * SK;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 template <int CELL, bool GEN, bool PLAIN>
-__global__ void __launch_bounds__(STHREADS, 1)
-    step_tc_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmH, __half* __restrict__ h16) {
+__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
   constexpr int NR = SJ * G;      // gate rows of this CTA (MMA N): 64, 48 or 16
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(STHREADS, 1)
   const __half* h0 = static_cast<const __half*>(p.h0);
   const __half* c0 = static_cast<const __half*>(p.c0);
   __half* Y = static_cast<__half*>(p.Y);
-  const size_t hplane = (size_t)p.D * N * H;  // one h16 buffer
+  const int tin = team % p.teams_per_dir;      // team index within its direction
   // rows of h per ring stage: the team's batch rounded up to 64 (the MMA
   // still spans 128 rows; rows past the stage's are never read back)
   const int box_rows = p.nbc;                      // 64 or 128, set by the host
@@ -240,11 +252,14 @@ __global__ void __launch_bounds__(STHREADS, 1)
     mbar_init(smem_u32(&bars[2 * SMAXST]), 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmH)) : "memory");
   }
   // R was written by ordinary stores; the tensor cores read it through the async proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  constexpr uint32_t kTmemCols = NR <= 32 ? 32 : (NR <= 64 ? 64 : 128);
+  // four accumulators (k blocks kb % 4), so consecutive MMAs do not wait on
+  // each other's results; columns 64 apart
+  constexpr int NACC = 4;
+  constexpr uint32_t kAccStride = 64;
+  constexpr uint32_t kTmemCols = NACC * kAccStride;
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                  "r"(kTmemCols)
@@ -273,7 +288,18 @@ __global__ void __launch_bounds__(STHREADS, 1)
       const size_t si = state_index(p, d, bg, j < H ? j : 0);
       hreg[u] = (j < H && h0 != nullptr) ? __half2float(h0[si]) : 0.0f;
       creg[u] = (CELL == 0 && j < H && c0 != nullptr) ? __half2float(c0[si]) : 0.0f;
-      if (j < H) h16[((size_t)d * N + bg) * H + j] = __float2half_rn(hreg[u]);  // h_0 into buffer 0
+      // h_0 into buffer 0 (units past H are zero: the k padding of the product)
+      *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_block(p, 0, d, tin, j / SK, KB, box_rows)) +
+                                 sw128_offset(br, j % SK)) = __float2half_rn(j < H ? hreg[u] : 0.0f);
+    }
+    // k columns past the last CTA's units (up to the 64-wide block) belong to
+    // no CTA: zero them once in both buffers (R is zero there too, but a stale
+    // Inf or NaN times zero would not be)
+    if (rank == C - 1 && uh0 == 0) {
+      for (int k = C * SJ; k < KB * SK; ++k)
+        for (int buf = 0; buf < 2; ++buf)
+          *reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_block(p, buf, d, tin, k / SK, KB, box_rows)) +
+                                     sw128_offset(br, k % SK)) = __float2half_rn(0.0f);
     }
   } else {
 #pragma unroll
@@ -344,7 +370,8 @@ __global__ void __launch_bounds__(STHREADS, 1)
           break;
         }
         bar_expect(su32(&bars[st]), stage_bytes);
-        tma_load_2d(su32(sRing + st * stage_bytes), &tmH, kb * SK, cur * p.D * N + d * N + b0, su32(&bars[st]));
+        bulk_load(su32(sRing + st * stage_bytes), h16 + h16_block(p, cur, d, tin, kb, KB, box_rows), stage_bytes,
+                  su32(&bars[st]));
         armed[st] = (int)ph;
         if (++st == nstages) {
           st = 0;
@@ -364,9 +391,10 @@ __global__ void __launch_bounds__(STHREADS, 1)
         tc_fence_after();
         const uint32_t a0 = su32(sRing + st * stage_bytes);
         const uint32_t b0s = su32(sR + (size_t)kb * NR * 128);
+        const uint32_t tmem_d = tmem_acc + (uint32_t)(kb % NACC) * kAccStride;
 #pragma unroll
         for (int k = 0; k < SK / 16; ++k)
-          tc_mma(tmem_acc, desc_sw128(a0 + k * 32), desc_sw128(b0s + k * 32), idesc, (kb | k) != 0);
+          tc_mma(tmem_d, desc_sw128(a0 + k * 32), desc_sw128(b0s + k * 32), idesc, (kb >= NACC) || (k != 0));
         tc_commit(su32(&bars[SMAXST + st]));
         if (++st == nstages) {
           st = 0;
@@ -389,8 +417,36 @@ __global__ void __launch_bounds__(STHREADS, 1)
         atomicOr(p.status, 1);
       }
       tc_fence_after();
+      // sum of the accumulators in a fixed order: ((a0 + a1) + (a2 + a3))
       uint32_t acc[NCOL];
-      tmem_ld<NCOL>(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(uh0 * G), acc);
+      {
+        const uint32_t ta = tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(uh0 * G);
+        const int nacc = KB < NACC ? KB : NACC;
+        float sum01[NCOL], sum23[NCOL];
+        uint32_t t0[NCOL];
+        tmem_ld<NCOL>(ta, t0);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) sum01[i] = __uint_as_float(t0[i]);
+        if (nacc > 1) {
+          tmem_ld<NCOL>(ta + kAccStride, t0);
+#pragma unroll
+          for (int i = 0; i < NCOL; ++i) sum01[i] += __uint_as_float(t0[i]);
+        }
+        if (nacc > 2) {
+          tmem_ld<NCOL>(ta + 2 * kAccStride, t0);
+#pragma unroll
+          for (int i = 0; i < NCOL; ++i) sum23[i] = __uint_as_float(t0[i]);
+          if (nacc > 3) {
+            tmem_ld<NCOL>(ta + 3 * kAccStride, t0);
+#pragma unroll
+            for (int i = 0; i < NCOL; ++i) sum23[i] += __uint_as_float(t0[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < NCOL; ++i) sum01[i] += sum23[i];
+        }
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) acc[i] = __float_as_uint(sum01[i]);
+      }
       const bool active = s < len;
       const int t = active ? (reverse ? len - 1 - s : s) : s;
       float hn[UH];
@@ -430,32 +486,26 @@ __global__ void __launch_bounds__(STHREADS, 1)
         }
       }
       if (grow) {
-        __half* hdst = h16 + (size_t)nxt * hplane + ((size_t)d * N + bg) * H + j0 + uh0;
-        __half* ydst = Y != nullptr ? Y + y_index(p, t, d, bg, j0 + uh0) : nullptr;
-        if (j0 + uh0 + UH <= H) {
-          __align__(16) __half hv[UH], yv[UH];
+        // the 8 units are one 16-byte chunk of their k block's row br
+        const int jb = j0 + uh0;
+        __half* hdst = reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_block(p, nxt, d, tin, jb / SK, KB, box_rows)) +
+                                                 sw128_offset(br, jb % SK));
+        __half* ydst = Y != nullptr ? Y + y_index(p, t, d, bg, jb) : nullptr;
+        __align__(16) __half hv[UH], yv[UH];
 #pragma unroll
-          for (int u = 0; u < UH; ++u) {
-            hreg[u] = hn[u];
-            hv[u] = __float2half_rn(hn[u]);
-            yv[u] = __float2half_rn(active ? hn[u] : 0.0f);
-          }
-          if (s + 1 < Tn) {
-            if ((reinterpret_cast<uintptr_t>(hdst) & 15) == 0) *reinterpret_cast<uint4*>(hdst) = *reinterpret_cast<const uint4*>(hv);
-            else for (int u = 0; u < UH; ++u) hdst[u] = hv[u];
-          }
-          if (ydst != nullptr) {
-            if ((reinterpret_cast<uintptr_t>(ydst) & 15) == 0) *reinterpret_cast<uint4*>(ydst) = *reinterpret_cast<const uint4*>(yv);
-            else for (int u = 0; u < UH; ++u) ydst[u] = yv[u];
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < UH; ++u) {
-            if (j0 + uh0 + u < H) {
-              hreg[u] = hn[u];
-              if (s + 1 < Tn) hdst[u] = __float2half_rn(hn[u]);
-              if (ydst != nullptr) ydst[u] = __float2half_rn(active ? hn[u] : 0.0f);
-            }
+        for (int u = 0; u < UH; ++u) {
+          const bool in = jb + u < H;
+          if (in) hreg[u] = hn[u];
+          hv[u] = __float2half_rn(in ? hn[u] : 0.0f);
+          yv[u] = __float2half_rn(active ? hn[u] : 0.0f);
+        }
+        if (s + 1 < Tn) *reinterpret_cast<uint4*>(hdst) = *reinterpret_cast<const uint4*>(hv);
+        if (ydst != nullptr) {
+          if (jb + UH <= H && (reinterpret_cast<uintptr_t>(ydst) & 15) == 0) {
+            *reinterpret_cast<uint4*>(ydst) = *reinterpret_cast<const uint4*>(yv);
+          } else {
+            for (int u = 0; u < UH; ++u)
+              if (jb + u < H) ydst[u] = yv[u];
           }
         }
       }
@@ -502,23 +552,6 @@ __global__ void __launch_bounds__(STHREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 template <int CELL, bool GEN, bool PLAIN>
 cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
   auto kern = step_tc_kernel<CELL, GEN, PLAIN>;
@@ -532,18 +565,6 @@ cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream
     *resident = (e == cudaSuccess) ? (per_sm * sms) / plan.team_ctas : 0;
     return e;
   }
-  // h copies: [2 buffers][D * N rows][H] Half, K-major rows for TMA
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)p.H, (cuuint64_t)2 * p.D * p.N};
-  const cuuint64_t strides[1] = {(cuuint64_t)p.H * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)SK, (cuuint32_t)plan.nbc};
-  const cuuint32_t estr[2] = {1, 1};
-  if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, h16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-      CUDA_SUCCESS)
-    return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
   cfg.blockDim = dim3(STHREADS, 1, 1);
@@ -554,7 +575,7 @@ cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, map, h16);
+  return cudaLaunchKernelEx(&cfg, kern, p, h16);
 }
 
 template <int CELL>

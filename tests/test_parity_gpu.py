@@ -337,6 +337,25 @@ def test_caller_scratch_in_one_arena_is_bitwise_equal():
         assert torch.equal(base[k], got[k])
 
 
+@pytest.mark.parametrize("H,N", [(40, 5), (96, 130)])
+def test_tensor_core_step_ignores_stale_scratch(H, N):
+    """The tensor-core step kernel reads its Half h copies in whole 64-wide k
+    blocks and batch blocks; parts no CTA owns must not leak stale scratch.
+    Caller scratch filled with NaN bytes gives the same bits as fresh scratch."""
+    pr = rk.Problem("lstm", seq=6, batch=N, input=16, hidden=H, direction="bidirectional", dtype="f16")
+    assert "step=tensor" in layer().plan(pr)
+    inp = rand_inputs(pr, seed=H * N, scale=0.15)
+    base = run_gpu(pr, inp)
+    c = pr.to_c()
+    nx, ns = rk.rk_xw_length(c), rk.rk_state_length(c)
+    arena = torch.full((nx + ns + 64,), float("nan"), dtype=torch.float32, device="cuda")
+    sc = rk.rk_scratch(arena.data_ptr(), 0, nx, arena.data_ptr(), nx + 4, nx + ns + 64)
+    got = run_gpu(pr, inp, scratch=sc)
+    for k in ("Y_raw", "Y_h_raw", "Y_c_raw"):
+        assert torch.equal(base[k], got[k]), k
+    assert np.isfinite(got["Y"]).all()
+
+
 def test_host_buffer_entry_matches_device_entry():
     w = workloads.WORKLOADS["bigru_s128_b8_i512_h512_f16_lbr0"]
     pr = w.problem
