@@ -160,12 +160,50 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- profile summaries
 
-def step_kernel_source_hash():
+# Source files of each kernel, hashed so a committed ncu summary is only used
+# while the kernel it measured is unchanged.
+KERNEL_SOURCES = {
+    "fast": ("step_kernel", ("rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh")),
+    "cluster": ("step_cluster_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
+    "grid": ("step_grid_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
+    "tensor": ("step_tc_kernel", ("rk_step.cuh", "rk_step_tc.cu")),
+    "proj_tc": ("proj_tc_kernel", ("rk_proj_tc.cu",)),
+    "proj_simt": ("projection", ("rk_proj.cu",)),
+}
+
+
+def kernel_source_hash(files):
     h = hashlib.sha256()
-    for name in ("rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh"):
+    for name in files:
         with open(os.path.join(ROOT, "onnx_lstm_gru_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def step_kernel_source_hash():
+    return kernel_source_hash(KERNEL_SOURCES["fast"][1])
+
+
+def plan_fields(plan: str) -> dict:
+    """'proj=tc step=tensor shape=..' -> {'proj': 'tc', 'step': 'tensor', ...}"""
+    return dict(kv.split("=", 1) for kv in plan.split() if "=" in kv)
+
+
+def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, alu_peak: float, alu_src: str,
+                    workload: str) -> dict:
+    """Roofline entry of one kernel: tensor-core kernels against the measured
+    dense bf16 rate (fp16 has the same nominal dense rate), FP32 SIMT kernels
+    against the FP32 FMA rate derived from the SM count and clock."""
+    achieved = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
+    name, files = KERNEL_SOURCES[kind]
+    traffic = profiled_traffic(name, workload, kernel_source_hash(files))
+    if kind in ("tensor", "proj_tc"):
+        peak = float(peaks["bf16_tflops"])
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": name,
+                "peak_source": "measured dense bf16 burst; fp16 runs at the same nominal dense rate"}
+    return {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s", "frac": achieved / alu_peak,
+            "traffic": traffic, "kernel": name, "peak_source": alu_src}
 
 
 def profiled_traffic(kernel: str, workload: str, source_hash: str):
@@ -351,17 +389,19 @@ def run_gb300(args):
     proj_flops = 2.0 * pr.seq * pr.batch * pr.input * G * H * D
     if proj_ms <= 0.0:  # projection fused into the step kernel
         step_flops += proj_flops
-    dominant = "step" if step_ms >= proj_ms else "projection"
-    kflops, kms = (step_flops, step_ms) if dominant == "step" else (proj_flops, proj_ms)
-    achieved = kflops / (kms * 1e-3) / 1e12
-    src_hash = step_kernel_source_hash()
-    traffic = profiled_traffic("step_kernel", name, src_hash) if dominant == "step" else None
-    roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak_tflops, "unit": "TFLOP/s",
-                "frac": achieved / alu_peak_tflops, "traffic": traffic, "kernel": f"{dominant} kernel",
-                "peak_source": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz"}
+    pf = plan_fields(plan)
+    alu_src = f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz"
+    step_kind = pf.get("step", "fast")
+    proj_kind = "proj_tc" if pf.get("proj") == "tc" else "proj_simt"
+    r_step = kernel_roofline(step_kind, step_flops, step_ms, peaks, alu_peak_tflops, alu_src, name)
+    r_proj = kernel_roofline(proj_kind, proj_flops, proj_ms, peaks, alu_peak_tflops, alu_src, name) \
+        if proj_ms > 0 else None
+    roofline = r_step if (r_proj is None or step_ms >= proj_ms) else r_proj
+    roofline = dict(roofline, others=[r for r in (r_step, r_proj) if r is not None and r is not roofline])
     # whole-layer roofline: max(FLOPs at peak, compulsory bytes at HBM) / measured time
     cbytes = workloads.compulsory_bytes(pr, {**inp, **{n: None for n in outs}})
-    t_flops = flops / (alu_peak_tflops * 1e12)
+    # FLOPs at the peak of the unit each kernel runs on
+    t_flops = step_flops / (r_step["peak"] * 1e12) + (proj_flops / (r_proj["peak"] * 1e12) if r_proj else 0.0)
     t_bytes = cbytes / (float(peaks["hbm_gbs"]) * 1e9)
     layer_roofline = {"t_roofline_us": max(t_flops, t_bytes) * 1e6, "t_measured_us": ms_local * 1e3,
                       "frac": max(t_flops, t_bytes) / (ms_local * 1e-3), "flops": flops, "compulsory_bytes": cbytes,
