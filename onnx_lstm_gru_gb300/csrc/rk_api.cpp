@@ -290,19 +290,24 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     pl.kind = rk::kStepTensor;
     pl.team_ctas = (H + 15) / 16;
     pl.nb = std::min(N, 128);
-    pl.nbc = pl.nb <= 64 ? 64 : 128;  // rows of h per TMA box
+    // rows of h per 128 k: a team of at most 64 rows pairs two 64-wide k
+    // blocks in one 128-row tile
+    pl.nbc = pl.nb <= 64 ? 64 : 128;
     pl.teams_per_dir = (N + 127) / 128;
     pl.J = 16;
     pl.threads = 320;
     pl.grid = D * pl.teams_per_dir * pl.team_ctas;
-    pl.smem = rk::step_tc_smem(G, H);
-    const bool fits = (int)pl.smem <= smem_cap && pl.grid <= h->sms && D * pl.teams_per_dir <= rk::kStateHeader;
+    pl.stages = rk::step_tc_stages(G, H, (size_t)smem_cap);
+    pl.smem = rk::step_tc_smem(G, H, std::max(pl.stages, 2));
+    // one publication flag per CTA in the state header
+    const bool fits = pl.stages >= 2 && pl.grid <= h->sms && pl.grid <= rk::kStateHeader;
     if (fits && (!check || resident(pl) * pl.team_ctas >= pl.grid)) {
       sp->team_ctas = pl.team_ctas;
       sp->J = pl.J;
       sp->nb = pl.nb;
       sp->teams_per_dir = pl.teams_per_dir;
       sp->nbc = pl.nbc;
+      sp->stages = pl.stages;
       *out = pl;
       return RK_OK;
     }

@@ -60,6 +60,7 @@ struct StepParams {
   int teams_per_dir;
   int rows_pad;        // rows of R held per CTA (warps x rows per warp)
   int nbc;             // batch rows per h chunk in shared memory
+  int stages;          // kStepTensor: 16 KB stages of the h ring
   // grid exchange (kStepGrid) and status
   float* hglob;        // [2][D*N][KP]
   float* rhglob;       // [D*N][KP]
@@ -81,6 +82,7 @@ struct StepPlan {
   StepShape shape;
   int threads;
   int team_ctas, J, KP, nb, teams_per_dir, rows_pad, nbc;
+  int stages;  // kStepTensor: 16 KB stages of the h ring
   size_t smem;
   int grid;
   int kv;     // kStepClusterFast: KP / kKChunk (R chunks per lane and row)
@@ -109,10 +111,13 @@ size_t step_smem_for(const StepParams& p, const StepPlan& plan);
 // with cudaGetSymbolAddress on the first call for each device).
 constexpr long long kNoAllocScratchFloats = 4LL << 20;  // 16 MiB
 cudaError_t noalloc_scratch(float** scratch, int** status);
-// Tensor-core step kernel (kStepTensor): dynamic shared memory for G gates
-// and hidden H, and the launch (resident != nullptr: occupancy query only).
-// h16 is the Half copy of the exchanged hidden state, [2][D*N][H].
-size_t step_tc_smem(int G, int H);
+// Tensor-core step kernel (kStepTensor): dynamic shared memory for G gates,
+// hidden H and a ring of `stages` 16 KB stages; the most stages (2..8) that
+// fit in smem_cap bytes (0 if not even 2 fit); and the launch (resident !=
+// nullptr: occupancy query only).  h16 is the Half copy of the exchanged
+// hidden state, 2 x D x teams x 16 KB regions per 128 k.
+size_t step_tc_smem(int G, int H, int stages);
+int step_tc_stages(int G, int H, size_t smem_cap);
 cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 // Self-test of the bounded waits (see rk_selftest_timeout).
 cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);

@@ -1,0 +1,702 @@
+// rk_step_tc.cuh -- persistent recurrent-step kernel on the tcgen05 tensor
+// cores, for Half layers whose batch makes R . h a dense product.
+//
+// What it computes is the same as rk_step.cuh (web page "Recurrent layers",
+// sections "How a layer runs" and "Arithmetic and determinism"): per step and
+// gate row pre = ((xw + rec) + Wb) + Rb with rec = R_row . h_prev, then
+// peepholes, clip, activation and state update (LSTM, RNN, GRU with
+// linear_before_reset = 1).  The state (h, c) stays float32 in registers;
+// the product's h operand is the state rounded to Half, so R (Half, exact)
+// times that operand is exact in float32 and summed in float32.
+//
+// Layout: a team per (direction, group of up to 128 batch rows); a team is
+// ceil(H / 16) CTAs, each owning 16 hidden units, all CTAs of the launch
+// co-resident (cooperative launch).  A CTA keeps its 16 units' G rows of R in
+// shared memory, unit-major (row u*G + g), in the 128-byte swizzled K-major
+// layout the tensor cores read.  The Half copy of the exchanged h lives in
+// global memory as 16 KB regions already in that layout, one 128-row x 64 k
+// tile each: for a team of more than 64 rows a region is one 64-wide k block
+// of rows 0..127; for a team of at most 64 rows (PAIR) a region holds two
+// consecutive k blocks, rows of the even block at tile rows 32 (b / 16) +
+// b % 16 and of the odd block 16 rows further, so no tile row is wasted.
+// Per step:
+//   1. the producer warp copies each region of h_t into a ring of 16 KB
+//      stages with one bulk copy, as soon as the CTAs owning it have
+//      published it;
+//   2. one lane issues tcgen05.mma kind::f16 with M = 128 (tile rows),
+//      N = 16 G (the CTA's gate rows), K = 16 per instruction, into fp32 TMEM
+//      accumulators (lane = tile row, column = gate row): one accumulator, or
+//      with PAIR one for even and one for odd k blocks, each MMA reading the
+//      whole tile so that the lanes of the other block's rows hold unused
+//      products; operand descriptors are precomputed so issue keeps up with
+//      the tensor core; then commits to an mbarrier;
+//   3. eight warps read the accumulators with tcgen05.ld (warp w sees lanes
+//      32 (w % 4) .. + 31).  Without PAIR thread (w, l) takes batch row
+//      32 (w % 4) + l and 8 units; with PAIR lanes l and l + 16 both hold
+//      batch row 16 (w % 4) + l, one the even and one the odd partial sum,
+//      they swap halves with a shuffle and take 4 units each.  Each thread
+//      does the gate arithmetic with its units' c and h in registers and the
+//      next step's xw prefetched, writes its piece of the Half copy of the new
+//      h and publishes it (proxy fence, then a release store of the CTA's step
+//      count to its flag), then writes Y.
+// The three roles run their own loops, linked by mbarriers; no barrier spans
+// the CTA or the team inside the step loop.  The summation order is fixed by
+// the shape (tensor-core k blocks of 16 in increasing k, then even + odd), so
+// runs are bit-identical.  Every wait is bounded; on expiry the kernel sets
+// the status word, drains its copies and MMAs, frees its TMEM and returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "rk_step.cuh"
+
+namespace rk {
+
+namespace {
+
+constexpr int SB = 128;          // batch rows per team (MMA M)
+constexpr int SK = 64;           // k per ring stage (one 128-byte swizzle atom of Half)
+constexpr int SSTAGE = 16 * 1024; // one ring stage: a 128-row x 64 k tile of Half
+constexpr int SMAXST = 8;         // most ring stages
+constexpr int SJ = 16;           // hidden units per CTA
+constexpr int STHREADS = 320;    // 8 gate warps + producer warp + MMA warp
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ bool bar_try(uint32_t b, uint32_t par) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(par)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t par, long long timeout_ns) {
+  if (bar_try(b, par)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    if (bar_try(b, par)) return true;
+    if ((it & 15u) == 0 && (long long)(global_ns() - t0) > timeout_ns) return false;
+  }
+}
+__device__ __forceinline__ void bar_expect(uint32_t b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16, A and B Half, D float32, both K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(SB >> 4) << 24);
+}
+// Byte offset of element (row r, k) of a K-major tile of 64-element rows in
+// the 128-byte swizzled layout (16-byte chunks of a row XORed with r % 8).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
+  const int chunk = (k >> 3) ^ (r & 7);
+  return (uint32_t)(r * 128 + chunk * 16 + (k & 7) * 2);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+// NCOL consecutive accumulator columns of this warp's 32 lanes (NCOL a
+// multiple of 4), then wait for the loads.
+template <int NCOL>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[NCOL]) {
+  static_assert(NCOL % 4 == 0, "columns in groups of 4");
+  int c = 0;
+#pragma unroll
+  for (; c + 16 <= NCOL; c += 16) tmem_ld16(taddr + c, r + c);
+  if constexpr (NCOL % 16 >= 8) {
+    tmem_ld8(taddr + c, r + c);
+    c += 8;
+  }
+  if constexpr (NCOL % 8 == 4) tmem_ld4(taddr + c, r + c);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// UH Half values to 16 (UH = 8) or 8 (UH = 4) aligned bytes.
+template <int UH>
+__device__ __forceinline__ void store_halves(__half* dst, const __half (&v)[UH]) {
+  if constexpr (UH == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(v);
+  else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(v);
+}
+
+
+// Shared memory: [R slice: KB blocks of (16 G rows x 64 k) Half][ring: stages x 16 KB][barriers][biases]
+struct TcSmem {
+  size_t r, ring, bar, bias, total;
+};
+__host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages) {
+  TcSmem L{};
+  const int KB = (H + SK - 1) / SK;
+  const size_t rbytes = (size_t)KB * SJ * G * SK * 2;
+  size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
+  L.r = o;    o += (rbytes + 1023) & ~(size_t)1023;
+  L.ring = o; o += (size_t)stages * SSTAGE;
+  L.bar = o;  o += 256;
+  L.bias = o; o += (size_t)2 * SJ * G * 4 + 3 * SJ * 4;
+  L.total = o;
+  return L;
+}
+
+// Region (16 KB, 8192 Half) of the Half h copy: buffer, direction, team, region.
+__device__ __forceinline__ size_t h16_region(const StepParams& p, int buf, int d, int team_in_dir, int region, int NREG) {
+  return ((((size_t)buf * p.D + d) * p.teams_per_dir + team_in_dir) * NREG + region) * (size_t)(SSTAGE / 2);
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int CELL, bool GEN, bool PLAIN, bool PAIR>
+__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16) {
+  constexpr int G = CellInfo<CELL>::G;
+  constexpr int A = CellInfo<CELL>::A;
+  constexpr int NR = SJ * G;           // gate rows of this CTA (MMA N): 64, 48 or 16
+  constexpr int UH = PAIR ? 4 : 8;     // units per gate thread
+  constexpr int NCOL = UH * G;         // accumulator values per gate thread
+  constexpr int BPR = PAIR ? 2 : 1;    // k blocks per region
+  constexpr uint32_t kTmemCols = 128;  // accumulators at columns 0 and 64
+  constexpr uint32_t kOddCol = 64;
+  static_assert(NR <= (int)kOddCol, "accumulators fit the allocation");
+  extern __shared__ unsigned char tsm_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
+  const int NST = p.stages;
+  const TcSmem L = tc_smem_layout(G, p.H, NST);
+  unsigned char* sR = base + (L.r - 1024);
+  unsigned char* sRing = base + (L.ring - 1024);
+  // full[8], empty[8], done, pub, free, drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SMAXST + 4);
+  float* wb_s = reinterpret_cast<float*>(base + (L.bias - 1024));
+  float* rb_s = wb_s + NR;
+  float* pp_s = rb_s + NR;
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H, N = p.N, S = p.S, Tn = p.T;
+  const int C = p.team_ctas;
+  // teams interleaved over the block index: consecutive blocks tend to share
+  // a die, and a team spread evenly over both dies keeps a steadier pace
+  // than one split unevenly
+  const int nteams = gridDim.x / C;
+  const int team = blockIdx.x % nteams, rank = blockIdx.x / nteams;
+  const int d = team / p.teams_per_dir;
+  const int tin = team % p.teams_per_dir;  // team index within its direction
+  const int b0 = tin * SB;
+  const int nbt = min(SB, N - b0);
+  const int j0 = rank * SJ;
+  const int KB = (H + SK - 1) / SK;
+  const int NREG = (KB + BPR - 1) / BPR;  // regions per step
+  const bool reverse = p.direction == 1 || (p.direction == 2 && d == 1);
+  const size_t GH = (size_t)G * H;
+  const __half* R = static_cast<const __half*>(p.R);
+  const __half* Bias = static_cast<const __half*>(p.Bias);
+  const __half* P = static_cast<const __half*>(p.P);
+  const __half* h0 = static_cast<const __half*>(p.h0);
+  const __half* c0 = static_cast<const __half*>(p.c0);
+  __half* Y = static_cast<__half*>(p.Y);
+
+  // ---------------- prologue: R slice (unit-major rows, swizzled), biases, barriers, TMEM
+  for (size_t e = tid; e < (size_t)KB * NR * SK; e += blockDim.x) {
+    const int kb = (int)(e / ((size_t)NR * SK));
+    const int rem = (int)(e % ((size_t)NR * SK));
+    const int r = rem / SK, kk = rem % SK;
+    const int u = r / G, g = r % G, k = kb * SK + kk;
+    __half v = __float2half(0.0f);
+    if (j0 + u < H && k < H) v = R[((size_t)d * GH + (size_t)g * H + j0 + u) * H + k];
+    *reinterpret_cast<__half*>(sR + (size_t)kb * NR * 128 + sw128_offset(r, kk)) = v;
+  }
+  for (int e = tid; e < NR; e += blockDim.x) {
+    const int u = e / G, g = e % G;
+    const bool ok = j0 + u < H && Bias != nullptr;
+    wb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + (size_t)g * H + j0 + u]) : 0.0f;
+    rb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + GH + (size_t)g * H + j0 + u]) : 0.0f;
+  }
+  for (int e = tid; e < 3 * SJ; e += blockDim.x) {
+    const int u = e / 3, g = e % 3;
+    pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? __half2float(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < SMAXST; ++i) {
+      mbar_init(smem_u32(&bars[i]), 1);
+      mbar_init(smem_u32(&bars[SMAXST + i]), 1);
+    }
+    mbar_init(smem_u32(&bars[2 * SMAXST]), 1);      // accumulators complete (MMA commit)
+    mbar_init(smem_u32(&bars[2 * SMAXST + 1]), 8);  // gate warps' h copies written
+    mbar_init(smem_u32(&bars[2 * SMAXST + 2]), 8);  // gate warps read the accumulators
+    mbar_init(smem_u32(&bars[2 * SMAXST + 3]), 1);  // final MMA drain
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // R was written by ordinary stores; the tensor cores read it through the async proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // gate threads: warps 0..7 (warp w reads TMEM lanes 32 (w % 4) .. + 31)
+  const bool gate_warp = warp < 8;
+  const int q = warp & 3;
+  const bool odd_lane = PAIR && lane >= 16;
+  const int br = PAIR ? 16 * q + (lane & 15) : 32 * q + lane;  // batch row within the team
+  const int uh0 = (warp >> 2) * 8 + (odd_lane ? 4 : 0);        // first of this thread's units
+  const bool grow = gate_warp && br < nbt;
+  const int bg = b0 + br;  // global batch row
+  float hreg[UH], creg[UH];
+  int len = Tn;
+  // address of (this thread's batch row, unit j) in buffer buf of the Half h copy
+  auto h16_at = [&](int buf, int j) {
+    const int kb = j / SK;
+    const int row = PAIR ? 32 * (br >> 4) + 16 * (kb & 1) + (br & 15) : br;
+    return reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_region(p, buf, d, tin, kb / BPR, NREG)) +
+                                     sw128_offset(row, j % SK));
+  };
+  if (grow) {
+    if (p.lens != nullptr) {
+      len = p.lens[bg];
+      len = len < 0 ? 0 : (len > S ? S : len);
+      len = len > Tn ? Tn : len;
+    }
+    __align__(16) __half hv[UH];
+#pragma unroll
+    for (int u = 0; u < UH; ++u) {
+      const int j = j0 + uh0 + u;
+      const size_t si = state_index(p, d, bg, j < H ? j : 0);
+      hreg[u] = (j < H && h0 != nullptr) ? __half2float(h0[si]) : 0.0f;
+      creg[u] = (CELL == 0 && j < H && c0 != nullptr) ? __half2float(c0[si]) : 0.0f;
+      hv[u] = __float2half_rn(j < H ? hreg[u] : 0.0f);  // units past H: the k padding of the product
+    }
+    store_halves<UH>(h16_at(0, j0 + uh0), hv);  // h_0 into buffer 0
+    // k columns past the last CTA's units (up to the 64-wide block) belong to
+    // no CTA: zero them once in both buffers (R is zero there too, but a stale
+    // Inf or NaN times zero would not be)
+    if (rank == C - 1 && uh0 == 0) {
+      for (int k = C * SJ; k < KB * SK; ++k)
+        for (int buf = 0; buf < 2; ++buf) *h16_at(buf, k) = __float2half_rn(0.0f);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < UH; ++u) hreg[u] = creg[u] = 0.0f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_acc = *tmem_slot;
+
+  // Publication flags: flags[rank] = how many h copies this CTA has published
+  // (h_0 counts as one).  The copy of a region for step s waits until the
+  // CTAs owning its units have published h_s, i.e. their flags reach s + 1;
+  // no barrier spans the team.  Reusing the two h buffers is safe without
+  // one: a CTA writes h_{s+1} only after its product of step s consumed h_s
+  // of every CTA, and each CTA published h_s after its own copies of h_{s-1},
+  // the buffer being overwritten, had landed.
+  unsigned* flags = p.counters + (size_t)team * C;
+  const uint32_t bar_done = su32(&bars[2 * SMAXST]);      // accumulators of a step complete
+  const uint32_t bar_pub = su32(&bars[2 * SMAXST + 1]);   // 8 gate-warp arrivals
+  const uint32_t bar_free = su32(&bars[2 * SMAXST + 2]);  // accumulators read (8 gate warps)
+  const uint32_t bar_drain = su32(&bars[2 * SMAXST + 3]);
+  // gate warps: make this CTA's new h copies visible to the async proxy of
+  // other CTAs, then thread 0 releases the flag once all 8 warps are in
+  auto publish = [&](unsigned value, uint32_t pub_parity) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_pub) : "memory");
+    if (tid == 0) {
+      if (bar_wait(bar_pub, pub_parity, p.timeout_ns)) {
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + rank), "r"(value) : "memory");
+      } else {
+        abort_flag = 1;
+        atomicOr(p.status, 1);
+      }
+    }
+  };
+  uint32_t pub_parity = 0;
+  if (gate_warp) publish(1u, pub_parity++ & 1u);
+
+  // xw of this thread's units for step s: Xw[d][m(t, bg)][g*H + j]
+  const size_t xw_tstride = p.layout == 0 ? (size_t)N * GH : GH;
+  const float* xw_row = p.xw + xw_index(p, d, 0, grow ? bg : 0, 0, 0);
+  // the UH units of a gate are contiguous floats: 16-byte loads when they
+  // are aligned and all inside H
+  const bool xw_vec = (j0 + uh0 + UH <= H) && (H % 4 == 0) && (reinterpret_cast<uintptr_t>(p.xw) % 16 == 0);
+  auto load_xw = [&](int s, float (&x)[UH * G]) {
+    const bool on = grow && s < len && s < Tn;
+    const float* qx = xw_row + (size_t)(reverse ? len - 1 - s : s) * xw_tstride;
+    if (on && xw_vec) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int v = 0; v < UH / 4; ++v) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(qx + (size_t)g * H + j0 + uh0 + 4 * v));
+          x[(4 * v + 0) * G + g] = a.x;
+          x[(4 * v + 1) * G + g] = a.y;
+          x[(4 * v + 2) * G + g] = a.z;
+          x[(4 * v + 3) * G + g] = a.w;
+        }
+    } else {
+#pragma unroll
+      for (int u = 0; u < UH; ++u)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int j = j0 + uh0 + u;
+          x[u * G + g] = (on && j < H) ? __ldg(qx + (size_t)g * H + j) : 0.0f;
+        }
+    }
+  };
+  const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
+  const float clip = PLAIN ? 0.0f : p.clip;
+  const bool input_forget = !PLAIN && p.input_forget;
+  constexpr int RPB = SK * BPR / SJ;  // CTAs owning one region: 4 or 8
+  constexpr int kMaxFlagWords = 8;    // a team has at most 256 CTAs
+
+  if (warp == 8) {
+    // ---------------- producer warp: poll the team's flags (lane l reads CTAs
+    // l, l + 32, ...), then one bulk copy per region whose owners have all
+    // published, in k order
+    int armed[SMAXST];
+    for (int i = 0; i < SMAXST; ++i) armed[i] = -1;
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int s = 0; s < Tn && ok; ++s) {
+      const unsigned want = (unsigned)s + 1u;
+      const unsigned long long t0 = global_ns();
+      int next = 0;  // next region to copy
+      while (next < NREG && ok) {
+        unsigned m[kMaxFlagWords];
+#pragma unroll
+        for (int i = 0; i < kMaxFlagWords; ++i) {
+          const int c = 32 * i + lane;
+          bool rd = true;
+          if (32 * i < C && c < C && c >= next * RPB) rd = ld_acquire_gpu(flags + c) >= want;
+          m[i] = 32 * i < C ? __ballot_sync(0xffffffffu, rd) : 0xffffffffu;
+        }
+        // regions [next, end) are ready (RPB divides 32: no region spans two words)
+        int end = next;
+        bool go = true;
+#pragma unroll
+        for (int i = 0; i < kMaxFlagWords; ++i) {
+          while (go && end < NREG && end * RPB < 32 * (i + 1)) {
+            const unsigned bm = ((1u << RPB) - 1u) << ((end * RPB) & 31);
+            if ((m[i] & bm) == bm) ++end;
+            else go = false;
+          }
+        }
+        __syncwarp();
+        if (end == next) {
+          const bool give_up = lane == 0 && (abort_flag || (long long)(global_ns() - t0) > p.timeout_ns);
+          if (__any_sync(0xffffffffu, give_up)) ok = false;
+          continue;
+        }
+        if (lane == 0) {
+          // the owners' generic-proxy stores, acquired above, are read by the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        for (; next < end; ++next) {
+          if (lane == 0) {
+            if (bar_wait(su32(&bars[SMAXST + st]), ph ^ 1u, p.timeout_ns)) {
+              bar_expect(su32(&bars[st]), SSTAGE);
+              bulk_load(su32(sRing + st * SSTAGE), h16 + h16_region(p, s & 1, d, tin, next, NREG), SSTAGE,
+                        su32(&bars[st]));
+              armed[st] = (int)ph;
+            } else {
+              ok = false;
+            }
+          }
+          if (++st == NST) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      }
+    }
+    if (!ok && lane == 0) {
+      abort_flag = 1;
+      atomicOr(p.status, 1);
+    }
+    // drain: copies this CTA issued must land before it exits
+    if (lane == 0)
+      for (int i = 0; i < SMAXST; ++i)
+        if (armed[i] >= 0) bar_wait(su32(&bars[i]), (uint32_t)armed[i], p.timeout_ns);
+  } else if (warp == 9) {
+    // ---------------- MMA lane: acc[128 x NR] += tile[128 x 64] . R_block[NR x 64]^T per k block
+    if (lane == 0) {
+      // only the start-address field (address / 16, bits 0-13) differs
+      // between the MMAs' descriptors; every address stays below 256 KB
+      const uint32_t idesc = idesc_f16(NR);
+      const uint64_t adesc0 = desc_sw128(su32(sRing));
+      const uint64_t bdesc0 = desc_sw128(su32(sR));
+      constexpr uint64_t kK16 = 32 >> 4;                      // 16 Half of k
+      constexpr uint64_t kStageD = SSTAGE >> 4;
+      constexpr uint64_t kBlockD = (uint64_t)NR * 128 >> 4;  // one k block of R
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int s = 0; s < Tn && ok; ++s) {
+        // the gate warps must have read the previous step's accumulators
+        if (s > 0 && !bar_wait(bar_free, (uint32_t)((s - 1) & 1), p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint64_t bd = bdesc0;
+        for (int r = 0; r < NREG; ++r) {
+          if (abort_flag || !bar_wait(su32(&bars[st]), ph, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = adesc0 + (uint64_t)st * kStageD;
+          const uint32_t first = r != 0 ? 1u : 0u;
+          tc_mma(tmem_acc, ad, bd, idesc, first);
+          tc_mma(tmem_acc, ad + kK16, bd + kK16, idesc, 1u);
+          tc_mma(tmem_acc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
+          tc_mma(tmem_acc, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
+          bd += kBlockD;
+          if (PAIR && 2 * r + 1 < KB) {
+            tc_mma(tmem_acc + kOddCol, ad, bd, idesc, first);
+            tc_mma(tmem_acc + kOddCol, ad + kK16, bd + kK16, idesc, 1u);
+            tc_mma(tmem_acc + kOddCol, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
+            tc_mma(tmem_acc + kOddCol, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
+            bd += kBlockD;
+          }
+          tc_commit(su32(&bars[SMAXST + st]));
+          if (++st == NST) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (ok) tc_commit(bar_done);  // accumulators of step s complete
+      }
+      if (!ok) {
+        abort_flag = 1;
+        atomicOr(p.status, 1);
+      }
+      // drain: every MMA this CTA issued completes before TMEM is freed
+      tc_commit(bar_drain);
+      bar_wait(bar_drain, 0u, p.timeout_ns);
+    }
+  } else {
+    // ---------------- gate warps
+    float xv[UH * G];
+    load_xw(0, xv);
+    bool ok = true;
+    // columns of units (w / 4) * 8 .. + 7 of this warp's 32 lanes
+    const uint32_t ta = tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)((warp >> 2) * 8 * G);
+    for (int s = 0; s < Tn; ++s) {
+      if (abort_flag || !bar_wait(bar_done, (uint32_t)(s & 1), p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float acc[NCOL];
+      if constexpr (PAIR) {
+        // lane l < 16 holds the even-block sums of batch row br, lane l + 16
+        // the odd-block sums of the same row; each keeps 4 of the 8 units
+        // and sends the other 4 to its partner (lane ^ 16)
+        uint32_t ev[8 * G], od[8 * G];
+        tmem_ld<8 * G>(ta, ev);
+        tmem_ld<8 * G>(ta + kOddCol, od);
+        if (KB < 2) {
+#pragma unroll
+          for (int i = 0; i < 8 * G; ++i) od[i] = 0u;  // no odd block
+        }
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) {
+          const float mine = __uint_as_float(odd_lane ? od[NCOL + i] : ev[i]);
+          const float give = __uint_as_float(odd_lane ? od[i] : ev[NCOL + i]);
+          const float got = __shfl_xor_sync(0xffffffffu, give, 16);
+          acc[i] = odd_lane ? got + mine : mine + got;  // even + odd
+        }
+      } else {
+        uint32_t a[NCOL];
+        tmem_ld<NCOL>(ta, a);
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i) acc[i] = __uint_as_float(a[i]);
+      }
+      // the accumulators may be overwritten by the next step's product
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_free) : "memory");
+      const bool active = s < len;
+      const int t = active ? (reverse ? len - 1 - s : s) : s;
+      float hn[UH];
+#pragma unroll
+      for (int u = 0; u < UH; ++u) {
+        const int c = (uh0 + u) * G;
+        float pre[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) pre[g] = ((xv[u * G + g] + acc[u * G + g]) + wb_s[c + g]) + rb_s[c + g];
+        hn[u] = hreg[u];
+        if constexpr (CELL == 0) {
+          // rows u*4 + g: i, o, f, c
+          float pi = pre[0], po = pre[1], pf = pre[2], pc = pre[3];
+          if (has_p) {
+            pi = pi + pp_s[(uh0 + u) * 3 + 0] * creg[u];
+            pf = pf + pp_s[(uh0 + u) * 3 + 2] * creg[u];
+          }
+          const float ig = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pi));
+          const float fg = input_forget ? 1.0f - ig : act<GEN, 0>(p, d * A + 0, clip_pre(clip, pf));
+          const float cg = act<GEN, 1>(p, d * A + 1, clip_pre(clip, pc));
+          const float cn = fg * creg[u] + ig * cg;
+          if (has_p) po = po + pp_s[(uh0 + u) * 3 + 1] * cn;
+          const float og = act<GEN, 0>(p, d * A + 0, clip_pre(clip, po));
+          if (active) {
+            hn[u] = og * act<GEN, 1>(p, d * A + 2, cn);
+            creg[u] = cn;
+          }
+        } else if constexpr (CELL == 1) {
+          // linear_before_reset = 1: h~ = g((xw_h + r*(rec_h + Rb_h)) + Wb_h)
+          const float z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
+          const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
+          const float ph = (xv[u * G + 2] + r * (acc[u * G + 2] + rb_s[c + 2])) + wb_s[c + 2];
+          const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, ph));
+          if (active) hn[u] = (1.0f - z) * hc + z * hreg[u];
+        } else {
+          if (active) hn[u] = act<GEN, 1>(p, d * A + 0, clip_pre(clip, pre[0]));
+        }
+      }
+      // the UH units are one 8- or 16-byte piece of their k block's row
+      const int jb = j0 + uh0;
+      __align__(16) __half hv[UH], yv[UH];
+#pragma unroll
+      for (int u = 0; u < UH; ++u) {
+        const bool in = jb + u < H;
+        if (in) hreg[u] = hn[u];
+        hv[u] = __float2half_rn(in ? hn[u] : 0.0f);
+        yv[u] = __float2half_rn(active ? hn[u] : 0.0f);
+      }
+      if (s + 1 < Tn) {
+        if (grow) store_halves<UH>(h16_at((s + 1) & 1, jb), hv);
+        publish((unsigned)s + 2u, pub_parity++ & 1u);
+      }
+      if (grow && Y != nullptr) {
+        __half* ydst = Y + y_index(p, t, d, bg, jb);
+        if (jb + UH <= H && (reinterpret_cast<uintptr_t>(ydst) % (2 * UH)) == 0) {
+          store_halves<UH>(ydst, yv);
+        } else {
+          for (int u = 0; u < UH; ++u)
+            if (jb + u < H) ydst[u] = yv[u];
+        }
+      }
+      load_xw(s + 1, xv);
+    }
+    if (!ok) {
+      abort_flag = 1;
+      atomicOr(p.status, 1);
+    }
+    // ---------------- outputs: zero Y past the loop, final states
+    if (grow && ok && !abort_flag) {
+#pragma unroll
+      for (int u = 0; u < UH; ++u) {
+        const int j = j0 + uh0 + u;
+        if (j >= H) continue;
+        if (Y != nullptr)
+          for (int t = Tn; t < S; ++t) Y[y_index(p, t, d, bg, j)] = __float2half_rn(0.0f);
+        const bool zero = S > 0 && len == 0;
+        const size_t si = state_index(p, d, bg, j);
+        if (p.Yh != nullptr) static_cast<__half*>(p.Yh)[si] = __float2half_rn(zero ? 0.0f : hreg[u]);
+        if (CELL == 0 && p.Yc != nullptr) static_cast<__half*>(p.Yc)[si] = __float2half_rn(zero ? 0.0f : creg[u]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_acc), "r"(kTmemCols) : "memory");
+  }
+}
+
+template <int CELL, bool GEN, bool PLAIN, bool PAIR>
+cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
+  auto kern = step_tc_kernel<CELL, GEN, PLAIN, PAIR>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  if (e != cudaSuccess) return e;
+  if (resident != nullptr) {
+    int per_sm = 0, dev = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, STHREADS, plan.smem);
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    *resident = (e == cudaSuccess) ? (per_sm * sms) / plan.team_ctas : 0;
+    return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+  cfg.blockDim = dim3(STHREADS, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, h16);
+}
+
+template <bool PAIR>
+cudaError_t step_tc_pair_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16) {
+  const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
+  const bool gen = p.generic_acts != 0;
+  switch (p.cell) {
+    case 0:
+      if (gen) return plain ? step_tc_launch<0, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<0, true, false, PAIR>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<0, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<0, false, false, PAIR>(p, plan, s, q, h16);
+    case 1:
+      if (gen) return plain ? step_tc_launch<1, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<1, true, false, PAIR>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<1, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<1, false, false, PAIR>(p, plan, s, q, h16);
+    default:
+      if (gen) return plain ? step_tc_launch<2, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<2, true, false, PAIR>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<2, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<2, false, false, PAIR>(p, plan, s, q, h16);
+  }
+}
+
+}  // namespace
+
+// One translation unit per tile arrangement (they compile in parallel).
+cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
+cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
+
+}  // namespace rk
