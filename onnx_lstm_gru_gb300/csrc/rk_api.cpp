@@ -299,8 +299,11 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     pl.grid = D * pl.teams_per_dir * pl.team_ctas;
     pl.stages = rk::step_tc_stages(G, H, (size_t)smem_cap);
     pl.smem = rk::step_tc_smem(G, H, std::max(pl.stages, 2));
-    // one publication flag per CTA in the state header
-    const bool fits = pl.stages >= 2 && pl.grid <= h->sms && pl.grid <= rk::kStateHeader;
+    // one publication flag per CTA in the state header, each team's starting
+    // on a 32-byte boundary; one polling lane per 128 k
+    const int teams = D * pl.teams_per_dir;
+    const bool fits = pl.stages >= 2 && pl.grid <= h->sms &&
+                      teams * ((pl.team_ctas + 7) / 8 * 8) <= rk::kStateHeader && (H + 63) / 64 <= 32;
     if (fits && (!check || resident(pl) * pl.team_ctas >= pl.grid)) {
       sp->team_ctas = pl.team_ctas;
       sp->J = pl.J;

@@ -208,6 +208,9 @@ __global__ void __launch_bounds__(TTHREADS, 1)
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
+      // shared memory stays below 256 KB, so adding address / 16 to the
+      // start-address field never carries out of it
+      const uint64_t adesc0 = smem_desc_sw128(su32(sA)), bdesc0 = smem_desc_sw128(su32(sB));
       for (int tile = blockIdx.x; tile < ntiles && !abort_flag; tile += gridDim.x) {
         if (!bar_wait(su32(&bars[10 + acc]), acc_phase ^ 1u, timeout_ns)) {
           give_up();
@@ -223,12 +226,13 @@ __global__ void __launch_bounds__(TTHREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = su32(sA + stage * kStageBytesA), b0 = su32(sB + stage * kStageBytesB);
+          // descriptors differ only in the start-address field (address / 16):
+          // advance 16 elements (32 bytes) along K inside the swizzle atom
+          const uint64_t ad = adesc0 + (uint64_t)stage * (kStageBytesA >> 4);
+          const uint64_t bd = bdesc0 + (uint64_t)stage * (kStageBytesB >> 4);
+          tc_mma(tmem_d, ad, bd, kIdesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < TBK / 16; ++k) {
-            // advance 16 elements (32 bytes) along K inside the swizzle atom
-            tc_mma(tmem_d, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), kIdesc, (kb | k) != 0);
-          }
+          for (int k = 1; k < TBK / 16; ++k) tc_mma(tmem_d, ad + 2 * k, bd + 2 * k, kIdesc, 1u);
           tc_commit(su32(&bars[4 + stage]));  // stage free once these MMAs complete
           if (++stage == TSTAGES) {
             stage = 0;

@@ -179,6 +179,11 @@ __host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages) {
 __device__ __forceinline__ size_t h16_region(const StepParams& p, int buf, int d, int team_in_dir, int region, int NREG) {
   return ((((size_t)buf * p.D + d) * p.teams_per_dir + team_in_dir) * NREG + region) * (size_t)(SSTAGE / 2);
 }
+__device__ __forceinline__ uint4 ld_acquire_gpu_v4(const unsigned* p) {
+  uint4 v;
+  asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -331,7 +336,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // one: a CTA writes h_{s+1} only after its product of step s consumed h_s
   // of every CTA, and each CTA published h_s after its own copies of h_{s-1},
   // the buffer being overwritten, had landed.
-  unsigned* flags = p.counters + (size_t)team * C;
+  // (a team's flags start on a 32-byte boundary: stride C rounded up to 8)
+  unsigned* flags = p.counters + (size_t)team * ((C + 7) & ~7);
   const uint32_t bar_done = su32(&bars[2 * SMAXST]);      // accumulators of a step complete
   const uint32_t bar_pub = su32(&bars[2 * SMAXST + 1]);   // 8 gate-warp arrivals
   const uint32_t bar_free = su32(&bars[2 * SMAXST + 2]);  // accumulators read (8 gate warps)
@@ -387,13 +393,17 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
   const float clip = PLAIN ? 0.0f : p.clip;
   const bool input_forget = !PLAIN && p.input_forget;
-  constexpr int RPB = SK * BPR / SJ;  // CTAs owning one region: 4 or 8
-  constexpr int kMaxFlagWords = 8;    // a team has at most 256 CTAs
+  constexpr int RPB = SK * BPR / SJ;  // CTAs owning one region: 4 or 8 (a multiple of 4)
+
+  // Regions are taken in a fixed order per CTA, starting after the region
+  // this CTA helps write, so that one late region does not hold up the
+  // product of the others; the order (hence the summation order of each
+  // unit) depends only on the CTA's rank.
+  const int rot = (rank / RPB + 1) % NREG;
 
   if (warp == 8) {
-    // ---------------- producer warp: poll the team's flags (lane l reads CTAs
-    // l, l + 32, ...), then one bulk copy per region whose owners have all
-    // published, in k order
+    // ---------------- producer warp: lane l polls the flags of region l's
+    // owners, then one bulk copy per ready region, in this CTA's order
     int armed[SMAXST];
     for (int i = 0; i < SMAXST; ++i) armed[i] = -1;
     int st = 0;
@@ -402,29 +412,29 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     for (int s = 0; s < Tn && ok; ++s) {
       const unsigned want = (unsigned)s + 1u;
       const unsigned long long t0 = global_ns();
-      int next = 0;  // next region to copy
-      while (next < NREG && ok) {
-        unsigned m[kMaxFlagWords];
+      unsigned taken = 0;  // regions copied this step (bit r)
+      int pos = 0;         // regions issued so far, in this CTA's order
+      while (pos < NREG && ok) {
+        bool rd = true;
+        if (lane < NREG && !((taken >> lane) & 1u)) {
 #pragma unroll
-        for (int i = 0; i < kMaxFlagWords; ++i) {
-          const int c = 32 * i + lane;
-          bool rd = true;
-          if (32 * i < C && c < C && c >= next * RPB) rd = ld_acquire_gpu(flags + c) >= want;
-          m[i] = 32 * i < C ? __ballot_sync(0xffffffffu, rd) : 0xffffffffu;
-        }
-        // regions [next, end) are ready (RPB divides 32: no region spans two words)
-        int end = next;
-        bool go = true;
-#pragma unroll
-        for (int i = 0; i < kMaxFlagWords; ++i) {
-          while (go && end < NREG && end * RPB < 32 * (i + 1)) {
-            const unsigned bm = ((1u << RPB) - 1u) << ((end * RPB) & 31);
-            if ((m[i] & bm) == bm) ++end;
-            else go = false;
+          for (int o = 0; o < RPB; o += 4) {
+            const uint4 v = ld_acquire_gpu_v4(flags + lane * RPB + o);
+            const int c = lane * RPB + o;
+            rd = rd && (c + 0 >= C || v.x >= want) && (c + 1 >= C || v.y >= want) && (c + 2 >= C || v.z >= want) &&
+                 (c + 3 >= C || v.w >= want);
           }
         }
+        const unsigned ready = __ballot_sync(0xffffffffu, rd) | taken;
+        int end = pos;
+        while (end < NREG) {
+          int r = end + rot;
+          r = r >= NREG ? r - NREG : r;
+          if (!((ready >> r) & 1u)) break;
+          ++end;
+        }
         __syncwarp();
-        if (end == next) {
+        if (end == pos) {
           const bool give_up = lane == 0 && (abort_flag || (long long)(global_ns() - t0) > p.timeout_ns);
           if (__any_sync(0xffffffffu, give_up)) ok = false;
           continue;
@@ -433,12 +443,14 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
           // the owners' generic-proxy stores, acquired above, are read by the async proxy
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-        for (; next < end; ++next) {
+        for (; pos < end; ++pos) {
+          int r = pos + rot;
+          r = r >= NREG ? r - NREG : r;
+          taken |= 1u << r;
           if (lane == 0) {
             if (bar_wait(su32(&bars[SMAXST + st]), ph ^ 1u, p.timeout_ns)) {
               bar_expect(su32(&bars[st]), SSTAGE);
-              bulk_load(su32(sRing + st * SSTAGE), h16 + h16_region(p, s & 1, d, tin, next, NREG), SSTAGE,
-                        su32(&bars[st]));
+              bulk_load(su32(sRing + st * SSTAGE), h16 + h16_region(p, s & 1, d, tin, r, NREG), SSTAGE, su32(&bars[st]));
               armed[st] = (int)ph;
             } else {
               ok = false;
@@ -481,15 +493,17 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
           break;
         }
         tc_fence_after();
-        uint64_t bd = bdesc0;
-        for (int r = 0; r < NREG; ++r) {
+        for (int pos = 0; pos < NREG; ++pos) {
+          int r = pos + rot;
+          r = r >= NREG ? r - NREG : r;
           if (abort_flag || !bar_wait(su32(&bars[st]), ph, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t ad = adesc0 + (uint64_t)st * kStageD;
-          const uint32_t first = r != 0 ? 1u : 0u;
+          uint64_t bd = bdesc0 + (uint64_t)(r * BPR) * kBlockD;
+          const uint32_t first = pos != 0 ? 1u : 0u;
           tc_mma(tmem_acc, ad, bd, idesc, first);
           tc_mma(tmem_acc, ad + kK16, bd + kK16, idesc, 1u);
           tc_mma(tmem_acc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
