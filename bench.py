@@ -20,6 +20,7 @@ precision definition) on bounded samples of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -48,6 +49,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--seq-cut", type=int, default=None,
+                    help="profiling aid: the workload with its sequence cut to this many steps (workload name gets "
+                         "a _seqN suffix; not the headline configuration)")
     return ap.parse_args()
 
 
@@ -299,6 +303,9 @@ def run_gb300(args):
     rk.build()
     name = args.workload or workloads.HEADLINE
     w = workloads.WORKLOADS[name]
+    if args.seq_cut:
+        w = dataclasses.replace(w, problem=dataclasses.replace(w.problem, seq=min(args.seq_cut, w.problem.seq)))
+        name = f"{name}_seq{w.problem.seq}"
     pr = w.problem
     inp = workloads.make_inputs(w)
     tdt = torch.float32 if pr.dtype == "f32" else torch.float16
