@@ -240,14 +240,28 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   __half* Y = static_cast<__half*>(p.Y);
 
   // ---------------- prologue: R slice (unit-major rows, swizzled), biases, barriers, TMEM
-  for (size_t e = tid; e < (size_t)KB * NR * SK; e += blockDim.x) {
-    const int kb = (int)(e / ((size_t)NR * SK));
-    const int rem = (int)(e % ((size_t)NR * SK));
-    const int r = rem / SK, kk = rem % SK;
+  // 8 consecutive k (16 bytes) at a time: H is a multiple of 8, so a chunk
+  // is wholly inside or wholly past H, and lands as one 16-byte piece of the
+  // swizzled row; element loads when R is not 16-byte aligned
+  const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
+  for (int e = tid; e < KB * NR * (SK / 8); e += blockDim.x) {
+    const int kb = e / (NR * (SK / 8));
+    const int rem = e % (NR * (SK / 8));
+    const int r = rem / (SK / 8), kk = (rem % (SK / 8)) * 8;
     const int u = r / G, g = r % G, k = kb * SK + kk;
-    __half v = __float2half(0.0f);
-    if (j0 + u < H && k < H) v = R[((size_t)d * GH + (size_t)g * H + j0 + u) * H + k];
-    *reinterpret_cast<__half*>(sR + (size_t)kb * NR * 128 + sw128_offset(r, kk)) = v;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j0 + u < H && k < H) {
+      const __half* src = R + ((size_t)d * GH + (size_t)g * H + j0 + u) * H + k;
+      if (r_vec) {
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        __align__(16) __half t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = src[i];
+        v = *reinterpret_cast<const uint4*>(t8);
+      }
+    }
+    *reinterpret_cast<uint4*>(sR + (size_t)kb * NR * 128 + sw128_offset(r, kk)) = v;
   }
   for (int e = tid; e < NR; e += blockDim.x) {
     const int u = e / G, g = e % G;

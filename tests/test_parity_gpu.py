@@ -337,6 +337,24 @@ def test_caller_scratch_in_one_arena_is_bitwise_equal():
         assert torch.equal(base[k], got[k])
 
 
+@pytest.mark.parametrize("cell", ["lstm", "gru", "rnn"])
+def test_tensor_core_step_with_odd_offsets(cell):
+    """Operands at odd element offsets (R not 16-byte aligned: element loads
+    of the R slice; Y pieces stored element-wise) give the oracle's result
+    and leave the sentinels around the outputs untouched."""
+    pr = rk.Problem(cell, seq=5, batch=6, input=24, hidden=72, direction="bidirectional", dtype="f16",
+                    linear_before_reset=1 if cell == "gru" else 0)
+    assert "step=tensor" in layer().plan(pr)
+    inp = rand_inputs(pr, seed=77, scale=0.15)
+    got = run_gpu(pr, inp, in_off=3, out_off=5)
+    compare(pr, got, run_oracle(pr, inp), None)
+    # unaligned X and W take the SIMT projection: compare against it
+    aligned = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_PROJECTION)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], aligned[k]), k
+
+
 @pytest.mark.parametrize("H,N", [(40, 5), (96, 130)])
 def test_tensor_core_step_ignores_stale_scratch(H, N):
     """The tensor-core step kernel reads its Half h copies in whole 64-wide k
