@@ -34,6 +34,9 @@ __device__ __forceinline__ float widen<__half>(__half v) { return __half2float(v
 template <typename T>
 __global__ void __launch_bounds__(256) proj_simt_kernel(int M, int N, int K, const T* __restrict__ X,
                                                          const T* __restrict__ W, float* __restrict__ Xw) {
+  // the step kernel after this one may be launched early (programmatic
+  // dependent launch); it waits for this grid before reading Xw
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ __align__(16) float As[BK][BM + PADM];
   __shared__ __align__(16) float Bs[BK][BN + PADM];
   const int d = blockIdx.z;
@@ -134,6 +137,9 @@ __device__ __forceinline__ float4 load4_row<__half>(const __half* p) {
 template <typename T, int PBM>
 __global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K, const T* __restrict__ X,
                                                              const T* __restrict__ W, float* __restrict__ Xw) {
+  // the step kernel after this one may be launched early (programmatic
+  // dependent launch); it waits for this grid before reading Xw
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int E = PipeElem<T>::per16, LD = PipeElem<T>::ld;
   constexpr int RM = PBM / 8;  // rows per thread
   extern __shared__ __align__(16) unsigned char psm[];

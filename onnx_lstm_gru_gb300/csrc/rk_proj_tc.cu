@@ -123,6 +123,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __global__ void __launch_bounds__(TTHREADS, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, int D, float* __restrict__ Xw, int vec_store, int* status, long long timeout_ns) {
+  // the step kernel after this one may be launched early (programmatic
+  // dependent launch); it waits for this grid before reading Xw
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ unsigned char tsm_raw[];
   // 1024-byte aligned stage buffers (128-byte swizzle atoms)
   unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);

@@ -98,6 +98,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// Wait until the grids this one depends on (programmatic dependent launch)
+// have completed and their writes are visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream, if launched as a programmatic
+// dependent, start being scheduled.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -543,6 +549,11 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
 
   const int npairs = Jc * nbt;
   const uint32_t h_bytes = (uint32_t)nbt * (uint32_t)H * 4u;
+  // The cluster kernel's launch may overlap the projection that writes Xw
+  // (programmatic dependent launch); wait for it before the first Xw read.
+  // Xw is read with coherent loads (__ldcg): a read-only-path load may be
+  // scheduled ahead of the wait.
+  if constexpr (!GRID) grid_dependency_wait();
 
   // ---------------- the steps (step 3), all in this launch
   for (int s = 0; s < p.T && alive; ++s) {
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
       pact = s < pL;
       pt = pact ? (reverse ? pL - 1 - s : s) : s;
 #pragma unroll
-      for (int g = 0; g < G; ++g) xwv[g] = pact ? __ldg(p.xw + xw_index(p, d, pt, b0 + pb, g, j0 + pj)) : 0.0f;
+      for (int g = 0; g < G; ++g) xwv[g] = pact ? __ldcg(p.xw + xw_index(p, d, pt, b0 + pb, g, j0 + pj)) : 0.0f;
     }
     bool timed_out = false;
     if constexpr (!GRID) {
@@ -592,8 +603,8 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
           xz = xwv[0];
           xr = xwv[1];
         } else {
-          xz = active ? __ldg(p.xw + xw_index(p, d, t, b0 + bl, 0, j0 + jl)) : 0.0f;
-          xr = active ? __ldg(p.xw + xw_index(p, d, t, b0 + bl, 1, j0 + jl)) : 0.0f;
+          xz = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, 0, j0 + jl)) : 0.0f;
+          xr = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, 1, j0 + jl)) : 0.0f;
         }
         const float hp = hown[bl * J + jl];
         const float pz = ((xz + gs[(size_t)(0 * Jp + jl) * nb_ld + bl]) + wb_s[0 * Jp + jl]) + rb_s[0 * Jp + jl];
@@ -637,7 +648,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
         if (idx == tid) {
           xv[g] = xwv[g];
         } else {
-          xv[g] = active ? __ldg(p.xw + xw_index(p, d, t, b0 + bl, g, j0 + jl)) : 0.0f;
+          xv[g] = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, g, j0 + jl)) : 0.0f;
         }
       }
       const float hp = hown[bl * J + jl];

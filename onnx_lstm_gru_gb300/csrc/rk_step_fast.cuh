@@ -314,7 +314,10 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
     const bool on = gl && s < len && s < Tn;
     const float* q = xw_base + (size_t)(reverse ? len - 1 - s : s) * xw_tstride;
 #pragma unroll
-    for (int g = 0; g < G; ++g) x[g] = on ? __ldg(q + (size_t)g * H) : 0.0f;
+    // a coherent load: the projection may still have been running when this
+    // kernel started, and a read-only-path load could be moved ahead of the
+    // dependency wait
+    for (int g = 0; g < G; ++g) x[g] = on ? __ldcg(q + (size_t)g * H) : 0.0f;
   };
 
   const uint32_t h_bytes = (uint32_t)H * 4u;
@@ -322,6 +325,10 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
     if (Tn > 1) mbar_arrive_expect_tx(smem_u32(&bars[1]), h_bytes);
     if (lbr0 && Tn > 0) mbar_arrive_expect_tx(smem_u32(&bars[2]), h_bytes);
   }
+  // The launch may overlap the projection that writes Xw (programmatic
+  // dependent launch): everything above only reads operands the projection
+  // does not touch; wait for it before the first Xw read.
+  grid_dependency_wait();
   float xv[G];
   load_xw(0, xv);
 
@@ -428,13 +435,17 @@ cudaError_t step_fast_launch_one(const StepParams& p, const StepPlan& plan, cuda
   cfg.blockDim = dim3((unsigned)plan.threads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)plan.team_ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the projection (the previous kernel on the stream) runs;
+  // the kernel waits for it before reading Xw
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = resident != nullptr ? 1 : 2;
   if (resident != nullptr) {
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);

@@ -23,18 +23,21 @@ cudaError_t step_launch_one(const StepParams& p, const StepPlan& plan, cudaStrea
   cfg.blockDim = dim3((unsigned)plan.threads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (!GRID) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)plan.team_ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the projection runs; waits for it before reading Xw
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
   } else {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
   }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (!GRID && resident_teams == nullptr) ? 2 : 1;
   if (resident_teams != nullptr) {
     if (!GRID) {
       int n = 0;
