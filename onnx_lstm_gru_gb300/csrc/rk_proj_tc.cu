@@ -40,6 +40,7 @@ constexpr int TTHREADS = 192;
 constexpr uint32_t kStageBytesA = TBM * TBK * 2;  // 16 KB
 constexpr uint32_t kStageBytesB = TBN * TBK * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;               // two 256-column accumulators
+static_assert(2 * TBN <= (int)kTmemCols, "both accumulators fit the TMEM allocation");
 constexpr size_t kTcSmem = (size_t)TSTAGES * (kStageBytesA + kStageBytesB) + 1024 /* alignment */ + 256 /* barriers */;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
