@@ -286,6 +286,33 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   // (R . h on tcgen05), every CTA of the launch resident at once
   if (p->dtype == RK_F16 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
       !(p->cell == RK_GRU && !p->linear_before_reset) && H % 8 == 0 && N >= 4) {
+    // a team of at most 64 rows whose units fit one cluster at 32 per CTA
+    // publishes h inside the cluster (remote mbarrier arrivals), far faster
+    // than global flags; teams never wait on each other
+    const int Cc = (H + 31) / 32;
+    if (N <= 64 && Cc <= 16 && (H + 63) / 64 <= 32) {
+      StepPlan pl{};
+      pl.kind = rk::kStepTensor;
+      pl.team_ctas = Cc;
+      pl.nb = N;
+      pl.nbc = 64;
+      pl.teams_per_dir = 1;
+      pl.J = 32;
+      pl.threads = 320;
+      pl.grid = D * Cc;
+      pl.stages = rk::step_tc_stages(G, H, 32, (size_t)smem_cap);
+      pl.smem = rk::step_tc_smem(G, H, std::max(pl.stages, 2), 32);
+      if (pl.stages >= 2 && (!check || resident(pl) >= 1)) {
+        sp->team_ctas = pl.team_ctas;
+        sp->J = pl.J;
+        sp->nb = pl.nb;
+        sp->teams_per_dir = pl.teams_per_dir;
+        sp->nbc = pl.nbc;
+        sp->stages = pl.stages;
+        *out = pl;
+        return RK_OK;
+      }
+    }
     StepPlan pl{};
     pl.kind = rk::kStepTensor;
     pl.team_ctas = (H + 15) / 16;
@@ -297,8 +324,8 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     pl.J = 16;
     pl.threads = 320;
     pl.grid = D * pl.teams_per_dir * pl.team_ctas;
-    pl.stages = rk::step_tc_stages(G, H, (size_t)smem_cap);
-    pl.smem = rk::step_tc_smem(G, H, std::max(pl.stages, 2));
+    pl.stages = rk::step_tc_stages(G, H, 16, (size_t)smem_cap);
+    pl.smem = rk::step_tc_smem(G, H, std::max(pl.stages, 2), 16);
     // one publication flag per CTA in the state header, each team's starting
     // on a 32-byte boundary; one polling lane per 128 k
     const int teams = D * pl.teams_per_dir;

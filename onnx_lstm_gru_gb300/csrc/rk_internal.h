@@ -112,12 +112,14 @@ size_t step_smem_for(const StepParams& p, const StepPlan& plan);
 constexpr long long kNoAllocScratchFloats = 4LL << 20;  // 16 MiB
 cudaError_t noalloc_scratch(float** scratch, int** status);
 // Tensor-core step kernel (kStepTensor): dynamic shared memory for G gates,
-// hidden H and a ring of `stages` 16 KB stages; the most stages (2..8) that
+// hidden H, `units` hidden units per CTA (16, or 32 for a team that is one
+// cluster) and a ring of `stages` 16 KB stages; the most stages (2..8) that
 // fit in smem_cap bytes (0 if not even 2 fit); and the launch (resident !=
-// nullptr: occupancy query only).  h16 is the Half copy of the exchanged
-// hidden state, 2 x D x teams x 16 KB regions per 128 k.
-size_t step_tc_smem(int G, int H, int stages);
-int step_tc_stages(int G, int H, size_t smem_cap);
+// nullptr: occupancy query only: co-resident teams, or clusters for a
+// cluster team).  h16 is the Half copy of the exchanged hidden state,
+// 2 x D x teams x 16 KB regions per 128 k.
+size_t step_tc_smem(int G, int H, int stages, int units);
+int step_tc_stages(int G, int H, int units, size_t smem_cap);
 cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 // Self-test of the bounded waits (see rk_selftest_timeout).
 cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);

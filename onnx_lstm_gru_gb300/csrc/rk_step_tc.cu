@@ -6,20 +6,22 @@
 namespace rk {
 
 cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
-  return step_tc_pair_dispatch<false>(p, plan, s, resident, h16);
+  return step_tc_mode_dispatch<0>(p, plan, s, resident, h16);
 }
 
-size_t step_tc_smem(int G, int H, int stages) { return tc_smem_layout(G, H, stages).total; }
+size_t step_tc_smem(int G, int H, int stages, int units) { return tc_smem_layout(G, H, stages, units).total; }
 
-int step_tc_stages(int G, int H, size_t smem_cap) {
+int step_tc_stages(int G, int H, int units, size_t smem_cap) {
   for (int st = SMAXST; st >= 2; --st)
-    if (tc_smem_layout(G, H, st).total <= smem_cap) return st;
+    if (tc_smem_layout(G, H, st, units).total <= smem_cap) return st;
   return 0;
 }
 
 cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16) {
-  // the plan pads a team's rows to 64 (two k blocks per tile) or 128
+  // 32 units per CTA: a cluster team; else the plan pads a team's rows to
+  // 64 (two k blocks per tile) or 128
   __half* hp = static_cast<__half*>(h16);
+  if (plan.J == SJC) return step_tc_cluster(p, plan, s, resident, hp);
   return plan.nbc == 64 ? step_tc_pairs(p, plan, s, resident, hp) : step_tc_rows(p, plan, s, resident, hp);
 }
 

@@ -17,8 +17,10 @@
 // global memory as 16 KB regions already in that layout, one 128-row x 64 k
 // tile each: for a team of more than 64 rows a region is one 64-wide k block
 // of rows 0..127; for a team of at most 64 rows (PAIR) a region holds two
-// consecutive k blocks, rows of the even block at tile rows 32 (b / 16) +
-// b % 16 and of the odd block 16 rows further, so no tile row is wasted.
+// consecutive k blocks, rows of the even block at tile rows 32 (b % 4) +
+// b / 4 and of the odd block 16 rows further, so no tile row is wasted and
+// a small batch spreads over the four TMEM lane quarters (the four SM
+// sub-partitions that run the gate arithmetic).
 // Per step:
 //   1. the producer warp copies each region of h_t into a ring of 16 KB
 //      stages with one bulk copy, as soon as the CTAs owning it have
@@ -33,8 +35,8 @@
 //   3. eight warps read the accumulators with tcgen05.ld (warp w sees lanes
 //      32 (w % 4) .. + 31).  Without PAIR thread (w, l) takes batch row
 //      32 (w % 4) + l and 8 units; with PAIR lanes l and l + 16 both hold
-//      batch row 16 (w % 4) + l, one the even and one the odd partial sum,
-//      they swap halves with a shuffle and take 4 units each.  Each thread
+//      batch row 4 l + w % 4, one the even and one the odd partial sum,
+//      they swap halves with a shuffle and take half the units each.  Each thread
 //      does the gate arithmetic with its units' c and h in registers and the
 //      next step's xw prefetched, writes its piece of the Half copy of the new
 //      h and publishes it (proxy fence, then a release store of the CTA's step
@@ -61,7 +63,8 @@ constexpr int SB = 128;          // batch rows per team (MMA M)
 constexpr int SK = 64;           // k per ring stage (one 128-byte swizzle atom of Half)
 constexpr int SSTAGE = 16 * 1024; // one ring stage: a 128-row x 64 k tile of Half
 constexpr int SMAXST = 8;         // most ring stages
-constexpr int SJ = 16;           // hidden units per CTA
+constexpr int SJ = 16;           // hidden units per CTA (teams published by flags)
+constexpr int SJC = 32;          // hidden units per CTA of a cluster team
 constexpr int STHREADS = 320;    // 8 gate warps + producer warp + MMA warp
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -79,6 +82,24 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t par, long long tim
   const unsigned long long t0 = global_ns();
   for (unsigned it = 1;; ++it) {
     if (bar_try(b, par)) return true;
+    if ((it & 15u) == 0 && (long long)(global_ns() - t0) > timeout_ns) return false;
+  }
+}
+// The same wait with cluster-scope acquire, for arrivals from other CTAs.
+__device__ __forceinline__ bool bar_wait_cluster(uint32_t b, uint32_t par, long long timeout_ns) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(par)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    if (try_once()) return true;
     if ((it & 15u) == 0 && (long long)(global_ns() - t0) > timeout_ns) return false;
   }
 }
@@ -162,15 +183,15 @@ __device__ __forceinline__ void store_halves(__half* dst, const __half (&v)[UH])
 struct TcSmem {
   size_t r, ring, bar, bias, total;
 };
-__host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages) {
+__host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages, int sj) {
   TcSmem L{};
   const int KB = (H + SK - 1) / SK;
-  const size_t rbytes = (size_t)KB * SJ * G * SK * 2;
+  const size_t rbytes = (size_t)KB * sj * G * SK * 2;
   size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
   L.r = o;    o += (rbytes + 1023) & ~(size_t)1023;
   L.ring = o; o += (size_t)stages * SSTAGE;
   L.bar = o;  o += 256;
-  L.bias = o; o += (size_t)2 * SJ * G * 4 + 3 * SJ * 4;
+  L.bias = o; o += (size_t)2 * sj * G * 4 + 3 * sj * 4;
   L.total = o;
   return L;
 }
@@ -190,26 +211,34 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-template <int CELL, bool GEN, bool PLAIN, bool PAIR>
+// MODE 0: teams of more than 64 rows, one k block per tile, 16 units per
+// CTA, published by flags; MODE 1: teams of at most 64 rows, paired k
+// blocks, 16 units per CTA, flags; MODE 2: as MODE 1 with 32 units per CTA
+// and the team one thread-block cluster, published by remote mbarrier
+// arrivals instead of flags.
+template <int CELL, bool GEN, bool PLAIN, int MODE>
 __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16) {
+  constexpr bool PAIR = MODE >= 1;
+  constexpr bool CLU = MODE == 2;
+  constexpr int SJT = CLU ? SJC : SJ;  // hidden units per CTA
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
-  constexpr int NR = SJ * G;           // gate rows of this CTA (MMA N): 64, 48 or 16
-  constexpr int UH = PAIR ? 4 : 8;     // units per gate thread
+  constexpr int NR = SJT * G;          // gate rows of this CTA (MMA N): 16 to 128
+  constexpr int UH = PAIR ? SJT / 4 : SJT / 2;  // units per gate thread: 4 or 8
   constexpr int NCOL = UH * G;         // accumulator values per gate thread
   constexpr int BPR = PAIR ? 2 : 1;    // k blocks per region
-  constexpr uint32_t kTmemCols = 128;  // accumulators at columns 0 and 64
-  constexpr uint32_t kOddCol = 64;
-  static_assert(NR <= (int)kOddCol, "accumulators fit the allocation");
+  constexpr uint32_t kOddCol = SJT * 4;  // odd-block accumulator (>= NR columns after the even one)
+  constexpr uint32_t kTmemCols = 2 * kOddCol;  // 128 or 256
+  static_assert(NR <= (int)kOddCol && 2 * kOddCol <= 512, "accumulators fit the allocation");
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const int NST = p.stages;
-  const TcSmem L = tc_smem_layout(G, p.H, NST);
+  const TcSmem L = tc_smem_layout(G, p.H, NST, SJT);
   unsigned char* sR = base + (L.r - 1024);
   unsigned char* sRing = base + (L.ring - 1024);
-  // full[8], empty[8], done, pub, free, drain
+  // full[8], empty[8], done, pub, free, drain, cluster publication[2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SMAXST + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SMAXST + 6);
   float* wb_s = reinterpret_cast<float*>(base + (L.bias - 1024));
   float* rb_s = wb_s + NR;
   float* pp_s = rb_s + NR;
@@ -222,12 +251,20 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // a die, and a team spread evenly over both dies keeps a steadier pace
   // than one split unevenly
   const int nteams = gridDim.x / C;
-  const int team = blockIdx.x % nteams, rank = blockIdx.x / nteams;
+  int team, rank;
+  if constexpr (CLU) {
+    // one team per cluster of C CTAs
+    team = blockIdx.x / C;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  } else {
+    team = blockIdx.x % nteams;
+    rank = blockIdx.x / nteams;
+  }
   const int d = team / p.teams_per_dir;
   const int tin = team % p.teams_per_dir;  // team index within its direction
   const int b0 = tin * SB;
   const int nbt = min(SB, N - b0);
-  const int j0 = rank * SJ;
+  const int j0 = rank * SJT;
   const int KB = (H + SK - 1) / SK;
   const int NREG = (KB + BPR - 1) / BPR;  // regions per step
   const bool reverse = p.direction == 1 || (p.direction == 2 && d == 1);
@@ -269,7 +306,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     wb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + (size_t)g * H + j0 + u]) : 0.0f;
     rb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + GH + (size_t)g * H + j0 + u]) : 0.0f;
   }
-  for (int e = tid; e < 3 * SJ; e += blockDim.x) {
+  for (int e = tid; e < 3 * SJT; e += blockDim.x) {
     const int u = e / 3, g = e % 3;
     pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? __half2float(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
   }
@@ -282,6 +319,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     mbar_init(smem_u32(&bars[2 * SMAXST + 1]), 8);  // gate warps' h copies written
     mbar_init(smem_u32(&bars[2 * SMAXST + 2]), 8);  // gate warps read the accumulators
     mbar_init(smem_u32(&bars[2 * SMAXST + 3]), 1);  // final MMA drain
+    // cluster teams: every CTA's publication of h_s, s even / odd
+    mbar_init(smem_u32(&bars[2 * SMAXST + 4]), (unsigned)C);
+    mbar_init(smem_u32(&bars[2 * SMAXST + 5]), (unsigned)C);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -298,8 +338,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const bool gate_warp = warp < 8;
   const int q = warp & 3;
   const bool odd_lane = PAIR && lane >= 16;
-  const int br = PAIR ? 16 * q + (lane & 15) : 32 * q + lane;  // batch row within the team
-  const int uh0 = (warp >> 2) * 8 + (odd_lane ? 4 : 0);        // first of this thread's units
+  // batch row within the team; with paired blocks row b sits in TMEM lane
+  // quarter b % 4, so a small batch spreads over all four sub-partitions
+  const int br = PAIR ? 4 * (lane & 15) + q : 32 * q + lane;
+  const int uh0 = (warp >> 2) * (SJT / 2) + (odd_lane ? UH : 0);  // first of this thread's units
   const bool grow = gate_warp && br < nbt;
   const int bg = b0 + br;  // global batch row
   float hreg[UH], creg[UH];
@@ -307,7 +349,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // address of (this thread's batch row, unit j) in buffer buf of the Half h copy
   auto h16_at = [&](int buf, int j) {
     const int kb = j / SK;
-    const int row = PAIR ? 32 * (br >> 4) + 16 * (kb & 1) + (br & 15) : br;
+    const int row = PAIR ? 32 * (br & 3) + 16 * (kb & 1) + (br >> 2) : br;
     return reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_region(p, buf, d, tin, kb / BPR, NREG)) +
                                      sw128_offset(row, j % SK));
   };
@@ -331,7 +373,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     // no CTA: zero them once in both buffers (R is zero there too, but a stale
     // Inf or NaN times zero would not be)
     if (rank == C - 1 && uh0 == 0) {
-      for (int k = C * SJ; k < KB * SK; ++k)
+      for (int k = C * SJT; k < KB * SK; ++k)
         for (int buf = 0; buf < 2; ++buf) *h16_at(buf, k) = __float2half_rn(0.0f);
     }
   } else {
@@ -341,6 +383,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // cluster teams: every CTA's barriers are initialised before any remote
+  // arrival (all CTAs of a cluster run at once and reach this point)
+  if constexpr (CLU) asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   const uint32_t tmem_acc = *tmem_slot;
 
   // Publication flags: flags[rank] = how many h copies this CTA has published
@@ -358,11 +403,30 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const uint32_t bar_drain = su32(&bars[2 * SMAXST + 3]);
   // gate warps: make this CTA's new h copies visible to the async proxy of
   // other CTAs, then thread 0 releases the flag once all 8 warps are in
+  // Cluster teams instead arrive (release, cluster scope) on every CTA's
+  // publication barrier for h_s, one barrier per step parity: a CTA's
+  // arrivals for h_{s+2} come after it saw every arrival for h_{s+1}, each of
+  // which its sender made after its own arrivals for h_s, so no barrier can
+  // count an arrival of a later step in an earlier phase.
+  const uint32_t bar_pubc = su32(&bars[2 * SMAXST + 4]);
   auto publish = [&](unsigned value, uint32_t pub_parity) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_pub) : "memory");
-    if (tid == 0) {
+    if constexpr (CLU) {
+      // lane q of warp 0 waits for the 8 gate warps itself, then arrives on
+      // CTA q's barrier: the C releases go out in parallel
+      if (warp == 0 && lane < C) {
+        if (bar_wait(bar_pub, pub_parity, p.timeout_ns)) {
+          const uint32_t local = bar_pubc + 8u * ((value - 1u) & 1u);  // h_s, s = value - 1
+          asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(local, (uint32_t)lane))
+                       : "memory");
+        } else {
+          abort_flag = 1;
+          atomicOr(p.status, 1);
+        }
+      }
+    } else if (tid == 0) {
       if (bar_wait(bar_pub, pub_parity, p.timeout_ns)) {
         asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + rank), "r"(value) : "memory");
       } else {
@@ -407,7 +471,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
   const float clip = PLAIN ? 0.0f : p.clip;
   const bool input_forget = !PLAIN && p.input_forget;
-  constexpr int RPB = SK * BPR / SJ;  // CTAs owning one region: 4 or 8 (a multiple of 4)
+  constexpr int RPB = SK * BPR / SJT;  // CTAs owning one region: 4 or 8 (a multiple of 4)
 
   // Regions are taken in a fixed order per CTA, starting after the region
   // this CTA helps write, so that one late region does not hold up the
@@ -428,9 +492,18 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       const unsigned long long t0 = global_ns();
       unsigned taken = 0;  // regions copied this step (bit r)
       int pos = 0;         // regions issued so far, in this CTA's order
+      if constexpr (CLU) {
+        // every CTA of the cluster has published h_s: all regions are ready
+        bool okc = true;
+        if (lane == 0) okc = bar_wait_cluster(bar_pubc + 8u * (uint32_t)(s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, okc ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+      }
       while (pos < NREG && ok) {
         bool rd = true;
-        if (lane < NREG && !((taken >> lane) & 1u)) {
+        if (!CLU && lane < NREG && !((taken >> lane) & 1u)) {
 #pragma unroll
           for (int o = 0; o < RPB; o += 4) {
             const uint4 v = ld_acquire_gpu_v4(flags + lane * RPB + o);
@@ -507,6 +580,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
           break;
         }
         tc_fence_after();
+        bool odd_started = false;
         for (int pos = 0; pos < NREG; ++pos) {
           int r = pos + rot;
           r = r >= NREG ? r - NREG : r;
@@ -517,18 +591,21 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
           tc_fence_after();
           const uint64_t ad = adesc0 + (uint64_t)st * kStageD;
           uint64_t bd = bdesc0 + (uint64_t)(r * BPR) * kBlockD;
-          const uint32_t first = pos != 0 ? 1u : 0u;
-          tc_mma(tmem_acc, ad, bd, idesc, first);
+          // the first MMA of each accumulator in a step overwrites it; with
+          // an odd number of k blocks the last region has no odd block, and
+          // it may come first in this CTA's order
+          tc_mma(tmem_acc, ad, bd, idesc, pos != 0 ? 1u : 0u);
           tc_mma(tmem_acc, ad + kK16, bd + kK16, idesc, 1u);
           tc_mma(tmem_acc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
           tc_mma(tmem_acc, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
           bd += kBlockD;
           if (PAIR && 2 * r + 1 < KB) {
-            tc_mma(tmem_acc + kOddCol, ad, bd, idesc, first);
+            tc_mma(tmem_acc + kOddCol, ad, bd, idesc, odd_started ? 1u : 0u);
             tc_mma(tmem_acc + kOddCol, ad + kK16, bd + kK16, idesc, 1u);
             tc_mma(tmem_acc + kOddCol, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
             tc_mma(tmem_acc + kOddCol, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
             bd += kBlockD;
+            odd_started = true;
           }
           tc_commit(su32(&bars[SMAXST + st]));
           if (++st == NST) {
@@ -551,8 +628,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     float xv[UH * G];
     load_xw(0, xv);
     bool ok = true;
-    // columns of units (w / 4) * 8 .. + 7 of this warp's 32 lanes
-    const uint32_t ta = tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)((warp >> 2) * 8 * G);
+    // columns of this warp-half's units (w / 4) * SJT / 2 ... of its 32 lanes;
+    // without PAIR the thread's own units
+    const uint32_t ta = tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)((PAIR ? (warp >> 2) * (SJT / 2) : uh0) * G);
     for (int s = 0; s < Tn; ++s) {
       if (abort_flag || !bar_wait(bar_done, (uint32_t)(s & 1), p.timeout_ns)) {
         ok = false;
@@ -562,21 +640,25 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       float acc[NCOL];
       if constexpr (PAIR) {
         // lane l < 16 holds the even-block sums of batch row br, lane l + 16
-        // the odd-block sums of the same row; each keeps 4 of the 8 units
-        // and sends the other 4 to its partner (lane ^ 16)
-        uint32_t ev[8 * G], od[8 * G];
-        tmem_ld<8 * G>(ta, ev);
-        tmem_ld<8 * G>(ta + kOddCol, od);
-        if (KB < 2) {
+        // the odd-block sums of the same row; of the warp-half's 2 UH units
+        // the even lane takes the first UH and the odd lane the rest, each
+        // sending the partner the other half, 4 units at a time
 #pragma unroll
-          for (int i = 0; i < 8 * G; ++i) od[i] = 0u;  // no odd block
-        }
+        for (int r = 0; r < UH / 4; ++r) {
+          uint32_t ea[4 * G], eb[4 * G], oa[4 * G], ob[4 * G];
+          tmem_ld<4 * G>(ta + (uint32_t)(4 * r * G), ea);
+          tmem_ld<4 * G>(ta + (uint32_t)((UH + 4 * r) * G), eb);
+          tmem_ld<4 * G>(ta + kOddCol + (uint32_t)(4 * r * G), oa);
+          tmem_ld<4 * G>(ta + kOddCol + (uint32_t)((UH + 4 * r) * G), ob);
 #pragma unroll
-        for (int i = 0; i < NCOL; ++i) {
-          const float mine = __uint_as_float(odd_lane ? od[NCOL + i] : ev[i]);
-          const float give = __uint_as_float(odd_lane ? od[i] : ev[NCOL + i]);
-          const float got = __shfl_xor_sync(0xffffffffu, give, 16);
-          acc[i] = odd_lane ? got + mine : mine + got;  // even + odd
+          for (int i = 0; i < 4 * G; ++i) {
+            const float o_a = KB < 2 ? 0.0f : __uint_as_float(oa[i]);  // no odd block
+            const float o_b = KB < 2 ? 0.0f : __uint_as_float(ob[i]);
+            const float mine = odd_lane ? o_b : __uint_as_float(ea[i]);
+            const float give = odd_lane ? o_a : __uint_as_float(eb[i]);
+            const float got = __shfl_xor_sync(0xffffffffu, give, 16);
+            acc[4 * r * G + i] = odd_lane ? got + mine : mine + got;  // even + odd
+          }
         }
       } else {
         uint32_t a[NCOL];
@@ -676,14 +758,45 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   if (warp == 9) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_acc), "r"(kTmemCols) : "memory");
   }
+  // cluster teams: no CTA leaves while a peer may still arrive on its barriers
+  if constexpr (CLU) asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int CELL, bool GEN, bool PLAIN, bool PAIR>
+template <int CELL, bool GEN, bool PLAIN, int MODE>
 cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
-  auto kern = step_tc_kernel<CELL, GEN, PLAIN, PAIR>;
+  auto kern = step_tc_kernel<CELL, GEN, PLAIN, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+  cfg.blockDim = dim3(STHREADS, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (MODE == 2) {
+    // a team is one cluster; teams never wait on each other
+    if (plan.team_ctas > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.team_ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    // teams of CTAs that wait on each other's flags: all resident at once
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (resident != nullptr) {
+    if (MODE == 2) {
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      *resident = (e == cudaSuccess) ? n : 0;
+      return e;
+    }
     int per_sm = 0, dev = 0, sms = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, STHREADS, plan.smem);
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
@@ -691,40 +804,31 @@ cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream
     *resident = (e == cudaSuccess) ? (per_sm * sms) / plan.team_ctas : 0;
     return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
-  cfg.blockDim = dim3(STHREADS, 1, 1);
-  cfg.dynamicSmemBytes = plan.smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p, h16);
 }
 
-template <bool PAIR>
-cudaError_t step_tc_pair_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16) {
+template <int MODE>
+cudaError_t step_tc_mode_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16) {
   const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
   const bool gen = p.generic_acts != 0;
   switch (p.cell) {
     case 0:
-      if (gen) return plain ? step_tc_launch<0, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<0, true, false, PAIR>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<0, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<0, false, false, PAIR>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<0, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<0, true, false, MODE>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<0, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<0, false, false, MODE>(p, plan, s, q, h16);
     case 1:
-      if (gen) return plain ? step_tc_launch<1, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<1, true, false, PAIR>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<1, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<1, false, false, PAIR>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<1, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<1, true, false, MODE>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<1, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<1, false, false, MODE>(p, plan, s, q, h16);
     default:
-      if (gen) return plain ? step_tc_launch<2, true, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<2, true, false, PAIR>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<2, false, true, PAIR>(p, plan, s, q, h16) : step_tc_launch<2, false, false, PAIR>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<2, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<2, true, false, MODE>(p, plan, s, q, h16);
+      return plain ? step_tc_launch<2, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<2, false, false, MODE>(p, plan, s, q, h16);
   }
 }
 
 }  // namespace
 
-// One translation unit per tile arrangement (they compile in parallel).
+// One translation unit per MODE (they compile in parallel).
 cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
 cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
+cudaError_t step_tc_cluster(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
 
 }  // namespace rk

@@ -6,7 +6,7 @@
 namespace rk {
 
 cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
-  return step_tc_pair_dispatch<true>(p, plan, s, resident, h16);
+  return step_tc_mode_dispatch<1>(p, plan, s, resident, h16);
 }
 
 }  // namespace rk

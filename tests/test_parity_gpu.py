@@ -440,6 +440,9 @@ TC_STEP_CASES = [
     ("gru", 64, 9, "forward", 0, "full"),
     ("rnn", 48, 17, "bidirectional", 1, "plain"),
     ("lstm", 256, 64, "bidirectional", 0, "plain"),
+    # more than 16 CTAs of 32 units: teams published by global flags
+    ("lstm", 576, 16, "bidirectional", 1, "plain"),
+    ("gru", 544, 33, "reverse", 0, "full"),
 ]
 
 
