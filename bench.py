@@ -171,7 +171,7 @@ KERNEL_SOURCES = {
     "cluster": ("step_cluster_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
     "grid": ("step_grid_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
     "tensor": ("step_tc_kernel", ("rk_step.cuh", "rk_step_tc.cuh", "rk_step_tc.cu", "rk_step_tc_pair.cu",
-                                  "rk_step_tc_cluster.cu")),
+                                  "rk_step_tc_cluster.cu", "rk_step_tcs.cu")),
     "proj_tc": ("proj_tc_kernel", ("rk_proj_tc.cu",)),
     "proj_simt": ("projection", ("rk_proj.cu",)),
 }

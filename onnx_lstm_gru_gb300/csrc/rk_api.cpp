@@ -286,10 +286,35 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   // (R . h on tcgen05), every CTA of the launch resident at once
   if (p->dtype == RK_F16 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
       !(p->cell == RK_GRU && !p->linear_before_reset) && H % 8 == 0 && N >= 4) {
+    // at most 16 rows per direction: the gate rows are the MMA's M and the
+    // batch its N, one cluster of ceil(H / 32) CTAs per direction
+    const int Cc = (H + 31) / 32;
+    if (N <= 16 && Cc <= 16) {
+      StepPlan pl{};
+      pl.kind = rk::kStepTensor;
+      pl.team_ctas = Cc;
+      pl.nb = N;
+      pl.nbc = 16;
+      pl.teams_per_dir = 1;
+      pl.J = 32;
+      pl.threads = 320;
+      pl.grid = D * Cc;
+      pl.stages = 1;
+      pl.smem = rk::step_tcs_smem(G, H);
+      if ((int)pl.smem <= smem_cap && (!check || resident(pl) >= 1)) {
+        sp->team_ctas = pl.team_ctas;
+        sp->J = pl.J;
+        sp->nb = pl.nb;
+        sp->teams_per_dir = pl.teams_per_dir;
+        sp->nbc = pl.nbc;
+        sp->stages = pl.stages;
+        *out = pl;
+        return RK_OK;
+      }
+    }
     // a team of at most 64 rows whose units fit one cluster at 32 per CTA
     // publishes h inside the cluster (remote mbarrier arrivals), far faster
     // than global flags; teams never wait on each other
-    const int Cc = (H + 31) / 32;
     if (N <= 64 && Cc <= 16 && (H + 63) / 64 <= 32) {
       StepPlan pl{};
       pl.kind = rk::kStepTensor;

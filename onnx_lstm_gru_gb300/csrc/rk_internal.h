@@ -119,6 +119,11 @@ cudaError_t noalloc_scratch(float** scratch, int** status);
 // cluster team).  h16 is the Half copy of the exchanged hidden state,
 // 2 x D x teams x 16 KB regions per 128 k.
 size_t step_tc_smem(int G, int H, int stages, int units);
+// Small-batch variant (at most 16 rows per direction, one cluster of
+// ceil(H / 32) CTAs per direction; plans it with nbc = 16): dynamic shared
+// memory and the launch, same contract as step_tc_entry.
+size_t step_tcs_smem(int G, int H);
+cudaError_t step_tcs_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 int step_tc_stages(int G, int H, int units, size_t smem_cap);
 cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 // Self-test of the bounded waits (see rk_selftest_timeout).

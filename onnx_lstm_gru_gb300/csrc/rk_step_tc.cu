@@ -21,6 +21,7 @@ cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_
   // 32 units per CTA: a cluster team; else the plan pads a team's rows to
   // 64 (two k blocks per tile) or 128
   __half* hp = static_cast<__half*>(h16);
+  if (plan.nbc == 16) return step_tcs_entry(p, plan, s, resident, h16);
   if (plan.J == SJC) return step_tc_cluster(p, plan, s, resident, hp);
   return plan.nbc == 64 ? step_tc_pairs(p, plan, s, resident, hp) : step_tc_rows(p, plan, s, resident, hp);
 }
