@@ -285,7 +285,7 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   // tensor-core kernel: Half layers with a batch worth a dense product
   // (R . h on tcgen05), every CTA of the launch resident at once
   if (p->dtype == RK_F16 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
-      !(p->cell == RK_GRU && !p->linear_before_reset) && H % 8 == 0 && N >= 4) {
+      H % 8 == 0 && N >= 4) {
     // at most 16 rows per direction: the gate rows are the MMA's M and the
     // batch its N, one cluster of ceil(H / 32) CTAs per direction
     const int Cc = (H + 31) / 32;
@@ -312,10 +312,13 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
         return RK_OK;
       }
     }
+    // (GRU with linear_before_reset = 0 needs r (.) h exchanged within the
+    // step: only the small-batch kernel does that on the tensor cores)
+    const bool lbr0_cell = p->cell == RK_GRU && !p->linear_before_reset;
     // a team of at most 64 rows whose units fit one cluster at 32 per CTA
     // publishes h inside the cluster (remote mbarrier arrivals), far faster
     // than global flags; teams never wait on each other
-    if (N <= 64 && Cc <= 16 && (H + 63) / 64 <= 32) {
+    if (!lbr0_cell && N <= 64 && Cc <= 16 && (H + 63) / 64 <= 32) {
       StepPlan pl{};
       pl.kind = rk::kStepTensor;
       pl.team_ctas = Cc;
@@ -354,7 +357,7 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     // one publication flag per CTA in the state header, each team's starting
     // on a 32-byte boundary; one polling lane per 128 k
     const int teams = D * pl.teams_per_dir;
-    const bool fits = pl.stages >= 2 && pl.grid <= h->sms &&
+    const bool fits = !lbr0_cell && pl.stages >= 2 && pl.grid <= h->sms &&
                       teams * ((pl.team_ctas + 7) / 8 * 8) <= rk::kStateHeader && (H + 63) / 64 <= 32;
     if (fits && (!check || resident(pl) * pl.team_ctas >= pl.grid)) {
       sp->team_ctas = pl.team_ctas;

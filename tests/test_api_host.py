@@ -170,7 +170,15 @@ def test_plans_without_device(handle):
     plans = {name: rk.rk_describe_plan(handle, w.problem.to_c()) for name, w in workloads.WORKLOADS.items()}
     assert "step=fast" in plans["lstm_fwd_s8_b1_i16_h16_f32"]
     assert "step=fast" in plans["bilstm_s80_b1_i256_h256_f32"] and "ctas=16" in plans["bilstm_s80_b1_i256_h256_f32"]
-    assert "step=cluster" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]  # 16 clusters of 16 would not fit at once
+    # small batches of Half layers, GRU linear_before_reset = 0 included, run the
+    # small-batch tensor-core kernel (16 rows of h per direction: nb=8, 16 CTAs of 32 units)
+    assert "step=tensor" in plans["bigru_s128_b8_i512_h512_f16_lbr0"] and "J=32" in plans["bigru_s128_b8_i512_h512_f16_lbr0"]
+    h4 = rk.rk_create(rk.RK_FORCE_SIMT_STEP)
+    try:
+        lbr0 = workloads.WORKLOADS["bigru_s128_b8_i512_h512_f16_lbr0"].problem.to_c()
+        assert "step=cluster" in rk.rk_describe_plan(h4, lbr0)  # 16 clusters of 16 would not fit at once
+    finally:
+        rk.rk_destroy(h4)
     assert "step=grid" in plans["revlstm_peep_clip_s200_b4_i128_h1024_f32"]
     assert "proj=tc step=tensor" in plans["bilstm_s512_b64_i1024_h1024_f16"]
     assert "step=tensor" in plans["bigru_s128_b8_i512_h512_f16_lbr1"]

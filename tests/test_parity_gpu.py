@@ -355,6 +355,35 @@ def test_tensor_core_step_with_odd_offsets(cell):
             assert torch.equal(got[k], aligned[k]), k
 
 
+@pytest.mark.parametrize("H,N,direction,layout,opts", [(40, 4, "bidirectional", 0, "plain"),
+                                                     (96, 9, "reverse", 1, "full"),
+                                                     (200, 16, "forward", 0, "full"),
+                                                     (512, 8, "bidirectional", 1, "plain")])
+def test_tensor_core_gru_lbr0(H, N, direction, layout, opts):
+    """GRU with linear_before_reset = 0 on the small-batch tensor-core kernel:
+    two products per step, r (.) h_prev rounded to Half and exchanged inside
+    the cluster before the candidate's product.  Matches the oracle within
+    the Half tolerance and the SIMT cluster kernel."""
+    kw = dict(clip=1.5) if opts == "full" else {}
+    if opts == "full":
+        D = 2 if direction == "bidirectional" else 1
+        kw["activations"] = [("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0)] * D
+    pr = rk.Problem("gru", seq=9, batch=N, input=24, hidden=H, direction=direction, dtype="f16", layout=layout,
+                    linear_before_reset=0, **kw)
+    plan = layer().plan(pr)
+    assert "step=tensor" in plan and "J=32" in plan
+    lens = list(np.random.default_rng(H).integers(0, 10, N))
+    inp = rand_inputs(pr, seed=H + 7 * N, lens=lens, scale=0.2)
+    got = run_gpu(pr, inp)
+    compare(pr, got, run_oracle(pr, inp), lens)
+    simt = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_STEP)
+    compare(pr, got, {k: v for k, v in simt.items() if not k.endswith("_raw")}, lens)
+    again = run_gpu(pr, inp)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
+
+
 @pytest.mark.parametrize("H,N", [(40, 5), (96, 130)])
 def test_tensor_core_step_ignores_stale_scratch(H, N):
     """The tensor-core step kernel reads its Half h copies in whole 64-wide k
