@@ -141,6 +141,49 @@ __device__ __forceinline__ float rowsums(const RFrag<T> (&R)[RW][KV], const floa
   return acc[0];
 }
 
+// Grouped layout (LSTM and RNN): the warp's 32 lanes form 4 groups of 8;
+// group g holds rows g * NRG ... g * NRG + NRG - 1 (NRG = RW / 4, a power of
+// two) and lane i of a group holds, for each of them, the 4 KV chunks of 4
+// consecutive k at k = (c * 8 + i) * 4 + e.  A row's 8 lanes chain their
+// terms in increasing k, then fold() combines them over 3 levels (lanes
+// xor 4, 2, 1) instead of 5; rows are kept in the order
+// rho -> rho ^ group_perm<NRG>(i), so that afterwards lane 8 g + i holds the
+// full sum of row g * NRG + group_perm<NRG>(i).
+template <int NRG>
+__device__ __forceinline__ int group_perm(int lane) { return ((lane & 7) >> (3 - log2c<NRG>())) & (NRG - 1); }
+template <int NRG>
+__device__ __forceinline__ int group_row_lane(int r) { return 8 * (r / NRG) + ((r % NRG) << (3 - log2c<NRG>())); }
+
+template <int NRG, typename T, int NCH>
+__device__ __forceinline__ float rowsums_grouped(const RFrag<T> (&R)[NRG][NCH], const float* __restrict__ h, int lane) {
+  const int i = lane & 7;
+  float4 hv[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) hv[c] = *reinterpret_cast<const float4*>(h + (c * 8 + i) * 4);
+  float acc[NRG];
+#pragma unroll
+  for (int r = 0; r < NRG; ++r) {
+    float a = 0.0f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const float4 rv = R[r][c].get();
+      a = fmaf(rv.x, hv[c].x, a);
+      a = fmaf(rv.y, hv[c].y, a);
+      a = fmaf(rv.z, hv[c].z, a);
+      a = fmaf(rv.w, hv[c].w, a);
+    }
+    acc[r] = a;
+  }
+  fold<NRG, 4>(acc);
+  return acc[0];
+}
+
+template <int CELL, int RW>
+struct FastGrouped {
+  // LSTM and RNN whose rows per group (RW / 4) are a power of two
+  static constexpr bool value = CELL != 1 && RW % 4 == 0 && ((RW / 4) & (RW / 4 - 1)) == 0;
+};
+
 // PLAIN: no clip, no peepholes, no input_forget (the options compile out).
 template <int CELL, typename T, bool GEN, int KV, int U, bool PLAIN>
 __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const StepParams p) {
@@ -193,20 +236,43 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
     }
     return i ^ perm_mask<RW>(lane);
   };
-  RFrag<T> Rr[RW][KV];
+  constexpr bool GROUPED = FastGrouped<CELL, RW>::value;
+  constexpr int NRG = GROUPED ? RW / 4 : 1;   // rows per 8-lane group
+  constexpr int NCH = 4 * KV;                 // 4-k chunks per lane and row (grouped)
+  RFrag<T> Rr[GROUPED ? 1 : RW][KV];
+  RFrag<T> Rg[NRG][GROUPED ? NCH : 1];
+  if constexpr (GROUPED) {
+    const int grp = lane >> 3, gi = lane & 7;
 #pragma unroll
-  for (int i = 0; i < RW; ++i) {
-    const int r = row_of(i);
-    const int g = r / U, u = r % U;
-    const bool ok = g < G && u < Uc;
-    const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
+    for (int rho = 0; rho < NRG; ++rho) {
+      const int r = grp * NRG + (rho ^ group_perm<NRG>(lane));
+      const int g = r / U, u = r % U;
+      const bool ok = g < G && u < Uc;
+      const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
 #pragma unroll
-    for (int kc = 0; kc < KV; ++kc) {
-      const int k = (kc * 32 + lane) * 4;
-      float e[4];
+      for (int c = 0; c < NCH; ++c) {
+        const int k = (c * 8 + gi) * 4;
+        float e[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
-      Rr[i][kc].set(e);
+        for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
+        Rg[rho][c].set(e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      const int r = row_of(i);
+      const int g = r / U, u = r % U;
+      const bool ok = g < G && u < Uc;
+      const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
+#pragma unroll
+      for (int kc = 0; kc < KV; ++kc) {
+        const int k = (kc * 32 + lane) * 4;
+        float e[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
+        Rr[i][kc].set(e);
+      }
     }
   }
   for (int e = tid; e < 2 * KP; e += blockDim.x) {
@@ -373,11 +439,13 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
         if (active) hn = (1.0f - z) * hc + z * hreg;
       }
     } else {
-      const float v = rowsums<0, RW, T, KV>(Rr, hs + (size_t)cur * KP, lane);
+      float v;
+      if constexpr (GROUPED) v = rowsums_grouped<NRG, T, NCH>(Rg, hs + (size_t)cur * KP, lane);
+      else v = rowsums<0, RW, T, KV>(Rr, hs + (size_t)cur * KP, lane);
       float pre[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float sum = __shfl_sync(0xffffffffu, v, row_lane<RW>(g * U + ul));
+        const float sum = __shfl_sync(0xffffffffu, v, GROUPED ? group_row_lane<NRG>(g * U + ul) : row_lane<RW>(g * U + ul));
         pre[g] = ((xv[g] + sum) + wbv[g]) + rbv[g];
       }
       if constexpr (CELL == 0) {
