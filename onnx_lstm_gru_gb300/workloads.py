@@ -8,9 +8,10 @@ then cast to the tensor dtype (float16 by round-to-nearest-even).  "N(0, s)"
 means standard deviation s.  The same arrays feed the CUDA library and the
 oracle.
 
-The five named workloads are the layer shapes the recurrent-layers page
-measures and tests (its bidirectional LSTM 80 x 1 x 256 float32 and the
-recognizer-style shapes), plus larger Half layers for the tensor-core path.
+The named workloads are the layer shapes the recurrent-layers page measures
+and tests (its bidirectional LSTM 80 x 1 x 256 float32 and the recognizer's
+second shape, 48 x 8 x 192 x 96), plus larger layers for the grid and
+tensor-core paths.
 """
 from __future__ import annotations
 
@@ -77,6 +78,18 @@ WORKLOADS = {
         Problem("lstm", seq=512, batch=64, input=1024, hidden=1024, direction="bidirectional", dtype="f16",
                 layout=0),
         seed=4, x=("normal", 1.0), weights=("uniform", 0.03), lens="full"),
+    # the recognizer's second shape (bidirectional LSTM over 48 columns of 8
+    # text lines of varying width, 192 features, 96 units), float32 and Half
+    "bilstm_s48_b8_i192_h96_f32": Workload(
+        "bilstm_s48_b8_i192_h96_f32",
+        Problem("lstm", seq=48, batch=8, input=192, hidden=96, direction="bidirectional", dtype="f32", layout=0),
+        seed=5, x=("normal", 1.0), weights=("uniform", 0.1), init_h=("normal", 0.1), init_c=("normal", 0.1),
+        lens="uniform"),
+    "bilstm_s48_b8_i192_h96_f16": Workload(
+        "bilstm_s48_b8_i192_h96_f16",
+        Problem("lstm", seq=48, batch=8, input=192, hidden=96, direction="bidirectional", dtype="f16", layout=0),
+        seed=6, x=("normal", 1.0), weights=("uniform", 0.1), init_h=("normal", 0.1), init_c=("normal", 0.1),
+        lens="uniform"),
 }
 
 # the headline workload: the pages' bidirectional LSTM layer
