@@ -87,6 +87,8 @@ enum rk_activation_kind {
 #define RK_FORCE_GRID_STEP 2u       /* use the grid-wide step kernel even where a cluster fits */
 #define RK_FORCE_GENERAL_STEP 4u    /* never the one-row-per-cluster register-resident step kernel */
 #define RK_FORCE_SIMT_STEP 8u       /* Half problems: never the tensor-core step kernel */
+#define RK_SEPARATE_PROJECTION 16u  /* never compute the projection on the SMs the tensor-core
+                                       recurrence leaves idle (always a launch of its own) */
 
 /* One activation slot (GpuRecurrentActivation): kind plus resolved alpha/beta. */
 typedef struct rk_activation {

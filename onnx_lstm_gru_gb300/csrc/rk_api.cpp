@@ -233,6 +233,37 @@ void fill_params_problem(const rk_problem* p, StepParams* sp) {
   sp->KP = (int)kp_of(p);
 }
 
+// Whether the tensor-core recurrence computes the projection itself on the
+// SMs it leaves idle: flag-published teams (the projection's tiles are
+// produced in the order the steps consume them, which needs layout 0), the
+// tcgen05 projection usable, at least 8 idle SMs, and room in the state
+// header for the readiness counters after the teams' flags.  With maps !=
+// nullptr the tensor maps are encoded too (needs the operands).
+struct FusedProj {
+  bool on = false;
+  int np = 0, groups = 0, mpg = 0, counter0 = 0;
+};
+FusedProj fused_projection(const rk_handle* h, const rk_problem* p, const StepPlan& pl, const rk::ProjParams& pp,
+                           bool has_projection, CUtensorMap* tmA, CUtensorMap* tmB) {
+  FusedProj f;
+  if (!has_projection || pl.kind != rk::kStepTensor || pl.J != 16 || p->layout != 0 || p->dtype != RK_F16 ||
+      (h->flags & (RK_FORCE_SIMT_PROJECTION | RK_SEPARATE_PROJECTION)) || p->input % 8 != 0)
+    return f;
+  const int D = dirs_of(p);
+  const int np = h->sms - pl.grid;
+  const int counter0 = D * pl.teams_per_dir * ((pl.team_ctas + 7) / 8 * 8);
+  const int groups = (rk::kStateHeader - counter0) / D;
+  const int mt = (pp.M + 127) / 128;
+  if (np < 8 || groups < 1 || mt < 1) return f;
+  if (tmA != nullptr && !(rk::projection_tc_supported(pp) && rk::projection_tc_maps(pp, tmA, tmB))) return f;
+  f.on = true;
+  f.np = np;
+  f.groups = std::min(groups, mt);
+  f.mpg = (mt + f.groups - 1) / f.groups;
+  f.counter0 = counter0;
+  return f;
+}
+
 // Launch (or, with resident != nullptr, size) the step kernel of a plan.
 cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl, cudaStream_t stream, int* resident) {
   if (pl.kind == rk::kStepTensor) return rk::step_tc_entry(sp, pl, stream, resident, sp.rhglob);
@@ -558,8 +589,11 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
   const bool tc = p->dtype == RK_F16 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
+  rk::ProjParams pp{};
+  pp.M = (int)(p->seq * p->batch);
+  const bool fused = fused_projection(h, p, pl, pp, p->seq > 0 && p->input > 0, nullptr, nullptr).on;
   snprintf(buf, (size_t)len, "proj=%s step=%s shape=%d ctas=%d J=%d nb=%d teams=%d threads=%d smem=%zu grid=%d",
-           tc ? "tc" : "simt",
+           fused ? "fused" : (tc ? "tc" : "simt"),
            pl.kind == rk::kStepTensor ? "tensor"
                                       : (pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid")),
            (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
@@ -610,17 +644,20 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     state = h->state;
   }
 
-  // 1. input projection of every step and direction
-  if (sp.T > 0 && need_xw > 0) {
-    rk::ProjParams pp{};
-    pp.M = (int)(p->seq * p->batch);
-    pp.N = sp.G * sp.H;
-    pp.K = (int)p->input;
-    pp.D = sp.D;
-    pp.X = tptr(ops->X, eb);
-    pp.W = tptr(ops->W, eb);
-    pp.Xw = xw;
-    pp.dtype = p->dtype;
+  // 1. input projection of every step and direction: a launch of its own, or
+  // computed by the blocks the tensor-core recurrence leaves idle
+  rk::ProjParams pp{};
+  pp.M = (int)(p->seq * p->batch);
+  pp.N = sp.G * sp.H;
+  pp.K = (int)p->input;
+  pp.D = sp.D;
+  pp.X = tptr(ops->X, eb);
+  pp.W = tptr(ops->W, eb);
+  pp.Xw = xw;
+  pp.dtype = p->dtype;
+  CUtensorMap tmA{}, tmB{};
+  const FusedProj fz = fused_projection(h, p, pl, pp, sp.T > 0 && need_xw > 0, &tmA, &tmB);
+  if (sp.T > 0 && need_xw > 0 && !fz.on) {
     if (h->profiling) cudaEventRecord(h->ev[0], stream);
     const bool tc = !(h->flags & RK_FORCE_SIMT_PROJECTION) && rk::projection_tc_supported(pp);
     cudaError_t e = tc ? rk::launch_projection_tc(pp, h->status, h->timeout_ns, stream)
@@ -654,7 +691,23 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
   }
   if (h->profiling) cudaEventRecord(h->ev[2], stream);
-  cudaError_t e = step_dispatch(p->cell, sp, pl, stream, nullptr);
+  cudaError_t e;
+  if (fz.on) {
+    StepPlan fp = pl;
+    fp.grid = pl.grid + fz.np;
+    fp.smem = std::max(pl.smem, rk::projection_tc_smem());
+    sp.fused = 1;
+    sp.step_ctas = pl.grid;
+    sp.pj_M = pp.M;
+    sp.pj_K = pp.K;
+    sp.pj_vec = (reinterpret_cast<uintptr_t>(xw) % 16 == 0) && (pp.N % 4 == 0);
+    sp.xw_groups = fz.groups;
+    sp.xw_mpg = fz.mpg;
+    sp.xw_ready = sp.counters + fz.counter0;
+    e = rk::step_tc_entry(sp, fp, stream, nullptr, sp.rhglob, &tmA, &tmB);
+  } else {
+    e = step_dispatch(p->cell, sp, pl, stream, nullptr);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (e == cudaErrorCooperativeLaunchTooLarge)

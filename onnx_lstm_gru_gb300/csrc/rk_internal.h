@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace rk {
@@ -61,6 +62,15 @@ struct StepParams {
   int rows_pad;        // rows of R held per CTA (warps x rows per warp)
   int nbc;             // batch rows per h chunk in shared memory
   int stages;          // kStepTensor: 16 KB stages of the h ring
+  // projection computed by the launch's last blocks (tensor-core step kernel
+  // with flag-published teams, layout 0)
+  int fused;           // 1: blocks >= step_ctas run the projection
+  int step_ctas;       // blocks of the recurrence
+  int pj_M, pj_K;      // X rows (S * N) and input size
+  int pj_vec;          // float4 stores of Xw
+  int xw_groups;       // readiness counters per direction
+  int xw_mpg;          // 128-row tiles of Xw per counter
+  unsigned* xw_ready;  // [D][xw_groups]; 4 per (tile, 256 columns) stored
   // grid exchange (kStepGrid) and status
   float* hglob;        // [2][D*N][KP]
   float* rhglob;       // [D*N][KP]
@@ -94,6 +104,10 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s);
 // operands do not meet its alignment rules (then the SIMT kernel runs).
 bool projection_tc_supported(const ProjParams& p);
 cudaError_t launch_projection_tc(const ProjParams& p, int* status, long long timeout_ns, cudaStream_t s);
+// Tensor maps of X and W for the tcgen05 projection (false if they cannot be
+// encoded), and its dynamic shared memory per CTA.
+bool projection_tc_maps(const ProjParams& p, CUtensorMap* a, CUtensorMap* b);
+size_t projection_tc_smem();
 // Step kernel for one cell and exchange kind.  With resident_teams != nullptr
 // nothing is launched: the kernel is opted into the plan's shared memory /
 // cluster size and the number of teams that can be resident at once is
@@ -125,7 +139,8 @@ size_t step_tc_smem(int G, int H, int stages, int units);
 size_t step_tcs_smem(int G, int H);
 cudaError_t step_tcs_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 int step_tc_stages(int G, int H, int units, size_t smem_cap);
-cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
+cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16,
+                          const CUtensorMap* tmA = nullptr, const CUtensorMap* tmB = nullptr);
 // Self-test of the bounded waits (see rk_selftest_timeout).
 cudaError_t launch_selftest_timeout(unsigned* counter, int* status, long long timeout_ns, cudaStream_t s);
 

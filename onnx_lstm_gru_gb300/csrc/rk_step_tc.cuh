@@ -53,6 +53,7 @@
 
 #include <cstdint>
 
+#include "rk_proj_tc.cuh"
 #include "rk_step.cuh"
 
 namespace rk {
@@ -217,7 +218,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // and the team one thread-block cluster, published by remote mbarrier
 // arrivals instead of flags.
 template <int CELL, bool GEN, bool PLAIN, int MODE>
-__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16) {
+__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16,
+                                                             const __grid_constant__ CUtensorMap tmA,
+                                                             const __grid_constant__ CUtensorMap tmB) {
   constexpr bool PAIR = MODE >= 1;
   constexpr bool CLU = MODE == 2;
   constexpr int SJT = CLU ? SJC : SJ;  // hidden units per CTA
@@ -232,6 +235,28 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   static_assert(NR <= (int)kOddCol && 2 * kOddCol <= 512, "accumulators fit the allocation");
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
+  // projection of the layer computed by the blocks past the recurrence's
+  // (flag-published teams, layout 0): tiles in the order the recurrence
+  // consumes them (128 rows = time steps, both directions interleaved), each
+  // epilogue warp counting its stored rows into the tile's readiness counter
+  const int pj_mt = (p.pj_M + ptc::TBM - 1) / ptc::TBM, pj_nt = (G * p.H + ptc::TBN - 1) / ptc::TBN;
+  if constexpr (MODE != 2) {
+    if (p.fused && (int)blockIdx.x >= p.step_ctas) {
+      auto tile_of = [&](int tile) {
+        const int mi = tile / (p.D * pj_nt), rem = tile % (p.D * pj_nt);
+        const int dd = rem / pj_nt, n = rem % pj_nt;
+        const bool rev = p.direction == 1 || (p.direction == 2 && dd == 1);
+        return make_int3(dd, (rev ? pj_mt - 1 - mi : mi) * ptc::TBM, n * ptc::TBN);
+      };
+      auto signal = [&](int dd, int m0) {
+        atomicAdd(p.xw_ready + (size_t)dd * p.xw_groups + (m0 / ptc::TBM) / p.xw_mpg, 1u);
+      };
+      ptc::proj_tc_body(&tmA, &tmB, p.pj_M, G * p.H, p.pj_K, p.D, const_cast<float*>(p.xw), p.pj_vec, p.status,
+                        p.timeout_ns, base, (int)blockIdx.x - p.step_ctas, (int)gridDim.x - p.step_ctas, tile_of,
+                        signal);
+      return;
+    }
+  }
   const int NST = p.stages;
   const TcSmem L = tc_smem_layout(G, p.H, NST, SJT);
   unsigned char* sR = base + (L.r - 1024);
@@ -250,7 +275,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // teams interleaved over the block index: consecutive blocks tend to share
   // a die, and a team spread evenly over both dies keeps a steadier pace
   // than one split unevenly
-  const int nteams = gridDim.x / C;
+  const int nteams = (p.fused ? p.step_ctas : (int)gridDim.x) / C;
   int team, rank;
   if constexpr (CLU) {
     // one team per cluster of C CTAs
@@ -445,14 +470,39 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // are aligned and all inside H
   const bool xw_vec = (j0 + uh0 + UH <= H) && (H % 4 == 0) && (reinterpret_cast<uintptr_t>(p.xw) % 16 == 0);
   auto load_xw = [&](int s, float (&x)[UH * G]) {
-    const bool on = grow && s < len && s < Tn;
-    const float* qx = xw_row + (size_t)(reverse ? len - 1 - s : s) * xw_tstride;
+    bool on = grow && s < len && s < Tn;
+    const int tt = reverse ? len - 1 - s : s;
+    const float* qx = xw_row + (size_t)tt * xw_tstride;
+    if (MODE != 2 && p.fused && on) {
+      // the blocks computing the projection must have stored this row's
+      // 128-row tile of Xw for every column (layout 0: row tt * N + bg)
+      const int mtile = (tt * N + bg) / ptc::TBM;
+      const int grp = mtile / p.xw_mpg;
+      const unsigned target = (unsigned)(min(p.xw_mpg, pj_mt - grp * p.xw_mpg) * pj_nt * 4);
+      const unsigned* cnt = p.xw_ready + (size_t)d * p.xw_groups + grp;
+      if (ld_acquire_gpu(cnt) < target) {
+        const unsigned long long t0 = global_ns();
+        for (unsigned it = 1; ld_acquire_gpu(cnt) < target; ++it) {
+          if (abort_flag || ((it & 15u) == 0 && (long long)(global_ns() - t0) > p.timeout_ns)) {
+            abort_flag = 1;
+            atomicOr(p.status, 1);
+            on = false;
+            break;
+          }
+        }
+      }
+    }
+    // Xw written during this launch is read with coherent loads
+    auto ld = [&](const float* a) { return (MODE != 2 && p.fused) ? __ldcg(a) : __ldg(a); };
+    auto ld4 = [&](const float* a) {
+      return (MODE != 2 && p.fused) ? __ldcg(reinterpret_cast<const float4*>(a)) : __ldg(reinterpret_cast<const float4*>(a));
+    };
     if (on && xw_vec) {
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int v = 0; v < UH / 4; ++v) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(qx + (size_t)g * H + j0 + uh0 + 4 * v));
+          const float4 a = ld4(qx + (size_t)g * H + j0 + uh0 + 4 * v);
           x[(4 * v + 0) * G + g] = a.x;
           x[(4 * v + 1) * G + g] = a.y;
           x[(4 * v + 2) * G + g] = a.z;
@@ -464,7 +514,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const int j = j0 + uh0 + u;
-          x[u * G + g] = (on && j < H) ? __ldg(qx + (size_t)g * H + j) : 0.0f;
+          x[u * G + g] = (on && j < H) ? ld(qx + (size_t)g * H + j) : 0.0f;
         }
     }
   };
@@ -763,7 +813,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
 }
 
 template <int CELL, bool GEN, bool PLAIN, int MODE>
-cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
+cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
+                           const CUtensorMap* ta, const CUtensorMap* tb) {
   auto kern = step_tc_kernel<CELL, GEN, PLAIN, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
@@ -804,31 +855,35 @@ cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream
     *resident = (e == cudaSuccess) ? (per_sm * sms) / plan.team_ctas : 0;
     return e;
   }
-  return cudaLaunchKernelEx(&cfg, kern, p, h16);
+  static const CUtensorMap kNoMap{};  // the projection role does not run
+  return cudaLaunchKernelEx(&cfg, kern, p, h16, ta != nullptr ? *ta : kNoMap, tb != nullptr ? *tb : kNoMap);
 }
 
 template <int MODE>
-cudaError_t step_tc_mode_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16) {
+cudaError_t step_tc_mode_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16,
+                                  const CUtensorMap* ta, const CUtensorMap* tb) {
   const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
   const bool gen = p.generic_acts != 0;
   switch (p.cell) {
     case 0:
-      if (gen) return plain ? step_tc_launch<0, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<0, true, false, MODE>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<0, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<0, false, false, MODE>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<0, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, true, false, MODE>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<0, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, false, false, MODE>(p, plan, s, q, h16, ta, tb);
     case 1:
-      if (gen) return plain ? step_tc_launch<1, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<1, true, false, MODE>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<1, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<1, false, false, MODE>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<1, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, true, false, MODE>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<1, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, false, false, MODE>(p, plan, s, q, h16, ta, tb);
     default:
-      if (gen) return plain ? step_tc_launch<2, true, true, MODE>(p, plan, s, q, h16) : step_tc_launch<2, true, false, MODE>(p, plan, s, q, h16);
-      return plain ? step_tc_launch<2, false, true, MODE>(p, plan, s, q, h16) : step_tc_launch<2, false, false, MODE>(p, plan, s, q, h16);
+      if (gen) return plain ? step_tc_launch<2, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, true, false, MODE>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<2, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, false, false, MODE>(p, plan, s, q, h16, ta, tb);
   }
 }
 
 }  // namespace
 
 // One translation unit per MODE (they compile in parallel).
-cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
-cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
+cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
+                         const CUtensorMap* ta, const CUtensorMap* tb);
+cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
+                          const CUtensorMap* ta, const CUtensorMap* tb);
 cudaError_t step_tc_cluster(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
 
 }  // namespace rk

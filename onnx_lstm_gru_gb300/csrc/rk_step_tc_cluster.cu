@@ -7,7 +7,7 @@
 namespace rk {
 
 cudaError_t step_tc_cluster(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
-  return step_tc_mode_dispatch<2>(p, plan, s, resident, h16);
+  return step_tc_mode_dispatch<2>(p, plan, s, resident, h16, nullptr, nullptr);
 }
 
 }  // namespace rk

@@ -5,8 +5,9 @@
 
 namespace rk {
 
-cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16) {
-  return step_tc_mode_dispatch<1>(p, plan, s, resident, h16);
+cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
+                         const CUtensorMap* ta, const CUtensorMap* tb) {
+  return step_tc_mode_dispatch<1>(p, plan, s, resident, h16, ta, tb);
 }
 
 }  // namespace rk

@@ -180,7 +180,8 @@ def test_plans_without_device(handle):
     finally:
         rk.rk_destroy(h4)
     assert "step=grid" in plans["revlstm_peep_clip_s200_b4_i128_h1024_f32"]
-    assert "proj=tc step=tensor" in plans["bilstm_s512_b64_i1024_h1024_f16"]
+    # the projection runs on the SMs the 128 recurrence CTAs leave idle
+    assert "proj=fused step=tensor" in plans["bilstm_s512_b64_i1024_h1024_f16"]
     assert "step=tensor" in plans["bigru_s128_b8_i512_h512_f16_lbr1"]
     for name, text in plans.items():
         smem = int(re.search(r"smem=(\d+)", text).group(1))

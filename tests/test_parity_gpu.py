@@ -355,6 +355,29 @@ def test_tensor_core_step_with_odd_offsets(cell):
             assert torch.equal(got[k], aligned[k]), k
 
 
+@pytest.mark.parametrize("cell,H,N,direction", [("lstm", 576, 16, "bidirectional"),
+                                                ("gru", 640, 40, "reverse"),
+                                                ("rnn", 1024, 70, "forward")])
+def test_fused_projection_matches_separate(cell, H, N, direction):
+    """With flag-published tensor-core teams the projection runs on the SMs
+    the recurrence leaves idle, its tiles produced in the order the steps
+    consume them and each step waiting for its rows' tile.  The same tile
+    arithmetic as the projection's own launch: bit-identical outputs, and the
+    oracle's within the Half tolerance."""
+    pr = rk.Problem(cell, seq=6, batch=N, input=72, hidden=H, direction=direction, dtype="f16",
+                    linear_before_reset=1 if cell == "gru" else 0)
+    assert "proj=fused step=tensor" in layer().plan(pr)
+    assert "proj=tc step=tensor" in layer(rk.RK_SEPARATE_PROJECTION).plan(pr)
+    lens = list(np.random.default_rng(N).integers(0, 7, N))
+    inp = rand_inputs(pr, seed=H + N, lens=lens, scale=0.15)
+    got = run_gpu(pr, inp)
+    sep = run_gpu(pr, inp, flags=rk.RK_SEPARATE_PROJECTION)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], sep[k]), k
+    compare(pr, got, run_oracle(pr, inp), lens)
+
+
 @pytest.mark.parametrize("H,N,direction,layout,opts", [(40, 4, "bidirectional", 0, "plain"),
                                                      (96, 9, "reverse", 1, "full"),
                                                      (200, 16, "forward", 0, "full"),
@@ -450,7 +473,8 @@ def test_half_projection_tensor_cores(S, N, I, H):
     products of Half values, different summation order)."""
     pr = rk.Problem("rnn", seq=S, batch=N, input=I, hidden=H, direction="bidirectional", dtype="f16",
                     activations=[("affine", 1.0, 0.0)] * 2)
-    assert "proj=tc" in layer().plan(pr)
+    plan = layer().plan(pr)
+    assert "proj=tc" in plan or "proj=fused" in plan  # both the tcgen05 projection
     rng = np.random.default_rng(S + I)
     inp = {"X": rng.uniform(-1, 1, (S, N, I)).astype(np.float16),
            "W": rng.uniform(-0.1, 0.1, (2, H, I)).astype(np.float16),
