@@ -167,13 +167,13 @@ class ClockSampler:
 # Source files of each kernel, hashed so a committed ncu summary is only used
 # while the kernel it measured is unchanged.
 KERNEL_SOURCES = {
-    "fast": ("step_kernel", ("rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh")),
-    "cluster": ("step_cluster_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
-    "grid": ("step_grid_kernel", ("rk_step.cuh", "rk_step_launch.cuh")),
-    "tensor": ("step_tc_kernel", ("rk_step.cuh", "rk_step_tc.cuh", "rk_step_tc.cu", "rk_step_tc_pair.cu",
-                                  "rk_step_tc_cluster.cu", "rk_step_tcs.cu")),
-    "proj_tc": ("proj_tc_kernel", ("rk_proj_tc.cu",)),
-    "proj_simt": ("projection", ("rk_proj.cu",)),
+    "fast": ("step_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh")),
+    "cluster": ("step_cluster_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
+    "grid": ("step_grid_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
+    "tensor": ("step_tc_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_proj_tc.cuh", "rk_step_tc.cuh", "rk_step_tc.cu",
+                                  "rk_step_tc_pair.cu", "rk_step_tc_cluster.cu", "rk_step_tcs.cuh")),
+    "proj_tc": ("proj_tc_kernel", ("rk_elem.cuh", "rk_proj_tc.cuh", "rk_proj_tc.cu")),
+    "proj_simt": ("projection", ("rk_elem.cuh", "rk_proj.cu")),
 }
 
 
@@ -199,6 +199,7 @@ def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, alu_peak: f
     """Roofline entry of one kernel: tensor-core kernels against the measured
     dense bf16 rate (fp16 has the same nominal dense rate), FP32 SIMT kernels
     against the FP32 FMA rate derived from the SM count and clock."""
+    fp16 = "_f16" in workload
     achieved = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
     name, files = KERNEL_SOURCES[kind]
     traffic = profiled_traffic(name, workload, kernel_source_hash(files))
@@ -206,7 +207,8 @@ def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, alu_peak: f
         peak = float(peaks["bf16_tflops"])
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": name,
-                "peak_source": "measured dense bf16 burst; fp16 runs at the same nominal dense rate"}
+                "peak_source": "measured dense bf16 burst" +
+                               ("; fp16 runs at the same nominal dense rate" if fp16 else "")}
     return {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s", "frac": achieved / alu_peak,
             "traffic": traffic, "kernel": name, "peak_source": alu_src}
 
@@ -309,8 +311,14 @@ def run_gb300(args):
         name = f"{name}_seq{w.problem.seq}"
     pr = w.problem
     inp = workloads.make_inputs(w)
-    tdt = torch.float32 if pr.dtype == "f32" else torch.float16
-    dev_in = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    tdt = rk.torch_dtype(pr.dtype)
+
+    def host_tensor(k, v):
+        # bfloat16 inputs arrive as float32 arrays of bfloat16 numbers: exact cast
+        t = torch.from_numpy(v)
+        return t if k == "sequence_lens" else t.to(tdt)
+
+    dev_in = {k: host_tensor(k, v).to(dev) for k, v in inp.items()}
     shp = pr.shapes()
     outs = {n: torch.empty(shp[n], dtype=tdt, device=dev) for n in w.outputs if not (n == "Y_c" and pr.cell != "lstm")}
     layer = rk.RecurrentLayer()
@@ -369,8 +377,9 @@ def run_gb300(args):
     n_e2e = args.e2e_steps or max(3, min(args.steps, 300))
     pinned_in = {}
     for k, v in inp.items():
-        t = torch.empty(v.shape, dtype=torch.from_numpy(v).dtype, pin_memory=True)
-        t.copy_(torch.from_numpy(v))
+        hv = host_tensor(k, v)
+        t = torch.empty(hv.shape, dtype=hv.dtype, pin_memory=True)
+        t.copy_(hv)
         pinned_in[k] = t
     pinned_out = {n: torch.empty(shp[n], dtype=tdt, pin_memory=True) for n in outs}
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
@@ -428,7 +437,7 @@ def run_gb300(args):
     line = {
         "metric": METRIC, "value": gflops, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": vs, "dtype": "f32" if pr.dtype == "f32" else "f16 storage, f32 arithmetic",
+        "vs_baseline": vs, "dtype": "f32" if pr.dtype == "f32" else f"{pr.dtype} storage, f32 arithmetic",
         "data": "synthetic (seeded numpy PCG64, random weights)",
         "config": {"workload": name, "cell": pr.cell, "direction": pr.direction, "seq": pr.seq, "batch": pr.batch,
                    "input": pr.input, "hidden": pr.hidden, "layout": pr.layout, "tensor_dtype": pr.dtype,

@@ -8,7 +8,10 @@
  *     bidirectional; layouts 0 and 1; sequence_lens; initial states;
  *     peepholes; clip; input_forget; linear_before_reset; the eleven ONNX
  *     activations with alpha / beta resolved by the caller; all tensors
- *     float32 or all Half, with float32 accumulation and float32 state;
+ *     float32 or all Half, with float32 accumulation and float32 state
+ *     (bfloat16 tensors as a third type, the way the web page "Matrix
+ *     multiplication (Gemm)" admits them in its first paragraph, same
+ *     float32 arithmetic);
  *   - the C# example and the paragraph after it: a problem description
  *     (RecurrentProblem) and an operand list X, W, R, B, sequence_lens,
  *     initial_h, initial_c, P, Y, Y_h, Y_c, each a buffer plus an element
@@ -38,8 +41,9 @@
  *   Y            [S, D, N, H] (layout 0) or [N, S, D, H]  optional output
  *   Y_h          [D, N, H]   (layout 0) or [N, D, H]      optional output
  *   Y_c          same as Y_h, LSTM only                   optional output
- * Every tensor other than sequence_lens has the problem's dtype (float32 or
- * IEEE binary16).  Outputs are rounded to nearest even when Half.
+ * Every tensor other than sequence_lens has the problem's dtype (float32,
+ * IEEE binary16 or bfloat16).  Inputs are widened exactly to float32;
+ * outputs are rounded to nearest even when 16-bit.
  *
  * Ownership: every tensor pointer is caller-owned DEVICE memory (except in
  * rk_encode_host, which takes host memory).  The library never frees or
@@ -67,7 +71,7 @@ typedef int32_t rk_status;
 
 enum rk_cell { RK_LSTM = 0, RK_GRU = 1, RK_RNN = 2 };
 enum rk_direction { RK_FORWARD = 0, RK_REVERSE = 1, RK_BIDIRECTIONAL = 2 };
-enum rk_dtype { RK_F32 = 0, RK_F16 = 1 };
+enum rk_dtype { RK_F32 = 0, RK_F16 = 1, RK_BF16 = 2 };
 enum rk_activation_kind {
   RK_ACT_SIGMOID = 0,
   RK_ACT_TANH = 1,
@@ -83,10 +87,10 @@ enum rk_activation_kind {
 };
 
 /* rk_create flags */
-#define RK_FORCE_SIMT_PROJECTION 1u /* Half problems: SIMT projection, no tensor cores */
+#define RK_FORCE_SIMT_PROJECTION 1u /* 16-bit problems: SIMT projection, no tensor cores */
 #define RK_FORCE_GRID_STEP 2u       /* use the grid-wide step kernel even where a cluster fits */
 #define RK_FORCE_GENERAL_STEP 4u    /* never the one-row-per-cluster register-resident step kernel */
-#define RK_FORCE_SIMT_STEP 8u       /* Half problems: never the tensor-core step kernel */
+#define RK_FORCE_SIMT_STEP 8u       /* 16-bit problems: never the tensor-core step kernel */
 #define RK_SEPARATE_PROJECTION 16u  /* never compute the projection on the SMs the tensor-core
                                        recurrence leaves idle (always a launch of its own) */
 
@@ -160,8 +164,8 @@ int64_t rk_xw_length(const rk_problem* p);
 
 /* Floats of state scratch the problem needs (StateLength): 256 barrier
  * words, the double-buffered hidden state exchanged between blocks of the
- * step kernel, 2 * D * N * KP, and a region for r (.) h or the Half copies of
- * h used by the tensor cores, D * (N + 128) * KP (KP = hidden rounded up to a
+ * step kernel, 2 * D * N * KP, and a region for r (.) h or the 16-bit copies
+ * of h used by the tensor cores, D * (N + 128) * KP (KP = hidden rounded up to a
  * multiple of 128).  Returns -1 for an invalid problem. */
 int64_t rk_state_length(const rk_problem* p);
 

@@ -35,7 +35,7 @@ RK_FORCE_SIMT_STEP = 8
 RK_SEPARATE_PROJECTION = 16
 CELLS = {"lstm": 0, "gru": 1, "rnn": 2}
 DIRECTIONS = {"forward": 0, "reverse": 1, "bidirectional": 2}
-DTYPES = {"f32": 0, "float32": 0, "f16": 1, "float16": 1, "half": 1}
+DTYPES = {"f32": 0, "float32": 0, "f16": 1, "float16": 1, "half": 1, "bf16": 2, "bfloat16": 2}
 ACTIVATIONS = {
     "sigmoid": 0, "tanh": 1, "relu": 2, "affine": 3, "leakyrelu": 4, "thresholdedrelu": 5,
     "scaledtanh": 6, "hardsigmoid": 7, "elu": 8, "softsign": 9, "softplus": 10,
@@ -279,6 +279,12 @@ class Problem:
         }
 
 
+def torch_dtype(dtype: str):
+    """The torch element type of a problem's tensors (all but sequence_lens)."""
+    import torch
+    return (torch.float32, torch.float16, torch.bfloat16)[DTYPES[dtype]]
+
+
 def _tensor_ref(t, offset: int = 0) -> rk_tensor:
     r = rk_tensor()
     if t is None:
@@ -352,6 +358,14 @@ class RecurrentLayer:
     def encode(self, problem: Problem, stream=None, scratch: Optional[rk_scratch] = None, **tensors):
         import torch
         s = stream if stream is not None else torch.cuda.current_stream()
+        want = torch_dtype(problem.dtype)
+        for name, v in tensors.items():
+            t = v[0] if isinstance(v, tuple) else v
+            if t is None:
+                continue
+            need = torch.int32 if name == "sequence_lens" else want
+            if t.dtype != need:
+                raise TypeError(f"{name}: expected {need}, got {t.dtype}")
         ops = operands_from_tensors(**tensors)
         self._check(rk_encode(self.handle, problem.to_c(), ops, scratch, s.cuda_stream))
 
@@ -379,7 +393,7 @@ class RecurrentLayer:
     def forward(self, problem: Problem, X, W, R, B=None, sequence_lens=None, initial_h=None,
                 initial_c=None, P=None, want=("Y", "Y_h", "Y_c"), stream=None):
         import torch
-        dt = torch.float32 if DTYPES[problem.dtype] == 0 else torch.float16
+        dt = torch_dtype(problem.dtype)
         shp = problem.shapes()
         outs = {}
         for name in want:

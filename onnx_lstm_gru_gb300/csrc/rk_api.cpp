@@ -121,7 +121,8 @@ rk_status validate_problem(rk_handle* h, const rk_problem* p) {
   const char* cn = cell_name(p->cell);
   if (p->direction < RK_FORWARD || p->direction > RK_BIDIRECTIONAL)
     return fail(h, RK_ERR_SHAPE, "%s: direction: unknown value %d", cn, p->direction);
-  if (p->dtype != RK_F32 && p->dtype != RK_F16) return fail(h, RK_ERR_SHAPE, "%s: dtype: unknown value %d", cn, p->dtype);
+  if (p->dtype != RK_F32 && p->dtype != RK_F16 && p->dtype != RK_BF16)
+    return fail(h, RK_ERR_SHAPE, "%s: dtype: unknown value %d", cn, p->dtype);
   if (p->layout != 0 && p->layout != 1) return fail(h, RK_ERR_SHAPE, "%s: layout: must be 0 or 1, got %d", cn, p->layout);
   const int64_t lim = 0x7fffffffLL;
   if (p->seq < 0 || p->seq > lim) return fail(h, RK_ERR_SHAPE, "%s: seq: %lld out of range", cn, (long long)p->seq);
@@ -188,7 +189,7 @@ int64_t xw_len(const rk_problem* p) {
 int64_t kp_of(const rk_problem* p) { return round_up(std::max<int64_t>(p->hidden, 1), rk::kKChunk); }
 int64_t state_len(const rk_problem* p) {
   // barrier counters, the double-buffered float32 h of the grid kernel, and a
-  // region for r.h (grid kernel) or the Half copies of h (tensor-core kernel)
+  // region for r.h (grid kernel) or the 16-bit copies of h (tensor-core kernel)
   return rk::kStateHeader + 2 * (int64_t)dirs_of(p) * p->batch * kp_of(p) +
          (int64_t)dirs_of(p) * (p->batch + 128) * kp_of(p);
 }
@@ -246,7 +247,7 @@ struct FusedProj {
 FusedProj fused_projection(const rk_handle* h, const rk_problem* p, const StepPlan& pl, const rk::ProjParams& pp,
                            bool has_projection, CUtensorMap* tmA, CUtensorMap* tmB) {
   FusedProj f;
-  if (!has_projection || pl.kind != rk::kStepTensor || pl.J != 16 || p->layout != 0 || p->dtype != RK_F16 ||
+  if (!has_projection || pl.kind != rk::kStepTensor || pl.J != 16 || p->layout != 0 || p->dtype == RK_F32 ||
       (h->flags & (RK_FORCE_SIMT_PROJECTION | RK_SEPARATE_PROJECTION)) || p->input % 8 != 0)
     return f;
   const int D = dirs_of(p);
@@ -313,9 +314,9 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     }
     return teams;
   };
-  // tensor-core kernel: Half layers with a batch worth a dense product
-  // (R . h on tcgen05), every CTA of the launch resident at once
-  if (p->dtype == RK_F16 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
+  // tensor-core kernel: 16-bit layers (Half or bfloat16) with a batch worth
+  // a dense product (R . h on tcgen05), every CTA of the launch resident at once
+  if (p->dtype != RK_F32 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
       H % 8 == 0 && N >= 4) {
     // at most 16 rows per direction: the gate rows are the MMA's M and the
     // batch its N, one cluster of ceil(H / 32) CTAs per direction
@@ -588,7 +589,7 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
     return RK_OK;
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
-  const bool tc = p->dtype == RK_F16 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
+  const bool tc = p->dtype != RK_F32 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
   rk::ProjParams pp{};
   pp.M = (int)(p->seq * p->batch);
   const bool fused = fused_projection(h, p, pl, pp, p->seq > 0 && p->input > 0, nullptr, nullptr).on;

@@ -5,17 +5,16 @@
 //
 // X is [M, K] (M = seq * batch rows in X's storage order, K = input), W[d] is
 // [N, K] (N = gates * hidden), Xw[d] is [M, N] float32.  Elements are read
-// as float or Half and widened; every product and sum is float32 with fused
-// multiply-add, one chain per output element in increasing k, so the result
-// does not depend on scheduling.
+// as float32, Half or bfloat16 and widened; every product and sum is float32
+// with fused multiply-add, one chain per output element in increasing k, so
+// the result does not depend on scheduling.
 //
 // Two kernels.  The pipelined one (below) serves 16-byte aligned operands.
 // The fallback serves any M, N, K and any element offset: a 64 x 64 tile of
 // Xw per 256-thread CTA, k in steps of 16 staged through shared memory
 // k-major (so each thread reads its 4 rows and 4 columns as float4), 4 x 4
 // outputs per thread, bounds-checked element-wise loads.
-#include <cuda_fp16.h>
-
+#include "rk_elem.cuh"
 #include "rk_internal.h"
 
 namespace rk {
@@ -25,11 +24,7 @@ namespace {
 constexpr int BM = 64, BN = 64, BK = 16, PADM = 4;
 
 template <typename T>
-__device__ __forceinline__ float widen(T v);
-template <>
-__device__ __forceinline__ float widen<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float widen<__half>(__half v) { return __half2float(v); }
+__device__ __forceinline__ float widen(T v) { return Elem<T>::to_f(v); }
 
 template <typename T>
 __global__ void __launch_bounds__(256) proj_simt_kernel(int M, int N, int K, const T* __restrict__ X,
@@ -121,17 +116,12 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 template <typename T>
-__device__ __forceinline__ float4 load4_row(const T* p);
+__device__ __forceinline__ float4 load4_row(const T* p) {
+  return load4_16(p);
+}
 template <>
 __device__ __forceinline__ float4 load4_row<float>(const float* p) {
   return *reinterpret_cast<const float4*>(p);
-}
-template <>
-__device__ __forceinline__ float4 load4_row<__half>(const __half* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  return make_float4(a.x, a.y, b.x, b.y);
 }
 
 template <typename T, int PBM>
@@ -246,6 +236,7 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool small = tiles32 < 2LL * sms;
     if (p.dtype == 0) return small ? launch_pipe<float, 16>(p, s) : launch_pipe<float, 32>(p, s);
+    if (p.dtype == 2) return small ? launch_pipe<__nv_bfloat16, 16>(p, s) : launch_pipe<__nv_bfloat16, 32>(p, s);
     return small ? launch_pipe<__half, 16>(p, s) : launch_pipe<__half, 32>(p, s);
   }
   dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.D);
@@ -253,6 +244,9 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   if (p.dtype == 0) {
     proj_simt_kernel<float><<<grid, 256, 0, s>>>(p.M, p.N, p.K, static_cast<const float*>(p.X),
                                                   static_cast<const float*>(p.W), p.Xw);
+  } else if (p.dtype == 2) {
+    proj_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p.M, p.N, p.K, static_cast<const __nv_bfloat16*>(p.X),
+                                                          static_cast<const __nv_bfloat16*>(p.W), p.Xw);
   } else {
     proj_simt_kernel<__half><<<grid, 256, 0, s>>>(p.M, p.N, p.K, static_cast<const __half*>(p.X),
                                                    static_cast<const __half*>(p.W), p.Xw);

@@ -1,14 +1,14 @@
-// rk_proj_tc.cuh -- the tcgen05 input projection of Half layers as a device
-// routine (web page "Recurrent layers", section "How a layer runs", step 1:
-// Xw[d] = X . W[d]^T, one batched product; Fast mode may use matrix hardware
-// for Half).  Products of Half values are exact in float32 and the tensor
-// cores accumulate in float32; the order is fixed by the tile shape, so runs
-// are bit-identical.  Used by the standalone projection kernel
-// (rk_proj_tc.cu) and by the step kernel that computes the projection on the
-// SMs the recurrence leaves idle (rk_step_tc.cuh).
+// rk_proj_tc.cuh -- the tcgen05 input projection of 16-bit layers (Half or
+// bfloat16) as a device routine (web page "Recurrent layers", section "How a
+// layer runs", step 1: Xw[d] = X . W[d]^T, one batched product; Fast mode may
+// use matrix hardware for Half).  Products of two 16-bit values are exact in
+// float32 and the tensor cores accumulate in float32; the order is fixed by
+// the tile shape, so runs are bit-identical.  Used by the standalone
+// projection kernel (rk_proj_tc.cu) and by the step kernel that computes the
+// projection on the SMs the recurrence leaves idle (rk_step_tc.cuh).
 //
-// X is [M, K] and W is [D*N, K], both Half and K-contiguous (K-major
-// operands); Xw is [D, M, N] float32.  Requirements (else the SIMT kernel
+// X is [M, K] and W is [D*N, K], both of one 16-bit type and K-contiguous
+// (K-major operands); Xw is [D, M, N] float32.  Requirements (else the SIMT kernel
 // runs): X and W 16-byte aligned, K a multiple of 8 (TMA strides), M, N, K > 0.
 //
 // One CTA per SM, 192 threads:
@@ -27,11 +27,11 @@
 // flight, frees its TMEM and returns.
 #pragma once
 #include <cuda.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "rk_elem.cuh"
 #include "rk_internal.h"
 
 namespace rk {
@@ -109,7 +109,9 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 // Instruction descriptor: kind::f16, A and B F16, D F32, both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(TBN >> 3) << 17) | ((uint32_t)(TBM >> 4) << 24);
+// kind::f16 instruction descriptor: D float32, A and B K-major, M = 128,
+// N = 256; the A/B type fields (Half or bfloat16) are or-ed in per layer
+constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(TBN >> 3) << 17) | ((uint32_t)(TBM >> 4) << 24);
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -127,13 +129,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // D * mt * nt tiles, tile_of(tile) giving its (direction, first row, first
 // column), signal(d, m0) called by lane 0 of each epilogue warp once its 32
 // rows of the tile are stored and fenced.  tsm: 1024-byte aligned shared
-// memory of kTcSmem - 1024 bytes.  Warps 0-5 take the roles; further warps
-// of the block only pass the block-wide barriers.
+// memory of kTcSmem - 1024 bytes.  idesc: kIdescBase or-ed with the
+// element type's A/B fields.  Warps 0-5 take the roles; further warps of the
+// block only pass the block-wide barriers.
 template <class TileOf, class Signal>
 __device__ __forceinline__ void proj_tc_body(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K,
                                              int D, float* __restrict__ Xw, int vec_store, int* status,
                                              long long timeout_ns, unsigned char* tsm, int pb, int np,
-                                             TileOf tile_of, Signal signal) {
+                                             uint32_t idesc, TileOf tile_of, Signal signal) {
   unsigned char* sA = tsm;
   unsigned char* sB = tsm + TSTAGES * kStageBytesA;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + TSTAGES * kStageBytesB);
@@ -238,9 +241,9 @@ __device__ __forceinline__ void proj_tc_body(const CUtensorMap* tmA, const CUten
           // advance 16 elements (32 bytes) along K inside the swizzle atom
           const uint64_t ad = adesc0 + (uint64_t)stage * (kStageBytesA >> 4);
           const uint64_t bd = bdesc0 + (uint64_t)stage * (kStageBytesB >> 4);
-          tc_mma(tmem_d, ad, bd, kIdesc, kb != 0 ? 1u : 0u);
+          tc_mma(tmem_d, ad, bd, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 1; k < TBK / 16; ++k) tc_mma(tmem_d, ad + 2 * k, bd + 2 * k, kIdesc, 1u);
+          for (int k = 1; k < TBK / 16; ++k) tc_mma(tmem_d, ad + 2 * k, bd + 2 * k, idesc, 1u);
           tc_commit(su32(&bars[4 + stage]));  // stage free once these MMAs complete
           if (++stage == TSTAGES) {
             stage = 0;

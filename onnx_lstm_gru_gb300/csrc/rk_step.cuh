@@ -36,9 +36,9 @@
 // sets bit 0 of the status word and the kernel winds down without hanging.
 #pragma once
 
-#include <cuda_fp16.h>
 #include <cstdint>
 
+#include "rk_elem.cuh"
 #include "rk_internal.h"
 
 namespace rk {
@@ -122,32 +122,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------------ element access
 template <typename T>
-__device__ __forceinline__ float load_elem(const T* p);
-template <>
-__device__ __forceinline__ float load_elem<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float load_elem<__half>(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ float load_elem(const T* p) { return Elem<T>::to_f(*p); }
 
 template <typename T>
-__device__ __forceinline__ void store_elem(T* p, float v);
-template <>
-__device__ __forceinline__ void store_elem<float>(float* p, float v) { *p = v; }
-template <>
-__device__ __forceinline__ void store_elem<__half>(__half* p, float v) { *p = __float2half_rn(v); }
+__device__ __forceinline__ void store_elem(T* p, float v) { *p = Elem<T>::from_f(v); }
 
 // 4 consecutive R elements from shared memory as floats (16-byte aligned rows).
 template <typename T>
-__device__ __forceinline__ float4 load4_smem(const T* p);
+__device__ __forceinline__ float4 load4_smem(const T* p) { return load4_16(p); }
 template <>
 __device__ __forceinline__ float4 load4_smem<float>(const float* p) {
   return *reinterpret_cast<const float4*>(p);
-}
-template <>
-__device__ __forceinline__ float4 load4_smem<__half>(const __half* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // ------------------------------------------------------------------ activations

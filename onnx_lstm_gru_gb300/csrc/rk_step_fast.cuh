@@ -59,29 +59,27 @@ __host__ __device__ inline FastSmem fast_smem_layout(const StepParams& p) {
   return L;
 }
 
-// R fragment kept in registers: 4 consecutive k of one row.
+// R fragment kept in registers: 4 consecutive k of one row, in the storage
+// type (two packed 16-bit pairs for Half and bfloat16).
 template <typename T>
-struct RFrag;
+struct RFrag {
+  uint2 v;
+  __device__ __forceinline__ float4 get() const {
+    const float2 a = Elem<T>::pair_to_f(v.x);
+    const float2 b = Elem<T>::pair_to_f(v.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  // the values come from the stored tensor, so the rounding is exact
+  __device__ __forceinline__ void set(const float e[4]) {
+    v.x = Elem<T>::pair_from_f(e[0], e[1]);
+    v.y = Elem<T>::pair_from_f(e[2], e[3]);
+  }
+};
 template <>
 struct RFrag<float> {
   float4 v;
   __device__ __forceinline__ float4 get() const { return v; }
   __device__ __forceinline__ void set(const float e[4]) { v = make_float4(e[0], e[1], e[2], e[3]); }
-};
-template <>
-struct RFrag<__half> {
-  uint2 v;
-  __device__ __forceinline__ float4 get() const {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-  }
-  __device__ __forceinline__ void set(const float e[4]) {
-    __half2 a = __floats2half2_rn(e[0], e[1]);
-    __half2 b = __floats2half2_rn(e[2], e[3]);
-    v.x = *reinterpret_cast<uint32_t*>(&a);
-    v.y = *reinterpret_cast<uint32_t*>(&b);
-  }
 };
 
 __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar) {
@@ -556,6 +554,7 @@ cudaError_t step_fast_dtype(const StepParams& p, const StepPlan& plan, cudaStrea
 template <int CELL>
 cudaError_t step_fast_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q) {
   if (p.dtype == 0) return step_fast_dtype<CELL, float>(p, plan, s, q);
+  if (p.dtype == 2) return step_fast_dtype<CELL, __nv_bfloat16>(p, plan, s, q);
   return step_fast_dtype<CELL, __half>(p, plan, s, q);
 }
 

@@ -77,6 +77,10 @@ cudaError_t step_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s
     return gen ? step_launch_shape<CELL, float, true, GRID>(p, plan, s, q)
                : step_launch_shape<CELL, float, false, GRID>(p, plan, s, q);
   }
+  if (p.dtype == 2) {
+    return gen ? step_launch_shape<CELL, __nv_bfloat16, true, GRID>(p, plan, s, q)
+               : step_launch_shape<CELL, __nv_bfloat16, false, GRID>(p, plan, s, q);
+  }
   return gen ? step_launch_shape<CELL, __half, true, GRID>(p, plan, s, q)
              : step_launch_shape<CELL, __half, false, GRID>(p, plan, s, q);
 }

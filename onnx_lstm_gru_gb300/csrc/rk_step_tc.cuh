@@ -1,19 +1,20 @@
 // rk_step_tc.cuh -- persistent recurrent-step kernel on the tcgen05 tensor
-// cores, for Half layers whose batch makes R . h a dense product.
+// cores, for 16-bit layers (Half or bfloat16: the element type E) whose
+// batch makes R . h a dense product.
 //
 // What it computes is the same as rk_step.cuh (web page "Recurrent layers",
 // sections "How a layer runs" and "Arithmetic and determinism"): per step and
 // gate row pre = ((xw + rec) + Wb) + Rb with rec = R_row . h_prev, then
 // peepholes, clip, activation and state update (LSTM, RNN, GRU with
 // linear_before_reset = 1).  The state (h, c) stays float32 in registers;
-// the product's h operand is the state rounded to Half, so R (Half, exact)
+// the product's h operand is the state rounded to E, so R (E, exact)
 // times that operand is exact in float32 and summed in float32.
 //
 // Layout: a team per (direction, group of up to 128 batch rows); a team is
 // ceil(H / 16) CTAs, each owning 16 hidden units, all CTAs of the launch
 // co-resident (cooperative launch).  A CTA keeps its 16 units' G rows of R in
 // shared memory, unit-major (row u*G + g), in the 128-byte swizzled K-major
-// layout the tensor cores read.  The Half copy of the exchanged h lives in
+// layout the tensor cores read.  The 16-bit copy of the exchanged h lives in
 // global memory as 16 KB regions already in that layout, one 128-row x 64 k
 // tile each: for a team of more than 64 rows a region is one 64-wide k block
 // of rows 0..127; for a team of at most 64 rows (PAIR) a region holds two
@@ -38,7 +39,7 @@
 //      batch row 4 l + w % 4, one the even and one the odd partial sum,
 //      they swap halves with a shuffle and take half the units each.  Each thread
 //      does the gate arithmetic with its units' c and h in registers and the
-//      next step's xw prefetched, writes its piece of the Half copy of the new
+//      next step's xw prefetched, writes its piece of the 16-bit copy of the new
 //      h and publishes it (proxy fence, then a release store of the CTA's step
 //      count to its flag), then writes Y.
 // The three roles run their own loops, linked by mbarriers; no barrier spans
@@ -61,8 +62,8 @@ namespace rk {
 namespace {
 
 constexpr int SB = 128;          // batch rows per team (MMA M)
-constexpr int SK = 64;           // k per ring stage (one 128-byte swizzle atom of Half)
-constexpr int SSTAGE = 16 * 1024; // one ring stage: a 128-row x 64 k tile of Half
+constexpr int SK = 64;           // k per ring stage (one 128-byte swizzle atom)
+constexpr int SSTAGE = 16 * 1024; // one ring stage: a 128-row x 64 k tile
 constexpr int SMAXST = 8;         // most ring stages
 constexpr int SJ = 16;           // hidden units per CTA (teams published by flags)
 constexpr int SJC = 32;          // hidden units per CTA of a cluster team
@@ -128,7 +129,8 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   d |= (uint64_t)2 << 61;
   return d;
 }
-// kind::f16, A and B Half, D float32, both K-major, M = 128, N = n.
+// kind::f16, D float32, both K-major, M = 128, N = n; the A/B type fields
+// (Half or bfloat16, Elem<E>::kMmaAB) are or-ed in by the caller.
 __device__ __forceinline__ uint32_t idesc_f16(int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(SB >> 4) << 24);
 }
@@ -172,15 +174,15 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[NCOL]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// UH Half values to 16 (UH = 8) or 8 (UH = 4) aligned bytes.
-template <int UH>
-__device__ __forceinline__ void store_halves(__half* dst, const __half (&v)[UH]) {
+// UH 16-bit values to 16 (UH = 8) or 8 (UH = 4) aligned bytes.
+template <int UH, typename E>
+__device__ __forceinline__ void store_halves(E* dst, const E (&v)[UH]) {
   if constexpr (UH == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(v);
   else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(v);
 }
 
 
-// Shared memory: [R slice: KB blocks of (16 G rows x 64 k) Half][ring: stages x 16 KB][barriers][biases]
+// Shared memory: [R slice: KB blocks of (16 G rows x 64 k) E][ring: stages x 16 KB][barriers][biases]
 struct TcSmem {
   size_t r, ring, bar, bias, total;
 };
@@ -197,7 +199,7 @@ __host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages, int s
   return L;
 }
 
-// Region (16 KB, 8192 Half) of the Half h copy: buffer, direction, team, region.
+// Region (16 KB, 8192 elements) of the 16-bit h copy: buffer, direction, team, region.
 __device__ __forceinline__ size_t h16_region(const StepParams& p, int buf, int d, int team_in_dir, int region, int NREG) {
   return ((((size_t)buf * p.D + d) * p.teams_per_dir + team_in_dir) * NREG + region) * (size_t)(SSTAGE / 2);
 }
@@ -217,8 +219,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // blocks, 16 units per CTA, flags; MODE 2: as MODE 1 with 32 units per CTA
 // and the team one thread-block cluster, published by remote mbarrier
 // arrivals instead of flags.
-template <int CELL, bool GEN, bool PLAIN, int MODE>
-__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, __half* __restrict__ h16,
+template <int CELL, bool GEN, bool PLAIN, int MODE, typename E>
+__global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p, E* __restrict__ h16,
                                                              const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB) {
   constexpr bool PAIR = MODE >= 1;
@@ -252,8 +254,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
         atomicAdd(p.xw_ready + (size_t)dd * p.xw_groups + (m0 / ptc::TBM) / p.xw_mpg, 1u);
       };
       ptc::proj_tc_body(&tmA, &tmB, p.pj_M, G * p.H, p.pj_K, p.D, const_cast<float*>(p.xw), p.pj_vec, p.status,
-                        p.timeout_ns, base, (int)blockIdx.x - p.step_ctas, (int)gridDim.x - p.step_ctas, tile_of,
-                        signal);
+                        p.timeout_ns, base, (int)blockIdx.x - p.step_ctas, (int)gridDim.x - p.step_ctas,
+                        ptc::kIdescBase | Elem<E>::kMmaAB, tile_of, signal);
       return;
     }
   }
@@ -294,12 +296,12 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const int NREG = (KB + BPR - 1) / BPR;  // regions per step
   const bool reverse = p.direction == 1 || (p.direction == 2 && d == 1);
   const size_t GH = (size_t)G * H;
-  const __half* R = static_cast<const __half*>(p.R);
-  const __half* Bias = static_cast<const __half*>(p.Bias);
-  const __half* P = static_cast<const __half*>(p.P);
-  const __half* h0 = static_cast<const __half*>(p.h0);
-  const __half* c0 = static_cast<const __half*>(p.c0);
-  __half* Y = static_cast<__half*>(p.Y);
+  const E* R = static_cast<const E*>(p.R);
+  const E* Bias = static_cast<const E*>(p.Bias);
+  const E* P = static_cast<const E*>(p.P);
+  const E* h0 = static_cast<const E*>(p.h0);
+  const E* c0 = static_cast<const E*>(p.c0);
+  E* Y = static_cast<E*>(p.Y);
 
   // ---------------- prologue: R slice (unit-major rows, swizzled), biases, barriers, TMEM
   // 8 consecutive k (16 bytes) at a time: H is a multiple of 8, so a chunk
@@ -313,11 +315,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     const int u = r / G, g = r % G, k = kb * SK + kk;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (j0 + u < H && k < H) {
-      const __half* src = R + ((size_t)d * GH + (size_t)g * H + j0 + u) * H + k;
+      const E* src = R + ((size_t)d * GH + (size_t)g * H + j0 + u) * H + k;
       if (r_vec) {
         v = __ldg(reinterpret_cast<const uint4*>(src));
       } else {
-        __align__(16) __half t8[8];
+        __align__(16) E t8[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) t8[i] = src[i];
         v = *reinterpret_cast<const uint4*>(t8);
@@ -328,12 +330,12 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   for (int e = tid; e < NR; e += blockDim.x) {
     const int u = e / G, g = e % G;
     const bool ok = j0 + u < H && Bias != nullptr;
-    wb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + (size_t)g * H + j0 + u]) : 0.0f;
-    rb_s[e] = ok ? __half2float(Bias[(size_t)d * 2 * GH + GH + (size_t)g * H + j0 + u]) : 0.0f;
+    wb_s[e] = ok ? Elem<E>::to_f(Bias[(size_t)d * 2 * GH + (size_t)g * H + j0 + u]) : 0.0f;
+    rb_s[e] = ok ? Elem<E>::to_f(Bias[(size_t)d * 2 * GH + GH + (size_t)g * H + j0 + u]) : 0.0f;
   }
   for (int e = tid; e < 3 * SJT; e += blockDim.x) {
     const int u = e / 3, g = e % 3;
-    pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? __half2float(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
+    pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? Elem<E>::to_f(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
   }
   if (tid == 0) {
     for (int i = 0; i < SMAXST; ++i) {
@@ -371,11 +373,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   const int bg = b0 + br;  // global batch row
   float hreg[UH], creg[UH];
   int len = Tn;
-  // address of (this thread's batch row, unit j) in buffer buf of the Half h copy
+  // address of (this thread's batch row, unit j) in buffer buf of the 16-bit h copy
   auto h16_at = [&](int buf, int j) {
     const int kb = j / SK;
     const int row = PAIR ? 32 * (br & 3) + 16 * (kb & 1) + (br >> 2) : br;
-    return reinterpret_cast<__half*>(reinterpret_cast<unsigned char*>(h16 + h16_region(p, buf, d, tin, kb / BPR, NREG)) +
+    return reinterpret_cast<E*>(reinterpret_cast<unsigned char*>(h16 + h16_region(p, buf, d, tin, kb / BPR, NREG)) +
                                      sw128_offset(row, j % SK));
   };
   if (grow) {
@@ -384,14 +386,14 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       len = len < 0 ? 0 : (len > S ? S : len);
       len = len > Tn ? Tn : len;
     }
-    __align__(16) __half hv[UH];
+    __align__(16) E hv[UH];
 #pragma unroll
     for (int u = 0; u < UH; ++u) {
       const int j = j0 + uh0 + u;
       const size_t si = state_index(p, d, bg, j < H ? j : 0);
-      hreg[u] = (j < H && h0 != nullptr) ? __half2float(h0[si]) : 0.0f;
-      creg[u] = (CELL == 0 && j < H && c0 != nullptr) ? __half2float(c0[si]) : 0.0f;
-      hv[u] = __float2half_rn(j < H ? hreg[u] : 0.0f);  // units past H: the k padding of the product
+      hreg[u] = (j < H && h0 != nullptr) ? Elem<E>::to_f(h0[si]) : 0.0f;
+      creg[u] = (CELL == 0 && j < H && c0 != nullptr) ? Elem<E>::to_f(c0[si]) : 0.0f;
+      hv[u] = Elem<E>::from_f(j < H ? hreg[u] : 0.0f);  // units past H: the k padding of the product
     }
     store_halves<UH>(h16_at(0, j0 + uh0), hv);  // h_0 into buffer 0
     // k columns past the last CTA's units (up to the 64-wide block) belong to
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     // Inf or NaN times zero would not be)
     if (rank == C - 1 && uh0 == 0) {
       for (int k = C * SJT; k < KB * SK; ++k)
-        for (int buf = 0; buf < 2; ++buf) *h16_at(buf, k) = __float2half_rn(0.0f);
+        for (int buf = 0; buf < 2; ++buf) *h16_at(buf, k) = Elem<E>::from_f(0.0f);
     }
   } else {
 #pragma unroll
@@ -614,10 +616,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     if (lane == 0) {
       // only the start-address field (address / 16, bits 0-13) differs
       // between the MMAs' descriptors; every address stays below 256 KB
-      const uint32_t idesc = idesc_f16(NR);
+      const uint32_t idesc = idesc_f16(NR) | Elem<E>::kMmaAB;
       const uint64_t adesc0 = desc_sw128(su32(sRing));
       const uint64_t bdesc0 = desc_sw128(su32(sR));
-      constexpr uint64_t kK16 = 32 >> 4;                      // 16 Half of k
+      constexpr uint64_t kK16 = 32 >> 4;                      // 16 elements of k
       constexpr uint64_t kStageD = SSTAGE >> 4;
       constexpr uint64_t kBlockD = (uint64_t)NR * 128 >> 4;  // one k block of R
       int st = 0;
@@ -760,20 +762,20 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       }
       // the UH units are one 8- or 16-byte piece of their k block's row
       const int jb = j0 + uh0;
-      __align__(16) __half hv[UH], yv[UH];
+      __align__(16) E hv[UH], yv[UH];
 #pragma unroll
       for (int u = 0; u < UH; ++u) {
         const bool in = jb + u < H;
         if (in) hreg[u] = hn[u];
-        hv[u] = __float2half_rn(in ? hn[u] : 0.0f);
-        yv[u] = __float2half_rn(active ? hn[u] : 0.0f);
+        hv[u] = Elem<E>::from_f(in ? hn[u] : 0.0f);
+        yv[u] = Elem<E>::from_f(active ? hn[u] : 0.0f);
       }
       if (s + 1 < Tn) {
         if (grow) store_halves<UH>(h16_at((s + 1) & 1, jb), hv);
         publish((unsigned)s + 2u, pub_parity++ & 1u);
       }
       if (grow && Y != nullptr) {
-        __half* ydst = Y + y_index(p, t, d, bg, jb);
+        E* ydst = Y + y_index(p, t, d, bg, jb);
         if (jb + UH <= H && (reinterpret_cast<uintptr_t>(ydst) % (2 * UH)) == 0) {
           store_halves<UH>(ydst, yv);
         } else {
@@ -794,11 +796,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
         const int j = j0 + uh0 + u;
         if (j >= H) continue;
         if (Y != nullptr)
-          for (int t = Tn; t < S; ++t) Y[y_index(p, t, d, bg, j)] = __float2half_rn(0.0f);
+          for (int t = Tn; t < S; ++t) Y[y_index(p, t, d, bg, j)] = Elem<E>::from_f(0.0f);
         const bool zero = S > 0 && len == 0;
         const size_t si = state_index(p, d, bg, j);
-        if (p.Yh != nullptr) static_cast<__half*>(p.Yh)[si] = __float2half_rn(zero ? 0.0f : hreg[u]);
-        if (CELL == 0 && p.Yc != nullptr) static_cast<__half*>(p.Yc)[si] = __float2half_rn(zero ? 0.0f : creg[u]);
+        if (p.Yh != nullptr) static_cast<E*>(p.Yh)[si] = Elem<E>::from_f(zero ? 0.0f : hreg[u]);
+        if (CELL == 0 && p.Yc != nullptr) static_cast<E*>(p.Yc)[si] = Elem<E>::from_f(zero ? 0.0f : creg[u]);
       }
     }
   }
@@ -812,10 +814,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   if constexpr (CLU) asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int CELL, bool GEN, bool PLAIN, int MODE>
-cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
+template <int CELL, bool GEN, bool PLAIN, int MODE, typename E>
+cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, E* h16,
                            const CUtensorMap* ta, const CUtensorMap* tb) {
-  auto kern = step_tc_kernel<CELL, GEN, PLAIN, MODE>;
+  auto kern = step_tc_kernel<CELL, GEN, PLAIN, MODE, E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -859,31 +861,37 @@ cudaError_t step_tc_launch(const StepParams& p, const StepPlan& plan, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, p, h16, ta != nullptr ? *ta : kNoMap, tb != nullptr ? *tb : kNoMap);
 }
 
-template <int MODE>
-cudaError_t step_tc_mode_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, __half* h16,
+template <int MODE, typename E>
+cudaError_t step_tc_mode_dispatch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, E* h16,
                                   const CUtensorMap* ta, const CUtensorMap* tb) {
   const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
   const bool gen = p.generic_acts != 0;
   switch (p.cell) {
     case 0:
-      if (gen) return plain ? step_tc_launch<0, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, true, false, MODE>(p, plan, s, q, h16, ta, tb);
-      return plain ? step_tc_launch<0, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, false, false, MODE>(p, plan, s, q, h16, ta, tb);
+      if (gen) return plain ? step_tc_launch<0, true, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, true, false, MODE, E>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<0, false, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<0, false, false, MODE, E>(p, plan, s, q, h16, ta, tb);
     case 1:
-      if (gen) return plain ? step_tc_launch<1, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, true, false, MODE>(p, plan, s, q, h16, ta, tb);
-      return plain ? step_tc_launch<1, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, false, false, MODE>(p, plan, s, q, h16, ta, tb);
+      if (gen) return plain ? step_tc_launch<1, true, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, true, false, MODE, E>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<1, false, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<1, false, false, MODE, E>(p, plan, s, q, h16, ta, tb);
     default:
-      if (gen) return plain ? step_tc_launch<2, true, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, true, false, MODE>(p, plan, s, q, h16, ta, tb);
-      return plain ? step_tc_launch<2, false, true, MODE>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, false, false, MODE>(p, plan, s, q, h16, ta, tb);
+      if (gen) return plain ? step_tc_launch<2, true, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, true, false, MODE, E>(p, plan, s, q, h16, ta, tb);
+      return plain ? step_tc_launch<2, false, true, MODE, E>(p, plan, s, q, h16, ta, tb) : step_tc_launch<2, false, false, MODE, E>(p, plan, s, q, h16, ta, tb);
   }
 }
 
 }  // namespace
 
-// One translation unit per MODE (they compile in parallel).
+// One translation unit per MODE and element type (they compile in parallel).
 cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
                          const CUtensorMap* ta, const CUtensorMap* tb);
 cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16,
                           const CUtensorMap* ta, const CUtensorMap* tb);
 cudaError_t step_tc_cluster(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __half* h16);
+cudaError_t step_tc_rows(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident,
+                         __nv_bfloat16* h16, const CUtensorMap* ta, const CUtensorMap* tb);
+cudaError_t step_tc_pairs(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident,
+                          __nv_bfloat16* h16, const CUtensorMap* ta, const CUtensorMap* tb);
+cudaError_t step_tc_cluster(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident,
+                            __nv_bfloat16* h16);
 
 }  // namespace rk

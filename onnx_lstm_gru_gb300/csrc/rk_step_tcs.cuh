@@ -1,0 +1,529 @@
+// rk_step_tcs.cuh -- tensor-core recurrent step for small batches (at most 16
+// rows per direction) of 16-bit layers (Half or bfloat16: the element type
+// E) whose hidden units fit one cluster.  Instantiated by rk_step_tcs.cu
+// (Half, and the entry point) and rk_step_tcs_bf16.cu (bfloat16).
+//
+// Same arithmetic as rk_step.cuh and rk_step_tc.cuh (web page "Recurrent
+// layers", sections "How a layer runs" and "Arithmetic and determinism"):
+// per step and gate row pre = ((xw + rec) + Wb) + Rb with rec = R_row .
+// h_prev (h rounded to E for the product, state float32), then
+// peepholes, clip, activation and state update (LSTM, RNN, GRU with
+// linear_before_reset 0 or 1).
+//
+// With a small batch the product is turned around: the MMA's M = 128 rows
+// are this CTA's gate rows (row g * 32 + u for gate g, unit u of its 32
+// units; rows past G * 32 are zero) held in shared memory for the whole
+// layer, and its N = 16 columns are the direction's batch rows, so the
+// exchanged operand is only 16 rows of h (2 KB per 64 k).  A team is one
+// direction, one cluster of ceil(H / 32) CTAs.  Per step:
+//   1. the producer warp waits until every CTA of the cluster has published
+//      h_s (remote mbarrier arrivals, cluster-scope release / acquire) and
+//      copies the direction's whole 16-bit h_s (H / 64 blocks of 16 rows x 64
+//      k, 128-byte swizzled, double-buffered in global memory) with one
+//      bulk copy;
+//   2. one lane issues the H / 16 MMAs (kind::f16, M = 128, N = 16, K = 16)
+//      into one fp32 TMEM accumulator (lane = gate row, column = batch row);
+//   3. warp g < G reads gate g's lanes (unit = lane) and stages them in
+//      shared memory; every gate thread then takes one (unit, batch row)
+//      pair (two when the batch exceeds 8), does the gate arithmetic, writes
+//      its 16-bit h into the next global buffer and Y, and the CTA publishes.
+// GRU with linear_before_reset = 0 runs two rounds per step: the first
+// product gives z and r, each thread writes its 16-bit r (.) h_prev to a second
+// global buffer and the cluster publishes it, the producer copies it in
+// place of h and the second product's candidate rows give R_h . (r (.) h).
+// The summation order is fixed (k in increasing 16-wide steps), so runs are
+// bit-identical.  Every wait is bounded; on expiry the kernel sets the
+// status word, drains its copy and MMAs, frees its TMEM and returns.
+#pragma once
+#include "rk_step_tc.cuh"
+
+namespace rk {
+
+namespace {
+
+constexpr int XN = 16;         // MMA N: a direction's batch rows, padded
+constexpr int XJ = 32;         // hidden units per CTA
+constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at most
+constexpr int XBLK_A = 128 * 128;  // bytes of one 64-k block of the gate rows
+constexpr int XBLK_B = XN * 128;   // bytes of one 64-k block of h
+
+// Shared memory: [gate rows: KB x 16 KB][h: KB x 2 KB][staged products
+// [4][32][16] floats][barriers][biases]
+struct XsSmem {
+  size_t r, h, acc, bar, bias, total;
+};
+__host__ __device__ inline XsSmem xs_layout(int G, int H) {
+  XsSmem L{};
+  const int KB = (H + SK - 1) / SK;
+  size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
+  L.r = o;    o += (size_t)KB * XBLK_A;
+  L.h = o;    o += (size_t)KB * XBLK_B;
+  L.acc = o;  o += (size_t)4 * XJ * XN * 4;
+  L.bar = o;  o += 256;
+  L.bias = o; o += (size_t)2 * 4 * XJ * 4 + 3 * XJ * 4;
+  L.total = o;
+  (void)G;
+  return L;
+}
+
+// Element offset of block kb of (buffer, direction) in the 16-bit copies:
+// [h or r (.) h][2 buffers][D][KB blocks][16 rows x 64 k, swizzled].
+__device__ __forceinline__ size_t xs_h_block(const StepParams& p, int which, int buf, int d, int kb, int KB) {
+  return ((((size_t)which * 2 + buf) * p.D + d) * KB + kb) * (size_t)(XBLK_B / 2);
+}
+
+template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
+__global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams p, E* __restrict__ h16) {
+  static_assert(!LBR0 || CELL == 1, "two rounds only for GRU with linear_before_reset = 0");
+  constexpr int NRND = LBR0 ? 2 : 1;  // products per step
+  constexpr int G = CellInfo<CELL>::G;
+  constexpr int A = CellInfo<CELL>::A;
+  constexpr uint32_t kTmemCols = 32;  // accumulator: 128 lanes x 16 columns
+  extern __shared__ unsigned char tsm_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
+  const XsSmem L = xs_layout(G, p.H);
+  unsigned char* sR = base + (L.r - 1024);
+  unsigned char* sH = base + (L.h - 1024);
+  float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));  // [g][u][b]
+  // full, drain, then per round: done, free, staged, gather, cluster publication[2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  float* wb_s = reinterpret_cast<float*>(base + (L.bias - 1024));  // [g * XJ + u]
+  float* rb_s = wb_s + 4 * XJ;
+  float* pp_s = rb_s + 4 * XJ;                                     // [u * 3 + g]
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H, N = p.N, S = p.S, Tn = p.T;
+  const int C = p.team_ctas;
+  const int d = blockIdx.x / C;  // one team (cluster) per direction
+  int rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int j0 = rank * XJ;
+  const int KB = (H + SK - 1) / SK;
+  const bool reverse = p.direction == 1 || (p.direction == 2 && d == 1);
+  const size_t GH = (size_t)G * H;
+  const E* R = static_cast<const E*>(p.R);
+  const E* Bias = static_cast<const E*>(p.Bias);
+  const E* P = static_cast<const E*>(p.P);
+  const E* h0 = static_cast<const E*>(p.h0);
+  const E* c0 = static_cast<const E*>(p.c0);
+  E* Y = static_cast<E*>(p.Y);
+
+  // ---------------- prologue: gate rows (row g * 32 + u), 16 bytes at a time
+  const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
+  for (int e = tid; e < KB * 128 * (SK / 8); e += blockDim.x) {
+    const int kb = e / (128 * (SK / 8));
+    const int rem = e % (128 * (SK / 8));
+    const int r = rem / (SK / 8), kk = (rem % (SK / 8)) * 8;
+    const int g = r / XJ, u = r % XJ, k = kb * SK + kk;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (g < G && j0 + u < H && k < H) {
+      const E* src = R + ((size_t)d * GH + (size_t)g * H + j0 + u) * H + k;
+      if (r_vec) {
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        __align__(16) E t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] = src[i];
+        v = *reinterpret_cast<const uint4*>(t8);
+      }
+    }
+    *reinterpret_cast<uint4*>(sR + (size_t)kb * XBLK_A + sw128_offset(r, kk)) = v;
+  }
+  for (int e = tid; e < G * XJ; e += blockDim.x) {
+    const int g = e / XJ, u = e % XJ;
+    const bool ok = j0 + u < H && Bias != nullptr;
+    wb_s[e] = ok ? Elem<E>::to_f(Bias[(size_t)d * 2 * GH + (size_t)g * H + j0 + u]) : 0.0f;
+    rb_s[e] = ok ? Elem<E>::to_f(Bias[(size_t)d * 2 * GH + GH + (size_t)g * H + j0 + u]) : 0.0f;
+  }
+  for (int e = tid; e < 3 * XJ; e += blockDim.x) {
+    const int u = e / 3, g = e % 3;
+    pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? Elem<E>::to_f(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);  // operand copy landed (one per round)
+    mbar_init(smem_u32(&bars[1]), 1);  // final MMA drain
+    for (int rd = 0; rd < 2; ++rd) {
+      uint64_t* b6 = bars + 2 + 6 * rd;
+      mbar_init(smem_u32(&b6[0]), 1);            // accumulator complete (MMA commit)
+      mbar_init(smem_u32(&b6[1]), 8);            // accumulator read (8 gate warps)
+      mbar_init(smem_u32(&b6[2]), 8);            // products staged (8 gate warps)
+      mbar_init(smem_u32(&b6[3]), 8);            // 16-bit copies written (8 gate warps)
+      mbar_init(smem_u32(&b6[4]), (unsigned)C);  // every CTA published, step even
+      mbar_init(smem_u32(&b6[5]), (unsigned)C);  // ... step odd
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // the gate rows were written by ordinary stores; the tensor cores read them
+  // through the async proxy
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // gate threads: pair i = tid + 256 k is (unit i % 32, batch row i / 32)
+  const bool gate_warp = warp < 8;
+  float hreg[XPAIRS], creg[XPAIRS];
+  int lenv[XPAIRS];
+  bool pv[XPAIRS];
+  const int pu = tid & 31;  // the unit is the same for both pairs
+  const int pj = j0 + pu;
+#pragma unroll
+  for (int k = 0; k < XPAIRS; ++k) {
+    const int b = (tid + 256 * k) >> 5;
+    pv[k] = gate_warp && b < N;
+    hreg[k] = creg[k] = 0.0f;
+    lenv[k] = Tn;
+  }
+  // address of (buffer, batch row b, unit j) in the 16-bit h copy
+  auto h16_at = [&](int which, int buf, int b, int j) {
+    return reinterpret_cast<E*>(reinterpret_cast<unsigned char*>(h16 + xs_h_block(p, which, buf, d, j / SK, KB)) +
+                                     sw128_offset(b, j % SK));
+  };
+#pragma unroll
+  for (int k = 0; k < XPAIRS; ++k) {
+    if (!pv[k]) continue;
+    const int b = (tid + 256 * k) >> 5;
+    if (p.lens != nullptr) {
+      int len = p.lens[b];
+      len = len < 0 ? 0 : (len > S ? S : len);
+      lenv[k] = len > Tn ? Tn : len;
+    }
+    if (pj < H) {
+      const size_t si = state_index(p, d, b, pj);
+      hreg[k] = h0 != nullptr ? Elem<E>::to_f(h0[si]) : 0.0f;
+      creg[k] = (CELL == 0 && c0 != nullptr) ? Elem<E>::to_f(c0[si]) : 0.0f;
+    }
+    *h16_at(0, 0, b, pj) = Elem<E>::from_f(pj < H ? hreg[k] : 0.0f);  // h_0 into buffer 0
+  }
+  // k columns past the last CTA's units (up to the 64-wide block) belong to
+  // no CTA: zero them once in both buffers for every row (R is zero there
+  // too, but a stale Inf or NaN times zero would not be)
+  if (rank == C - 1) {
+    const int pad = KB * SK - C * XJ;
+    for (int e = tid; e < pad * XN * 2 * NRND; e += blockDim.x) {
+      const int k = C * XJ + e % pad, b = (e / pad) % XN, buf = (e / (pad * XN)) % 2, which = e / (pad * XN * 2);
+      *h16_at(which, buf, b, k) = Elem<E>::from_f(0.0f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // every CTA's barriers are initialised before any remote arrival (all CTAs
+  // of a cluster run at once and reach this point)
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  const uint32_t tmem_acc = *tmem_slot;
+
+  const uint32_t bar_full = su32(&bars[0]), bar_drain = su32(&bars[1]);
+  // round rd's barriers: done, free, staged, gather, cluster publication[2]
+  auto rbar = [&](int rd, int i) { return su32(&bars[2 + 6 * rd + i]); };
+  // gate warps: make this CTA's new h copies visible to the async proxy,
+  // gather the 8 warps, then lane q of warp 0 arrives on CTA q's
+  // publication barrier for h_s (one barrier per step parity: a CTA's
+  // arrivals for h_{s+2} come after it saw every arrival for h_{s+1}, each
+  // made after its sender's arrivals for h_s)
+  // round 0 publishes h_s (value = s + 1), round 1 r (.) h of step s
+  // (value = s + 1 too); a round's gather barrier completes once per value
+  auto publish = [&](int rd, unsigned value) {
+    const uint32_t bar_pub = rbar(rd, 3), bar_pubc = rbar(rd, 4);
+    const uint32_t pub_parity = (value - 1u) & 1u;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_pub) : "memory");
+    if (warp == 0 && lane < C) {
+      if (bar_wait(bar_pub, pub_parity, p.timeout_ns)) {
+        const uint32_t local = bar_pubc + 8u * ((value - 1u) & 1u);  // step value - 1
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(local, (uint32_t)lane))
+                     : "memory");
+      } else {
+        abort_flag = 1;
+        atomicOr(p.status, 1);
+      }
+    }
+  };
+  if (gate_warp) publish(0, 1u);
+
+  const size_t xw_tstride = p.layout == 0 ? (size_t)N * GH : GH;
+  const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
+  const float clip = PLAIN ? 0.0f : p.clip;
+  const bool input_forget = !PLAIN && p.input_forget;
+
+  if (warp == 8) {
+    // ---------------- producer lane: each round's whole operand (h_s, or
+    // r (.) h_s) in one bulk copy, once every CTA of the cluster published it
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)KB * XBLK_B;
+      int armed = -1;
+      bool ok = true;
+      for (int s = 0; s < Tn && ok; ++s) {
+        for (int rd = 0; rd < NRND; ++rd) {
+          if (abort_flag ||
+              !bar_wait_cluster(rbar(rd, 4) + 8u * (uint32_t)(s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          // the publishers' generic-proxy stores, acquired above, are read by the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          bar_expect(bar_full, bytes);
+          bulk_load(su32(sH), h16 + xs_h_block(p, rd, s & 1, d, 0, KB), bytes, bar_full);
+          armed = (s * NRND + rd) & 1;
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        atomicOr(p.status, 1);
+      }
+      // drain: the copy this CTA issued last must land before it exits
+      if (armed >= 0) bar_wait(bar_full, (uint32_t)armed, p.timeout_ns);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA lane: acc_rd[128 gate rows x 16 batch] = R_rows . operand^T
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(XN) | Elem<E>::kMmaAB;
+      const uint64_t adesc0 = desc_sw128(su32(sR));
+      const uint64_t bdesc0 = desc_sw128(su32(sH));
+      constexpr uint64_t kK16 = 32 >> 4;
+      bool ok = true;
+      for (int s = 0; s < Tn && ok; ++s) {
+        for (int rd = 0; rd < NRND; ++rd) {
+          if (abort_flag || !bar_wait(bar_full, (uint32_t)((s * NRND + rd) & 1), p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          // the gate warps must have read this accumulator of the previous step
+          if (s > 0 && !bar_wait(rbar(rd, 1), (uint32_t)((s - 1) & 1), p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
+          uint64_t ad = adesc0, bd = bdesc0;
+          for (int kb = 0; kb < KB; ++kb, ad += XBLK_A >> 4, bd += XBLK_B >> 4) {
+            tc_mma(tacc, ad, bd, idesc, kb != 0 ? 1u : 0u);
+            tc_mma(tacc, ad + kK16, bd + kK16, idesc, 1u);
+            tc_mma(tacc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
+            tc_mma(tacc, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
+          }
+          tc_commit(rbar(rd, 0));  // accumulator rd of step s complete
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        atomicOr(p.status, 1);
+      }
+      // drain: every MMA this CTA issued completes before TMEM is freed
+      tc_commit(bar_drain);
+      bar_wait(bar_drain, 0u, p.timeout_ns);
+    }
+  } else {
+    // ---------------- gate warps
+    float xv[XPAIRS][G];
+    auto load_xw = [&](int s) {
+#pragma unroll
+      for (int k = 0; k < XPAIRS; ++k) {
+        const int b = (tid + 256 * k) >> 5;
+        const bool on = pv[k] && s < lenv[k] && s < Tn && pj < H;
+        const float* qx = p.xw + xw_index(p, d, 0, on ? b : 0, 0, on ? pj : 0) +
+                          (size_t)(on ? (reverse ? lenv[k] - 1 - s : s) : 0) * xw_tstride;
+#pragma unroll
+        for (int g = 0; g < G; ++g) xv[k][g] = on ? __ldg(qx + (size_t)g * H) : 0.0f;
+      }
+    };
+    // wait for accumulator rd of step s, stage gates [g0, g1) of it (warp g
+    // holds gate g of the 32 units, lane = unit) and make them visible to
+    // every gate warp
+    auto stage = [&](int rd, int s, int g0, int g1) -> bool {
+      if (abort_flag || !bar_wait(rbar(rd, 0), (uint32_t)(s & 1), p.timeout_ns)) return false;
+      tc_fence_after();
+      if (warp >= g0 && warp < g1) {
+        uint32_t v[XN];
+        tmem_ld<XN>(tmem_acc + ((uint32_t)(warp * 32) << 16) + (uint32_t)(rd * XN), v);
+        float4* dst = reinterpret_cast<float4*>(sAcc + ((size_t)warp * XJ + lane) * XN);
+#pragma unroll
+        for (int i = 0; i < XN / 4; ++i)
+          dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                               __uint_as_float(v[4 * i + 3]));
+      }
+      // the accumulator may be overwritten by the next step's product
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(rbar(rd, 1)) : "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(rbar(rd, 2)) : "memory");
+      }
+      return bar_wait(rbar(rd, 2), (uint32_t)(s & 1), p.timeout_ns);
+    };
+    float zr[XPAIRS][2];  // GRU linear_before_reset = 0: z and r between the rounds
+    load_xw(0);
+    bool ok = true;
+    for (int s = 0; s < Tn; ++s) {
+      if constexpr (LBR0) {
+        // round 0: z and r; publish r (.) h_prev
+        if (!stage(0, s, 0, 2)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < XPAIRS; ++k) {
+          if (!pv[k]) continue;
+          const int b = (tid + 256 * k) >> 5;
+          float pre[2];
+#pragma unroll
+          for (int g = 0; g < 2; ++g)
+            pre[g] = ((xv[k][g] + sAcc[((size_t)g * XJ + pu) * XN + b]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
+          zr[k][0] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
+          zr[k][1] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
+          *h16_at(1, s & 1, b, pj) = Elem<E>::from_f(pj < H ? zr[k][1] * hreg[k] : 0.0f);
+        }
+        publish(1, (unsigned)s + 1u);
+      }
+      // the last (or only) round: the remaining gate arithmetic
+      constexpr int RL = NRND - 1;
+      if (!stage(RL, s, LBR0 ? 2 : 0, G)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int k = 0; k < XPAIRS; ++k) {
+        if (!pv[k]) continue;
+        const int b = (tid + 256 * k) >> 5;
+        const bool active = s < lenv[k];
+        const int t = active ? (reverse ? lenv[k] - 1 - s : s) : s;
+        float rec[G], pre[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          rec[g] = (LBR0 && g < 2) ? 0.0f : sAcc[((size_t)g * XJ + pu) * XN + b];
+          pre[g] = ((xv[k][g] + rec[g]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
+        }
+        float hn = hreg[k];
+        if constexpr (CELL == 0) {
+          // gates i, o, f, c
+          float pi = pre[0], po = pre[1], pf = pre[2], pc = pre[3];
+          if (has_p) {
+            pi = pi + pp_s[pu * 3 + 0] * creg[k];
+            pf = pf + pp_s[pu * 3 + 2] * creg[k];
+          }
+          const float ig = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pi));
+          const float fg = input_forget ? 1.0f - ig : act<GEN, 0>(p, d * A + 0, clip_pre(clip, pf));
+          const float cg = act<GEN, 1>(p, d * A + 1, clip_pre(clip, pc));
+          const float cn = fg * creg[k] + ig * cg;
+          if (has_p) po = po + pp_s[pu * 3 + 1] * cn;
+          const float og = act<GEN, 0>(p, d * A + 0, clip_pre(clip, po));
+          if (active) {
+            hn = og * act<GEN, 1>(p, d * A + 2, cn);
+            creg[k] = cn;
+          }
+        } else if constexpr (CELL == 1) {
+          float z, hc;
+          if constexpr (LBR0) {
+            // h~ = g(((xw_h + R_h . (r (.) h_prev)) + Wb_h) + Rb_h)
+            z = zr[k][0];
+            hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, pre[2]));
+          } else {
+            // linear_before_reset = 1: h~ = g((xw_h + r*(rec_h + Rb_h)) + Wb_h)
+            z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
+            const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
+            const float ph = (xv[k][2] + r * (rec[2] + rb_s[2 * XJ + pu])) + wb_s[2 * XJ + pu];
+            hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, ph));
+          }
+          if (active) hn = (1.0f - z) * hc + z * hreg[k];
+        } else {
+          if (active) hn = act<GEN, 1>(p, d * A + 0, clip_pre(clip, pre[0]));
+        }
+        if (pj < H) hreg[k] = hn;
+        if (s + 1 < Tn) *h16_at(0, (s + 1) & 1, b, pj) = Elem<E>::from_f(pj < H ? hn : 0.0f);
+        if (Y != nullptr && pj < H) Y[y_index(p, t, d, b, pj)] = Elem<E>::from_f(active ? hn : 0.0f);
+      }
+      if (s + 1 < Tn) publish(0, (unsigned)s + 2u);
+      load_xw(s + 1);
+    }
+    if (!ok) {
+      abort_flag = 1;
+      atomicOr(p.status, 1);
+    }
+    // ---------------- outputs: zero Y past the loop, final states
+    if (ok && !abort_flag && pj < H) {
+#pragma unroll
+      for (int k = 0; k < XPAIRS; ++k) {
+        if (!pv[k]) continue;
+        const int b = (tid + 256 * k) >> 5;
+        if (Y != nullptr)
+          for (int t = Tn; t < S; ++t) Y[y_index(p, t, d, b, pj)] = Elem<E>::from_f(0.0f);
+        const bool zero = S > 0 && lenv[k] == 0;
+        const size_t si = state_index(p, d, b, pj);
+        if (p.Yh != nullptr) static_cast<E*>(p.Yh)[si] = Elem<E>::from_f(zero ? 0.0f : hreg[k]);
+        if (CELL == 0 && p.Yc != nullptr) static_cast<E*>(p.Yc)[si] = Elem<E>::from_f(zero ? 0.0f : creg[k]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_acc), "r"(kTmemCols) : "memory");
+  }
+  // no CTA leaves while a peer may still arrive on its barriers
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
+cudaError_t step_tcs_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, E* h16) {
+  auto kern = step_tcs_kernel<CELL, GEN, PLAIN, LBR0, E>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  if (e != cudaSuccess) return e;
+  if (plan.team_ctas > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.grid, 1, 1);
+  cfg.blockDim = dim3(STHREADS, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  // a team (direction) is one cluster; teams never wait on each other
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)plan.team_ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (resident != nullptr) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    *resident = (e == cudaSuccess) ? n : 0;
+    return e;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, p, h16);
+}
+
+template <int CELL, bool LBR0, typename E>
+cudaError_t step_tcs_cell(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, E* h16) {
+  const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
+  if (p.generic_acts)
+    return plain ? step_tcs_launch<CELL, true, true, LBR0, E>(p, plan, s, q, h16)
+                 : step_tcs_launch<CELL, true, false, LBR0, E>(p, plan, s, q, h16);
+  return plain ? step_tcs_launch<CELL, false, true, LBR0, E>(p, plan, s, q, h16)
+               : step_tcs_launch<CELL, false, false, LBR0, E>(p, plan, s, q, h16);
+}
+
+template <typename E>
+cudaError_t step_tcs_cells(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, E* hp) {
+  switch (p.cell) {
+    case 0: return step_tcs_cell<0, false>(p, plan, s, resident, hp);
+    case 1: return p.lbr ? step_tcs_cell<1, false>(p, plan, s, resident, hp) : step_tcs_cell<1, true>(p, plan, s, resident, hp);
+    default: return step_tcs_cell<2, false>(p, plan, s, resident, hp);
+  }
+}
+
+}  // namespace
+
+// bfloat16 layers (rk_step_tcs_bf16.cu)
+cudaError_t step_tcs_bf16(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __nv_bfloat16* h16);
+
+}  // namespace rk

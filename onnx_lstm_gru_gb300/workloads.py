@@ -4,7 +4,10 @@ This module only describes layers and draws random arrays; it holds none of
 the layer's arithmetic.  Inputs are drawn with numpy's PCG64
 (``numpy.random.default_rng(seed)``) in float64, in the order X, W, R, B, P,
 initial_h, initial_c, sequence_lens (each only when the workload has it), and
-then cast to the tensor dtype (float16 by round-to-nearest-even).  "N(0, s)"
+then cast to the tensor dtype: float32 and float16 by numpy's
+round-to-nearest-even; bfloat16 (which numpy lacks) by rounding to float32
+first and then to the 8-bit significand, nearest-even on the float32 bits,
+the result kept as float32 arrays whose values are all bfloat16 numbers.  "N(0, s)"
 means standard deviation s.  The same arrays feed the CUDA library and the
 oracle.
 
@@ -85,6 +88,17 @@ WORKLOADS = {
         Problem("lstm", seq=48, batch=8, input=192, hidden=96, direction="bidirectional", dtype="f32", layout=0),
         seed=5, x=("normal", 1.0), weights=("uniform", 0.1), init_h=("normal", 0.1), init_c=("normal", 0.1),
         lens="uniform"),
+    # bfloat16 variants of the largest layer and of the recognizer's shape
+    "bilstm_s512_b64_i1024_h1024_bf16": Workload(
+        "bilstm_s512_b64_i1024_h1024_bf16",
+        Problem("lstm", seq=512, batch=64, input=1024, hidden=1024, direction="bidirectional", dtype="bf16",
+                layout=0),
+        seed=7, x=("normal", 1.0), weights=("uniform", 0.03), lens="full"),
+    "bilstm_s48_b8_i192_h96_bf16": Workload(
+        "bilstm_s48_b8_i192_h96_bf16",
+        Problem("lstm", seq=48, batch=8, input=192, hidden=96, direction="bidirectional", dtype="bf16", layout=0),
+        seed=8, x=("normal", 1.0), weights=("uniform", 0.1), init_h=("normal", 0.1), init_c=("normal", 0.1),
+        lens="uniform"),
     "bilstm_s48_b8_i192_h96_f16": Workload(
         "bilstm_s48_b8_i192_h96_f16",
         Problem("lstm", seq=48, batch=8, input=192, hidden=96, direction="bidirectional", dtype="f16", layout=0),
@@ -96,24 +110,41 @@ WORKLOADS = {
 HEADLINE = "bilstm_s80_b1_i256_h256_f32"
 
 
+def round_bf16(a) -> np.ndarray:
+    """float32 array of the bfloat16 numbers nearest (ties to even) to the
+    float32 rounding of ``a`` (finite values)."""
+    u = np.ascontiguousarray(np.asarray(a, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def cast(a, dtype: str) -> np.ndarray:
+    """Values in the tensor dtype: float32, float16, or float32 holding bfloat16 numbers."""
+    if dtype in ("f32", "float32"):
+        return np.asarray(a).astype(np.float32)
+    if dtype in ("bf16", "bfloat16"):
+        return round_bf16(a)
+    return np.asarray(a).astype(np.float16)
+
+
 def make_inputs(w: Workload, problem: Optional[Problem] = None) -> dict:
-    """Draw the workload's inputs (numpy arrays in the tensor dtype; lengths
-    int32).  ``problem`` may override sizes for scaled-down variants."""
+    """Draw the workload's inputs (numpy arrays in the tensor dtype, see
+    ``cast``; lengths int32).  ``problem`` may override sizes for scaled-down
+    variants."""
     pr = problem or w.problem
     rng = np.random.default_rng(w.seed)
     shp = pr.shapes()
-    dt = np.float32 if pr.dtype in ("f32", "float32") else np.float16
     out = {}
-    out["X"] = _draw(rng, w.x, shp["X"]).astype(dt)
-    out["W"] = _draw(rng, w.weights, shp["W"]).astype(dt)
-    out["R"] = _draw(rng, w.weights, shp["R"]).astype(dt)
-    out["B"] = _draw(rng, w.weights, shp["B"]).astype(dt)
+    out["X"] = cast(_draw(rng, w.x, shp["X"]), pr.dtype)
+    out["W"] = cast(_draw(rng, w.weights, shp["W"]), pr.dtype)
+    out["R"] = cast(_draw(rng, w.weights, shp["R"]), pr.dtype)
+    out["B"] = cast(_draw(rng, w.weights, shp["B"]), pr.dtype)
     if w.p is not None and pr.cell == "lstm":
-        out["P"] = _draw(rng, w.p, shp["P"]).astype(dt)
+        out["P"] = cast(_draw(rng, w.p, shp["P"]), pr.dtype)
     if w.init_h is not None:
-        out["initial_h"] = _draw(rng, w.init_h, shp["initial_h"]).astype(dt)
+        out["initial_h"] = cast(_draw(rng, w.init_h, shp["initial_h"]), pr.dtype)
     if w.init_c is not None and pr.cell == "lstm":
-        out["initial_c"] = _draw(rng, w.init_c, shp["initial_c"]).astype(dt)
+        out["initial_c"] = cast(_draw(rng, w.init_c, shp["initial_c"]), pr.dtype)
     if w.lens == "full":
         out["sequence_lens"] = np.full((pr.batch,), pr.seq, dtype=np.int32)
     elif w.lens == "uniform":

@@ -119,7 +119,7 @@ def test_options_illegal_for_cell(handle):
     c.act[0].kind = 11
     st = rk.rk_validate(handle, c, Host(p).ops())
     assert st == rk.RK_ERR_SHAPE and "unknown kind 11" in rk.rk_last_error(handle)
-    for bad in [dict(layout=2), dict(seq=-1), dict(max_length=5)]:
+    for bad in [dict(layout=2), dict(seq=-1), dict(max_length=5), dict(dtype=3), dict(dtype=-1)]:
         q = rk.Problem("lstm", 2, 1, 2, 4)
         cq = q.to_c()
         for k, v in bad.items():
@@ -183,6 +183,10 @@ def test_plans_without_device(handle):
     # the projection runs on the SMs the 128 recurrence CTAs leave idle
     assert "proj=fused step=tensor" in plans["bilstm_s512_b64_i1024_h1024_f16"]
     assert "step=tensor" in plans["bigru_s128_b8_i512_h512_f16_lbr1"]
+    # bfloat16 layers take the same kernels as Half ones
+    assert plans["bilstm_s512_b64_i1024_h1024_bf16"] == plans["bilstm_s512_b64_i1024_h1024_f16"]
+    assert plans["bilstm_s48_b8_i192_h96_bf16"] == plans["bilstm_s48_b8_i192_h96_f16"]
+    assert "step=tensor" in plans["bilstm_s48_b8_i192_h96_bf16"] and "J=32" in plans["bilstm_s48_b8_i192_h96_bf16"]
     for name, text in plans.items():
         smem = int(re.search(r"smem=(\d+)", text).group(1))
         assert smem <= 232448 - 1024, (name, text)
@@ -201,6 +205,27 @@ def test_plans_without_device(handle):
             assert want in rk.rk_describe_plan(h2, c2), flags
         finally:
             rk.rk_destroy(h2)
+
+
+def test_bfloat16_inputs_round_like_torch():
+    """The generator's bfloat16 rounding (float32 first, then nearest-even on
+    the float32 bits) gives torch's own float32 -> bfloat16 conversion, ties
+    included, and every bfloat16 workload input is a bfloat16 number."""
+    import torch
+    rng = np.random.default_rng(11)
+    a = rng.normal(size=20000) * np.exp(rng.uniform(-30, 30, 20000))
+    # exact ties between two bfloat16 neighbours, both parities, and signed zeros
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3 * 2.0 ** -9 + 1, 0.0, -0.0, 1e30, -1e-30])
+    for v in (a, ties):
+        want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).float().numpy()
+        got = workloads.round_bf16(v)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert workloads.round_bf16([1 + 2.0 ** -8])[0] == 1.0           # tie to even (down)
+    assert workloads.round_bf16([1 + 3 * 2.0 ** -8])[0] == 1 + 2.0 ** -6  # tie to even (up)
+    for name in ("bilstm_s48_b8_i192_h96_bf16",):
+        for k, v in workloads.make_inputs(workloads.WORKLOADS[name]).items():
+            if k != "sequence_lens":
+                assert v.dtype == np.float32 and np.all((v.view(np.uint32) & 0xFFFF) == 0), k
 
 
 def test_workload_inputs_are_seeded_and_shaped():

@@ -3,7 +3,11 @@
 Every case compares Y, Y_h and Y_c element by element on the same seeded
 inputs: |gpu - oracle| <= tol or <= tol * |oracle| with tol 1e-4 for float32
 and 5e-3 for Half tensors (float32 accumulation and state, outputs rounded to
-half).  Positions past a row's length must be exactly 0, bytes around every
+half).  bfloat16 tensors get 2e-2: the Half tolerance times the ratio of the
+two types' unit roundoffs (2^-9 / 2^-11 = 4), since the two errors that
+matter scale with it -- the rounding of every output, and on the tensor
+cores the rounding of h before the recurrent product (the Gemm page's own
+bounds grow by the same factor, 2e-3 to 8e-3).  Positions past a row's length must be exactly 0, bytes around every
 output (sentinels) must be untouched, and two runs must give the same bits.
 
 The test matrix follows the one the recurrent-layers page lists: every cell x
@@ -25,8 +29,8 @@ from onnx_lstm_gru_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 1e-4, "f16": 5e-3}
-SENTINEL = -777.0  # exactly representable in float32 and in binary16
+TOL = {"f32": 1e-4, "f16": 5e-3, "bf16": 2e-2}
+SENTINEL = -776.0  # exactly representable in float32, binary16 and bfloat16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,7 +52,7 @@ def layer(flags=0):
 
 
 def torch_dtype(pr):
-    return torch.float32 if pr.dtype == "f32" else torch.float16
+    return rk.torch_dtype(pr.dtype)
 
 
 def to_device(arr, offset, dtype):
@@ -137,18 +141,26 @@ def compare(pr, got, ref, lens=None):
 def rand_inputs(pr, seed, lens=None, init=True, peep=False, bias=True, scale=0.5):
     rng = np.random.default_rng(seed)
     shp = pr.shapes()
-    dt = np.float32 if pr.dtype == "f32" else np.float16
-    a = {"X": rng.uniform(-1, 1, shp["X"]).astype(dt),
-         "W": rng.uniform(-scale, scale, shp["W"]).astype(dt),
-         "R": rng.uniform(-scale, scale, shp["R"]).astype(dt)}
+    def dt(v):
+        return workloads.cast(v, pr.dtype)
+    # bfloat16 keeps 8 significant bits, and the tensor-core steps round h to
+    # it before every recurrent product, so that error grows by the
+    # recurrence's gain each step.  Uniform R of scale a has gain about
+    # a * sqrt(H / 3); above 1 (large H at the default scales) the layer is
+    # chaotic and no fixed tolerance holds, so bfloat16 cases cap R's scale
+    # at sqrt(3 / H) (gain at most 1).
+    rscale = min(scale, float(np.sqrt(3.0 / max(pr.hidden, 1)))) if pr.dtype == "bf16" else scale
+    a = {"X": dt(rng.uniform(-1, 1, shp["X"])),
+         "W": dt(rng.uniform(-scale, scale, shp["W"])),
+         "R": dt(rng.uniform(-rscale, rscale, shp["R"]))}
     if bias:
-        a["B"] = rng.uniform(-scale, scale, shp["B"]).astype(dt)
+        a["B"] = dt(rng.uniform(-scale, scale, shp["B"]))
     if peep and pr.cell == "lstm":
-        a["P"] = rng.uniform(-scale, scale, shp["P"]).astype(dt)
+        a["P"] = dt(rng.uniform(-scale, scale, shp["P"]))
     if init:
-        a["initial_h"] = rng.uniform(-1, 1, shp["initial_h"]).astype(dt)
+        a["initial_h"] = dt(rng.uniform(-1, 1, shp["initial_h"]))
         if pr.cell == "lstm":
-            a["initial_c"] = rng.uniform(-1, 1, shp["initial_c"]).astype(dt)
+            a["initial_c"] = dt(rng.uniform(-1, 1, shp["initial_c"]))
     if lens is not None:
         a["sequence_lens"] = np.asarray(lens, dtype=np.int32)
     return a
@@ -156,7 +168,10 @@ def rand_inputs(pr, seed, lens=None, init=True, peep=False, bias=True, scale=0.5
 
 # ------------------------------------------------------------------ the named workloads
 
-@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if n != "bilstm_s512_b64_i1024_h1024_f16"])
+LARGE = ["bilstm_s512_b64_i1024_h1024_f16", "bilstm_s512_b64_i1024_h1024_bf16"]
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.WORKLOADS if n not in LARGE])
 def test_workload_full_size(name):
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w)
@@ -169,10 +184,12 @@ def test_workload_full_size(name):
             assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
 
 
-def test_large_half_workload_sampled_rows():
-    """bi-LSTM 512 x 64 x 1024 x 1024 Half, run whole on the GPU; batch rows
-    0, 29 and 63 re-run through the oracle alone (rows are independent)."""
-    w = workloads.WORKLOADS["bilstm_s512_b64_i1024_h1024_f16"]
+@pytest.mark.parametrize("name", LARGE)
+def test_large_workload_sampled_rows(name):
+    """bi-LSTM 512 x 64 x 1024 x 1024 (Half, bfloat16), run whole on the GPU;
+    batch rows 0, 29 and 63 re-run through the oracle alone (rows are
+    independent)."""
+    w = workloads.WORKLOADS[name]
     pr = w.problem
     inp = workloads.make_inputs(w)
     got = run_gpu(pr, inp)
@@ -222,6 +239,27 @@ def test_option_matrix(cell, direction, layout, opts, kernel):
         compare(pr, got, ref, lens)
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("cell,direction", [(c, d) for c in ("lstm", "gru", "rnn")
+                                            for d in ("forward", "reverse", "bidirectional")])
+def test_bfloat16_option_matrix(cell, direction, kernel):
+    """bfloat16 tensors on the SIMT step kernels (bfloat16 R in registers or
+    shared memory, widened exactly; float32 products and state): every cell
+    and direction with lengths, initial state, peepholes, clip and
+    input_forget, both layouts."""
+    for layout in (0, 1):
+        kw = dict(clip=0.9)
+        if cell == "lstm":
+            kw["input_forget"] = 1
+        pr = rk.Problem(cell, seq=7, batch=3, input=5, hidden=40, direction=direction, layout=layout, dtype="bf16",
+                        **kw)
+        lens = [7, 0, 4]
+        for lbr in ((0, 1) if cell == "gru" else (0,)):
+            pr.linear_before_reset = lbr
+            inp = rand_inputs(pr, seed=200 + len(cell) + layout, lens=lens, peep=True)
+            compare(pr, run_gpu(pr, inp, flags=KERNELS[kernel] | rk.RK_FORCE_SIMT_STEP), run_oracle(pr, inp), lens)
+
+
 ALL_ACTS = [("sigmoid", 0, 0), ("tanh", 0, 0), ("relu", 0, 0), ("affine", 0.7, -0.2), ("leakyrelu", 0.15, 0),
             ("thresholdedrelu", 0.3, 0), ("scaledtanh", 1.3, 0.6), ("hardsigmoid", 0.25, 0.45), ("elu", 0.8, 0),
             ("softsign", 0, 0), ("softplus", 0, 0)]
@@ -243,7 +281,7 @@ def test_every_activation_in_every_slot(cell, act):
         compare(pr, got, run_oracle(pr, inp), [5, 3])
 
 
-@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_odd_offsets_and_sentinels(dtype):
     pr = rk.Problem("lstm", seq=6, batch=3, input=7, hidden=36, direction="bidirectional", dtype=dtype, layout=1)
     inp = rand_inputs(pr, seed=3, lens=[6, 2, 5], peep=True)
@@ -274,7 +312,7 @@ def test_ragged_hidden_and_large_batch(H, N, kernel):
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
-@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_kernels_agree_on_lstm_with_every_option(kernel, dtype):
     pr = rk.Problem("lstm", seq=9, batch=2, input=70, hidden=96, direction="bidirectional", dtype=dtype, layout=1,
                     clip=2.5, input_forget=1,
@@ -301,10 +339,10 @@ def test_getting_started_rows_exact():
     """RNN with Affine(1, 0), R = 0: Y is the projection, the pages' example rows."""
     A = np.arange(1, 9, dtype=np.float32).reshape(4, 1, 2)
     Bm = np.array([[1, 0, 2], [0, 1, 3]], dtype=np.float32)
-    for dtype in ("f32", "f16"):
+    for dtype in ("f32", "f16", "bf16"):  # small integers: exact in all three types
         pr = rk.Problem("rnn", seq=4, batch=1, input=2, hidden=3, activations=[("affine", 1.0, 0.0)], dtype=dtype)
-        dt = np.float32 if dtype == "f32" else np.float16
-        inp = {"X": A.astype(dt), "W": Bm.T.copy()[None].astype(dt), "R": np.zeros((1, 3, 3), dt)}
+        inp = {"X": workloads.cast(A, dtype), "W": workloads.cast(Bm.T.copy()[None], dtype),
+               "R": workloads.cast(np.zeros((1, 3, 3)), dtype)}
         got = run_gpu(pr, inp, outputs=("Y",))
         np.testing.assert_array_equal(got["Y"].reshape(4, 3), [[1, 2, 8], [3, 4, 18], [5, 6, 28], [7, 8, 38]])
 
@@ -337,12 +375,13 @@ def test_caller_scratch_in_one_arena_is_bitwise_equal():
         assert torch.equal(base[k], got[k])
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("cell", ["lstm", "gru", "rnn"])
-def test_tensor_core_step_with_odd_offsets(cell):
+def test_tensor_core_step_with_odd_offsets(cell, dtype):
     """Operands at odd element offsets (R not 16-byte aligned: element loads
     of the R slice; Y pieces stored element-wise) give the oracle's result
     and leave the sentinels around the outputs untouched."""
-    pr = rk.Problem(cell, seq=5, batch=6, input=24, hidden=72, direction="bidirectional", dtype="f16",
+    pr = rk.Problem(cell, seq=5, batch=6, input=24, hidden=72, direction="bidirectional", dtype=dtype,
                     linear_before_reset=1 if cell == "gru" else 0)
     assert "step=tensor" in layer().plan(pr)
     inp = rand_inputs(pr, seed=77, scale=0.15)
@@ -355,16 +394,17 @@ def test_tensor_core_step_with_odd_offsets(cell):
             assert torch.equal(got[k], aligned[k]), k
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("cell,H,N,direction", [("lstm", 576, 16, "bidirectional"),
                                                 ("gru", 640, 40, "reverse"),
                                                 ("rnn", 1024, 70, "forward")])
-def test_fused_projection_matches_separate(cell, H, N, direction):
+def test_fused_projection_matches_separate(cell, H, N, direction, dtype):
     """With flag-published tensor-core teams the projection runs on the SMs
     the recurrence leaves idle, its tiles produced in the order the steps
     consume them and each step waiting for its rows' tile.  The same tile
     arithmetic as the projection's own launch: bit-identical outputs, and the
-    oracle's within the Half tolerance."""
-    pr = rk.Problem(cell, seq=6, batch=N, input=72, hidden=H, direction=direction, dtype="f16",
+    oracle's within the tolerance of the element type."""
+    pr = rk.Problem(cell, seq=6, batch=N, input=72, hidden=H, direction=direction, dtype=dtype,
                     linear_before_reset=1 if cell == "gru" else 0)
     assert "proj=fused step=tensor" in layer().plan(pr)
     assert "proj=tc step=tensor" in layer(rk.RK_SEPARATE_PROJECTION).plan(pr)
@@ -382,16 +422,17 @@ def test_fused_projection_matches_separate(cell, H, N, direction):
                                                      (96, 9, "reverse", 1, "full"),
                                                      (200, 16, "forward", 0, "full"),
                                                      (512, 8, "bidirectional", 1, "plain")])
-def test_tensor_core_gru_lbr0(H, N, direction, layout, opts):
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tensor_core_gru_lbr0(H, N, direction, layout, opts, dtype):
     """GRU with linear_before_reset = 0 on the small-batch tensor-core kernel:
-    two products per step, r (.) h_prev rounded to Half and exchanged inside
-    the cluster before the candidate's product.  Matches the oracle within
-    the Half tolerance and the SIMT cluster kernel."""
+    two products per step, r (.) h_prev rounded to the 16-bit type and
+    exchanged inside the cluster before the candidate's product.  Matches
+    the oracle within the type's tolerance and the SIMT cluster kernel."""
     kw = dict(clip=1.5) if opts == "full" else {}
     if opts == "full":
         D = 2 if direction == "bidirectional" else 1
         kw["activations"] = [("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0)] * D
-    pr = rk.Problem("gru", seq=9, batch=N, input=24, hidden=H, direction=direction, dtype="f16", layout=layout,
+    pr = rk.Problem("gru", seq=9, batch=N, input=24, hidden=H, direction=direction, dtype=dtype, layout=layout,
                     linear_before_reset=0, **kw)
     plan = layer().plan(pr)
     assert "step=tensor" in plan and "J=32" in plan
@@ -439,6 +480,22 @@ def test_host_buffer_entry_matches_device_entry():
     np.testing.assert_array_equal(Yh.astype(np.float64), dev["Y_h"])
 
 
+def test_host_buffer_entry_bfloat16():
+    """bfloat16 host buffers (CPU tensors: numpy has no bfloat16) through the
+    host entry point give the device entry point's bits."""
+    w = workloads.WORKLOADS["bilstm_s48_b8_i192_h96_bf16"]
+    pr = w.problem
+    inp = workloads.make_inputs(w)
+    dev = run_gpu(pr, inp)
+    host_in = {k: (torch.from_numpy(v) if k == "sequence_lens" else torch.from_numpy(v).to(torch.bfloat16))
+               for k, v in inp.items()}
+    shp = pr.shapes()
+    outs = {n: torch.zeros(shp[n], dtype=torch.bfloat16) for n in ("Y", "Y_h", "Y_c")}
+    layer().encode_host(pr, **outs, **host_in)
+    for n, t in outs.items():
+        assert torch.equal(t.reshape(-1), dev[n + "_raw"].cpu()), n
+
+
 def test_bounded_wait_gives_up_and_context_survives():
     L = rk.RecurrentLayer()
     s = torch.cuda.current_stream()
@@ -465,20 +522,21 @@ def test_validation_error_launches_nothing():
     assert L.launches() == before
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("S,N,I,H", [(75, 4, 200, 600), (1, 1, 8, 16), (130, 1, 1024, 256)])
-def test_half_projection_tensor_cores(S, N, I, H):
+def test_16bit_projection_tensor_cores(S, N, I, H, dtype):
     """An RNN with Affine(1, 0), R = 0 and no bias outputs its projection:
-    Y[t] = x_t . W^T.  Half inputs take the tcgen05 projection; the result
-    matches the oracle's projection and the SIMT projection (same float32
-    products of Half values, different summation order)."""
-    pr = rk.Problem("rnn", seq=S, batch=N, input=I, hidden=H, direction="bidirectional", dtype="f16",
+    Y[t] = x_t . W^T.  Half and bfloat16 inputs take the tcgen05 projection;
+    the result matches the oracle's projection and the SIMT projection (same
+    float32 products of 16-bit values, different summation order)."""
+    pr = rk.Problem("rnn", seq=S, batch=N, input=I, hidden=H, direction="bidirectional", dtype=dtype,
                     activations=[("affine", 1.0, 0.0)] * 2)
     plan = layer().plan(pr)
     assert "proj=tc" in plan or "proj=fused" in plan  # both the tcgen05 projection
     rng = np.random.default_rng(S + I)
-    inp = {"X": rng.uniform(-1, 1, (S, N, I)).astype(np.float16),
-           "W": rng.uniform(-0.1, 0.1, (2, H, I)).astype(np.float16),
-           "R": np.zeros((2, H, H), np.float16)}
+    inp = {"X": workloads.cast(rng.uniform(-1, 1, (S, N, I)), dtype),
+           "W": workloads.cast(rng.uniform(-0.1, 0.1, (2, H, I)), dtype),
+           "R": workloads.cast(np.zeros((2, H, H)), dtype)}
     got = run_gpu(pr, inp, outputs=("Y",))
     want = oracle.projection(inp["X"].astype(np.float64).reshape(S * N, I), inp["W"].astype(np.float64))
     ref = {"Y": want.reshape(2, S, N, H).transpose(1, 0, 2, 3)}
@@ -499,11 +557,13 @@ TC_STEP_CASES = [
 ]
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("cell,H,N,direction,layout,opts", TC_STEP_CASES)
-def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts):
-    """Half layers with a batch of 4 or more run R . h on the tensor cores
-    (h rounded to Half for the product, state float32); results match the
-    oracle within the Half tolerance and the SIMT step kernel."""
+def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts, dtype):
+    """16-bit layers (Half, bfloat16) with a batch of 4 or more run R . h on
+    the tensor cores (h rounded to the 16-bit type for the product, state
+    float32); results match the oracle within the type's tolerance and the
+    SIMT step kernel."""
     kw = dict(clip=1.5) if opts == "full" else {}
     if opts == "full" and cell == "lstm":
         kw["input_forget"] = 1
@@ -511,7 +571,7 @@ def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts):
         A = {"lstm": 3, "gru": 2, "rnn": 1}[cell]
         D = 2 if direction == "bidirectional" else 1
         kw["activations"] = ([("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0), ("tanh", 0, 0)][:A]) * D
-    pr = rk.Problem(cell, seq=7, batch=N, input=24, hidden=H, direction=direction, dtype="f16", layout=layout,
+    pr = rk.Problem(cell, seq=7, batch=N, input=24, hidden=H, direction=direction, dtype=dtype, layout=layout,
                     linear_before_reset=1 if cell == "gru" else 0, **kw)
     assert "step=tensor" in layer().plan(pr)
     lens = list(np.random.default_rng(N).integers(0, 8, N))
