@@ -93,6 +93,9 @@ enum rk_activation_kind {
 #define RK_FORCE_SIMT_STEP 8u       /* 16-bit problems: never the tensor-core step kernel */
 #define RK_SEPARATE_PROJECTION 16u  /* never compute the projection on the SMs the tensor-core
                                        recurrence leaves idle (always a launch of its own) */
+#define RK_PREFER_TENSOR_STEP 32u   /* 16-bit problems: a tensor-core step kernel wherever one applies,
+                                       ahead of the register-resident SIMT kernel (which is faster
+                                       wherever all its clusters fit the GPU) */
 
 /* One activation slot (GpuRecurrentActivation): kind plus resolved alpha/beta. */
 typedef struct rk_activation {
@@ -151,7 +154,8 @@ typedef struct rk_handle rk_handle;
 int32_t rk_version(void);
 
 /* Create a handle.  No CUDA call is made until the first encode, so this
- * works without a GPU.  flags: RK_FORCE_* bits.  *out receives the handle. */
+ * works without a GPU.  flags: the rk_create flag bits above.  *out receives
+ * the handle. */
 rk_status rk_create(rk_handle** out, uint32_t flags);
 
 /* Wait for the handle's work on the streams it used, free its scratch and the

@@ -24,7 +24,7 @@ __all__ = [
     "rk_describe_plan", "rk_version", "rk_selftest_timeout", "rk_set_profiling", "rk_last_timings",
     "rk_encode_noalloc", "RK_OK", "RK_ERR_SHAPE", "RK_ERR_UNSUPPORTED", "RK_ERR_CUDA", "RK_ERR_TIMEOUT", "RK_ERR_OOM", "RK_ERR_ARG",
     "RK_FORCE_SIMT_PROJECTION", "RK_FORCE_GRID_STEP", "RK_FORCE_GENERAL_STEP", "RK_FORCE_SIMT_STEP",
-    "RK_SEPARATE_PROJECTION", "EXPORTED_SYMBOLS",
+    "RK_SEPARATE_PROJECTION", "RK_PREFER_TENSOR_STEP", "EXPORTED_SYMBOLS",
 ]
 
 RK_OK, RK_ERR_SHAPE, RK_ERR_UNSUPPORTED, RK_ERR_CUDA, RK_ERR_TIMEOUT, RK_ERR_OOM, RK_ERR_ARG = range(7)
@@ -33,6 +33,7 @@ RK_FORCE_GRID_STEP = 2
 RK_FORCE_GENERAL_STEP = 4
 RK_FORCE_SIMT_STEP = 8
 RK_SEPARATE_PROJECTION = 16
+RK_PREFER_TENSOR_STEP = 32
 CELLS = {"lstm": 0, "gru": 1, "rnn": 2}
 DIRECTIONS = {"forward": 0, "reverse": 1, "bidirectional": 2}
 DTYPES = {"f32": 0, "float32": 0, "f16": 1, "float16": 1, "half": 1, "bf16": 2, "bfloat16": 2}

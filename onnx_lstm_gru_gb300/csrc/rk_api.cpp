@@ -285,9 +285,11 @@ cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl
 
 // Step-kernel plan, in order of preference: the one-row-per-cluster
 // kernel (R in registers) when a row's hidden units fit 16 CTAs of <= 32
-// units and R's chunks fit the registers; else the cluster kernel when R
-// fits one cluster's shared memory; else the grid kernel.  `check` asks the
-// occupancy API (needs a device).
+// units, R's chunks fit the registers and every cluster fits the GPU at
+// once; else, for 16-bit layers with 4 or more rows, a tensor-core kernel;
+// else the cluster kernel when R fits one cluster's shared memory; else the
+// grid kernel.  RK_PREFER_TENSOR_STEP puts the tensor-core kernels first.
+// `check` asks the occupancy API (needs a device).
 rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
   const int G = sp->G, D = sp->D, N = sp->N, H = sp->H, KP = sp->KP;
   const int eb = p->dtype == RK_F32 ? 4 : 2;
@@ -314,6 +316,42 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     }
     return teams;
   };
+  // fast kernel: one batch row per cluster, R rows in registers.  Largest
+  // cluster (<= 16 CTAs) whose clusters all fit the GPU at once, with 16 to
+  // 32 hidden units per CTA (fewer when H itself is smaller).  Where it fits
+  // it beats the tensor-core kernels at every size measured (16-bit
+  // bidirectional layers, H 64 to 512, 4 to 16 rows: 0.7-2.0 against
+  // 1.9-3.5 us per step), its h exchange being a push into the peers'
+  // shared memory rather than a publication through global memory.
+  const int KV = KP / rk::kKChunk;
+  const bool kv_ok = (p->dtype == RK_F32 ? KV <= 2 : KV <= 4) && KV != 3;
+  const int U = p->cell == RK_RNN ? 8 : (KV <= 2 ? 4 : 2);  // units per warp, as the kernel uses
+  auto try_fast = [&]() -> bool {
+    if ((h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP)) || !kv_ok) return false;
+    for (int C = 16; C >= 1; C /= 2) {
+      StepPlan pl{};
+      pl.kind = rk::kStepClusterFast;
+      pl.shape = rk::kShapeR8B1;
+      pl.team_ctas = C;
+      pl.J = (H + C - 1) / C;
+      if (pl.J > 32 || pl.J < std::min(H, 16)) continue;
+      if (C > 1 && (int64_t)(C - 1) * pl.J >= H) continue;  // no CTA without units
+      if ((int64_t)D * N * C > h->sms) continue;            // all clusters at once
+      pl.nb = 1;
+      pl.nbc = 1;
+      pl.teams_per_dir = N;
+      pl.kv = KV;
+      pl.threads = (pl.J + U - 1) / U * 32;
+      pl.grid = D * N * C;
+      if (!finish(pl)) continue;
+      if (check && resident(pl) < 1) continue;
+      *out = pl;
+      return true;
+    }
+    return false;
+  };
+  const bool tensor_first = p->dtype != RK_F32 && (h->flags & RK_PREFER_TENSOR_STEP);
+  if (!tensor_first && try_fast()) return RK_OK;
   // tensor-core kernel: 16-bit layers (Half or bfloat16) with a batch worth
   // a dense product (R . h on tcgen05), every CTA of the launch resident at once
   if (p->dtype != RK_F32 && !(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP | RK_FORCE_SIMT_STEP)) &&
@@ -402,34 +440,7 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
       return RK_OK;
     }
   }
-  // fast kernel: one batch row per cluster, R rows in registers.  Largest
-  // cluster (<= 16 CTAs) whose clusters all fit the GPU at once, with 16 to
-  // 32 hidden units per CTA (fewer when H itself is smaller).
-  const int KV = KP / rk::kKChunk;
-  const bool kv_ok = (p->dtype == RK_F32 ? KV <= 2 : KV <= 4) && KV != 3;
-  const int U = p->cell == RK_RNN ? 8 : (KV <= 2 ? 4 : 2);  // units per warp, as the kernel uses
-  if (!(h->flags & (RK_FORCE_GRID_STEP | RK_FORCE_GENERAL_STEP)) && kv_ok) {
-    for (int C = 16; C >= 1; C /= 2) {
-      StepPlan pl{};
-      pl.kind = rk::kStepClusterFast;
-      pl.shape = rk::kShapeR8B1;
-      pl.team_ctas = C;
-      pl.J = (H + C - 1) / C;
-      if (pl.J > 32 || pl.J < std::min(H, 16)) continue;
-      if (C > 1 && (int64_t)(C - 1) * pl.J >= H) continue;  // no CTA without units
-      if ((int64_t)D * N * C > h->sms) continue;            // all clusters at once
-      pl.nb = 1;
-      pl.nbc = 1;
-      pl.teams_per_dir = N;
-      pl.kv = KV;
-      pl.threads = (pl.J + U - 1) / U * 32;
-      pl.grid = D * N * C;
-      if (!finish(pl)) continue;
-      if (check && resident(pl) < 1) continue;
-      *out = pl;
-      return RK_OK;
-    }
-  }
+  if (tensor_first && try_fast()) return RK_OK;
   if (!(h->flags & RK_FORCE_GRID_STEP)) {
     const int nb = N == 1 ? 1 : std::min(N, 8);
     const rk::StepShape shape = nb == 1 ? rk::kShapeR8B1 : rk::kShapeR4B8;

@@ -186,7 +186,17 @@ def test_plans_without_device(handle):
     # bfloat16 layers take the same kernels as Half ones
     assert plans["bilstm_s512_b64_i1024_h1024_bf16"] == plans["bilstm_s512_b64_i1024_h1024_f16"]
     assert plans["bilstm_s48_b8_i192_h96_bf16"] == plans["bilstm_s48_b8_i192_h96_f16"]
-    assert "step=tensor" in plans["bilstm_s48_b8_i192_h96_bf16"] and "J=32" in plans["bilstm_s48_b8_i192_h96_bf16"]
+    # the register-resident SIMT kernel wherever all its clusters fit (here 16
+    # rows x 2 directions x 4 CTAs), the tensor-core kernel only when asked
+    assert "step=fast" in plans["bilstm_s48_b8_i192_h96_f16"] and "ctas=4" in plans["bilstm_s48_b8_i192_h96_f16"]
+    h5 = rk.rk_create(rk.RK_PREFER_TENSOR_STEP)
+    try:
+        rec = workloads.WORKLOADS["bilstm_s48_b8_i192_h96_bf16"].problem.to_c()
+        assert "step=tensor" in rk.rk_describe_plan(h5, rec) and "J=32" in rk.rk_describe_plan(h5, rec)
+        # float32 layers never take the tensor cores
+        assert "step=fast" in rk.rk_describe_plan(h5, workloads.WORKLOADS["bilstm_s48_b8_i192_h96_f32"].problem.to_c())
+    finally:
+        rk.rk_destroy(h5)
     for name, text in plans.items():
         smem = int(re.search(r"smem=(\d+)", text).group(1))
         assert smem <= 232448 - 1024, (name, text)

@@ -216,6 +216,9 @@ for cell in ("lstm", "gru", "rnn"):
 
 
 KERNELS = {"fast": 0, "cluster": rk.RK_FORCE_GENERAL_STEP, "grid": rk.RK_FORCE_GRID_STEP}
+# the tensor-core step kernels ahead of the register-resident SIMT kernel,
+# which the planner prefers wherever all its clusters fit the GPU
+TC = rk.RK_PREFER_TENSOR_STEP
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
@@ -383,12 +386,12 @@ def test_tensor_core_step_with_odd_offsets(cell, dtype):
     and leave the sentinels around the outputs untouched."""
     pr = rk.Problem(cell, seq=5, batch=6, input=24, hidden=72, direction="bidirectional", dtype=dtype,
                     linear_before_reset=1 if cell == "gru" else 0)
-    assert "step=tensor" in layer().plan(pr)
+    assert "step=tensor" in layer(TC).plan(pr)
     inp = rand_inputs(pr, seed=77, scale=0.15)
-    got = run_gpu(pr, inp, in_off=3, out_off=5)
+    got = run_gpu(pr, inp, in_off=3, out_off=5, flags=TC)
     compare(pr, got, run_oracle(pr, inp), None)
     # unaligned X and W take the SIMT projection: compare against it
-    aligned = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_PROJECTION)
+    aligned = run_gpu(pr, inp, flags=TC | rk.RK_FORCE_SIMT_PROJECTION)
     for k in got:
         if k.endswith("_raw"):
             assert torch.equal(got[k], aligned[k]), k
@@ -434,15 +437,15 @@ def test_tensor_core_gru_lbr0(H, N, direction, layout, opts, dtype):
         kw["activations"] = [("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0)] * D
     pr = rk.Problem("gru", seq=9, batch=N, input=24, hidden=H, direction=direction, dtype=dtype, layout=layout,
                     linear_before_reset=0, **kw)
-    plan = layer().plan(pr)
+    plan = layer(TC).plan(pr)
     assert "step=tensor" in plan and "J=32" in plan
     lens = list(np.random.default_rng(H).integers(0, 10, N))
     inp = rand_inputs(pr, seed=H + 7 * N, lens=lens, scale=0.2)
-    got = run_gpu(pr, inp)
+    got = run_gpu(pr, inp, flags=TC)
     compare(pr, got, run_oracle(pr, inp), lens)
     simt = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_STEP)
     compare(pr, got, {k: v for k, v in simt.items() if not k.endswith("_raw")}, lens)
-    again = run_gpu(pr, inp)
+    again = run_gpu(pr, inp, flags=TC)
     for k in got:
         if k.endswith("_raw"):
             assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
@@ -454,14 +457,14 @@ def test_tensor_core_step_ignores_stale_scratch(H, N):
     blocks and batch blocks; parts no CTA owns must not leak stale scratch.
     Caller scratch filled with NaN bytes gives the same bits as fresh scratch."""
     pr = rk.Problem("lstm", seq=6, batch=N, input=16, hidden=H, direction="bidirectional", dtype="f16")
-    assert "step=tensor" in layer().plan(pr)
+    assert "step=tensor" in layer(TC).plan(pr)
     inp = rand_inputs(pr, seed=H * N, scale=0.15)
-    base = run_gpu(pr, inp)
+    base = run_gpu(pr, inp, flags=TC)
     c = pr.to_c()
     nx, ns = rk.rk_xw_length(c), rk.rk_state_length(c)
     arena = torch.full((nx + ns + 64,), float("nan"), dtype=torch.float32, device="cuda")
     sc = rk.rk_scratch(arena.data_ptr(), 0, nx, arena.data_ptr(), nx + 4, nx + ns + 64)
-    got = run_gpu(pr, inp, scratch=sc)
+    got = run_gpu(pr, inp, scratch=sc, flags=TC)
     for k in ("Y_raw", "Y_h_raw", "Y_c_raw"):
         assert torch.equal(base[k], got[k]), k
     assert np.isfinite(got["Y"]).all()
@@ -573,14 +576,14 @@ def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts, dtype):
         kw["activations"] = ([("hardsigmoid", 0.2, 0.5), ("softsign", 0, 0), ("tanh", 0, 0)][:A]) * D
     pr = rk.Problem(cell, seq=7, batch=N, input=24, hidden=H, direction=direction, dtype=dtype, layout=layout,
                     linear_before_reset=1 if cell == "gru" else 0, **kw)
-    assert "step=tensor" in layer().plan(pr)
+    assert "step=tensor" in layer(TC).plan(pr)
     lens = list(np.random.default_rng(N).integers(0, 8, N))
     inp = rand_inputs(pr, seed=H + N, lens=lens, peep=(opts == "full"), scale=0.15)
-    got = run_gpu(pr, inp)
+    got = run_gpu(pr, inp, flags=TC)
     compare(pr, got, run_oracle(pr, inp), lens)
     simt = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_STEP)
     compare(pr, got, {k: v for k, v in simt.items() if not k.endswith("_raw")}, lens)
-    again = run_gpu(pr, inp)
+    again = run_gpu(pr, inp, flags=TC)
     for k in got:
         if k.endswith("_raw"):
             assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
