@@ -94,10 +94,11 @@ __global__ void __launch_bounds__(256) proj_simt_kernel(int M, int N, int K, con
 // aligned, K * element size a multiple of 16): 4 stages of 32-deep k tiles
 // are kept in flight with cp.async (16-byte copies, zero-filled past M, N
 // and K), so the loads of later tiles overlap the arithmetic of earlier ones.
-// Tiles are PBM x 64 of Xw per 128-thread CTA; thread (tm, tn) owns rows
-// tm + 8 i and columns tn + 16 j (strided, so the 16-byte shared loads of a
-// quarter warp hit distinct banks and the stores are coalesced).  Each output
-// is still one fused-multiply-add chain in increasing k.
+// Tiles are PBM x 64 (PBM = 8, 16, 24 or 32) of Xw per 128-thread CTA;
+// thread (tm, tn) owns rows tm + 8 i and columns tn + 16 j (strided, so the
+// 16-byte shared loads of a quarter warp hit distinct banks and the stores
+// are coalesced).  Each output is still one fused-multiply-add chain in
+// increasing k, whatever the tile height.
 constexpr int PBN = 64, PBK = 32, PSTAGES = 4, PTHREADS = 128;
 
 template <typename T>
@@ -127,6 +128,7 @@ __device__ __forceinline__ float4 load4_row<float>(const float* p) {
 template <typename T, int PBM>
 __global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K, const T* __restrict__ X,
                                                              const T* __restrict__ W, float* __restrict__ Xw) {
+  static_assert(PBM % 8 == 0 && PBM >= 8 && PBM <= 32, "tile rows: 8 to 32 in steps of 8");
   // the step kernel after this one may be launched early (programmatic
   // dependent launch); it waits for this grid before reading Xw
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -222,6 +224,35 @@ cudaError_t launch_pipe(const ProjParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_pipe_rows(const ProjParams& p, cudaStream_t s, int rows) {
+  switch (rows) {
+    case 8: return launch_pipe<T, 8>(p, s);
+    case 16: return launch_pipe<T, 16>(p, s);
+    case 24: return launch_pipe<T, 24>(p, s);
+    default: return launch_pipe<T, 32>(p, s);
+  }
+}
+
+// Tile height: the SM that gets the most tiles sets the time, so take the
+// height (8 to 32 rows) that minimises rows x tiles-per-SM, counting 4 rows'
+// worth of fixed cost per tile (the loads of W, the prologue).  A grid just
+// above the SM count (160 tiles of 16 rows on 152 SMs for the 80 x 1024 x
+// 256 bidirectional layer) leaves most SMs idle for the second half.
+int pipe_rows_for(long long M, long long col_tiles, int sms) {
+  int best = 32;
+  long long best_cost = -1;
+  for (int rows = 32; rows >= 8; rows -= 8) {
+    const long long tiles = col_tiles * ((M + rows - 1) / rows);
+    const long long cost = (long long)(rows + 4) * ((tiles + sms - 1) / sms);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = rows;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
@@ -230,14 +261,12 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   const bool aligned = (reinterpret_cast<uintptr_t>(p.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
                        ((size_t)p.K * eb) % 16 == 0 && p.K > 0;
   if (aligned) {
-    // 16-row tiles when 32-row tiles would leave SMs idle
-    const long long tiles32 = (long long)((p.N + PBN - 1) / PBN) * ((p.M + 31) / 32) * p.D;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool small = tiles32 < 2LL * sms;
-    if (p.dtype == 0) return small ? launch_pipe<float, 16>(p, s) : launch_pipe<float, 32>(p, s);
-    if (p.dtype == 2) return small ? launch_pipe<__nv_bfloat16, 16>(p, s) : launch_pipe<__nv_bfloat16, 32>(p, s);
-    return small ? launch_pipe<__half, 16>(p, s) : launch_pipe<__half, 32>(p, s);
+    const int rows = pipe_rows_for(p.M, (long long)((p.N + PBN - 1) / PBN) * p.D, sms);
+    if (p.dtype == 0) return launch_pipe_rows<float>(p, s, rows);
+    if (p.dtype == 2) return launch_pipe_rows<__nv_bfloat16>(p, s, rows);
+    return launch_pipe_rows<__half>(p, s, rows);
   }
   dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.D);
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
