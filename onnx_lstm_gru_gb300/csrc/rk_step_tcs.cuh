@@ -15,25 +15,32 @@
 // units; rows past G * 32 are zero) held in shared memory for the whole
 // layer, and its N = 16 columns are the direction's batch rows, so the
 // exchanged operand is only 16 rows of h (2 KB per 64 k).  A team is one
-// direction, one cluster of ceil(H / 32) CTAs.  Per step:
-//   1. the producer warp waits until every CTA of the cluster has published
-//      h_s (remote mbarrier arrivals, cluster-scope release / acquire) and
-//      copies the direction's whole 16-bit h_s (H / 64 blocks of 16 rows x 64
-//      k, 128-byte swizzled, double-buffered in global memory) with one
-//      bulk copy;
-//   2. one lane issues the H / 16 MMAs (kind::f16, M = 128, N = 16, K = 16)
-//      into one fp32 TMEM accumulator (lane = gate row, column = batch row);
-//   3. warp g < G reads gate g's lanes (unit = lane) and stages them in
+// direction, one cluster of ceil(H / 32) CTAs.  Every CTA keeps the whole
+// 16-bit operand, double-buffered, in its own shared memory in the layout
+// the tensor cores read (H / 64 blocks of 16 rows x 64 k, 128-byte
+// swizzled).  Per step:
+//   1. one lane issues the H / 16 MMAs (kind::f16, M = 128, N = 16,
+//      K = 16) on buffer s % 2 into one fp32 TMEM accumulator (lane = gate
+//      row, column = batch row) once that buffer's byte-counting mbarrier
+//      has completed;
+//   2. warp g < G reads gate g's lanes (unit = lane) and stages them in
 //      shared memory; every gate thread then takes one (unit, batch row)
-//      pair (two when the batch exceeds 8), does the gate arithmetic, writes
-//      its 16-bit h into the next global buffer and Y, and the CTA publishes.
-// GRU with linear_before_reset = 0 runs two rounds per step: the first
-// product gives z and r, each thread writes its 16-bit r (.) h_prev to a second
-// global buffer and the cluster publishes it, the producer copies it in
-// place of h and the second product's candidate rows give R_h . (r (.) h).
-// The summation order is fixed (k in increasing 16-wide steps), so runs are
+//      pair (two when the batch exceeds 8) and does the gate arithmetic;
+//   3. each warp packs its row's 32 new 16-bit h values into four 16-byte
+//      chunks (shuffles) and pushes every chunk into buffer (s + 1) % 2 of
+//      every CTA of the cluster with st.async, whose completion counts the
+//      bytes on the receiver's mbarrier -- no global memory, no flags, no
+//      copy back.
+// A buffer is re-armed (expected bytes) before this CTA pushes the h that
+// lets its peers produce the next value for it, and a peer can only write
+// h_{s+2} into buffer s % 2 after it has every CTA's h_{s+1}, by which time
+// every product that read h_s is complete.  GRU with linear_before_reset
+// = 0 runs two rounds per step: the first product gives z and r, each warp
+// pushes its 16-bit r (.) h_prev the same way into a second pair of buffers,
+// and the second product's candidate rows give R_h . (r (.) h).  The
+// summation order is fixed (k in increasing 16-wide steps), so runs are
 // bit-identical.  Every wait is bounded; on expiry the kernel sets the
-// status word, drains its copy and MMAs, frees its TMEM and returns.
+// status word, drains its MMAs, frees its TMEM and returns.
 #pragma once
 #include "rk_step_tc.cuh"
 
@@ -47,8 +54,8 @@ constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at mos
 constexpr int XBLK_A = 128 * 128;  // bytes of one 64-k block of the gate rows
 constexpr int XBLK_B = XN * 128;   // bytes of one 64-k block of h
 
-// Shared memory: [gate rows: KB x 16 KB][h: KB x 2 KB][staged products
-// [4][32][16] floats][barriers][biases]
+// Shared memory: [gate rows: KB x 16 KB][operands: [h, r (.) h][2 buffers]
+// [KB x 2 KB]][staged products [4][32][16] floats][barriers][biases]
 struct XsSmem {
   size_t r, h, acc, bar, bias, total;
 };
@@ -57,7 +64,7 @@ __host__ __device__ inline XsSmem xs_layout(int G, int H) {
   const int KB = (H + SK - 1) / SK;
   size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
   L.r = o;    o += (size_t)KB * XBLK_A;
-  L.h = o;    o += (size_t)KB * XBLK_B;
+  L.h = o;    o += (size_t)2 * 2 * KB * XBLK_B;
   L.acc = o;  o += (size_t)4 * XJ * XN * 4;
   L.bar = o;  o += 256;
   L.bias = o; o += (size_t)2 * 4 * XJ * 4 + 3 * XJ * 4;
@@ -66,14 +73,8 @@ __host__ __device__ inline XsSmem xs_layout(int G, int H) {
   return L;
 }
 
-// Element offset of block kb of (buffer, direction) in the 16-bit copies:
-// [h or r (.) h][2 buffers][D][KB blocks][16 rows x 64 k, swizzled].
-__device__ __forceinline__ size_t xs_h_block(const StepParams& p, int which, int buf, int d, int kb, int KB) {
-  return ((((size_t)which * 2 + buf) * p.D + d) * KB + kb) * (size_t)(XBLK_B / 2);
-}
-
 template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
-__global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams p, E* __restrict__ h16) {
+__global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams p) {
   static_assert(!LBR0 || CELL == 1, "two rounds only for GRU with linear_before_reset = 0");
   constexpr int NRND = LBR0 ? 2 : 1;  // products per step
   constexpr int G = CellInfo<CELL>::G;
@@ -85,9 +86,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   unsigned char* sR = base + (L.r - 1024);
   unsigned char* sH = base + (L.h - 1024);
   float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));  // [g][u][b]
-  // full, drain, then per round: done, free, staged, gather, cluster publication[2]
+  // operand arrived [round][buffer], drain, then per round: done, free, staged
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   float* wb_s = reinterpret_cast<float*>(base + (L.bias - 1024));  // [g * XJ + u]
   float* rb_s = wb_s + 4 * XJ;
   float* pp_s = rb_s + 4 * XJ;                                     // [u * 3 + g]
@@ -141,23 +142,42 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     const int u = e / 3, g = e % 3;
     pp_s[e] = (CELL == 0 && !PLAIN && P != nullptr && j0 + u < H) ? Elem<E>::to_f(P[(size_t)d * 3 * H + (size_t)g * H + j0 + u]) : 0.0f;
   }
+  // operand buffers: zero all (the k columns past the last CTA's units and
+  // the rows past the batch belong to nobody; R is zero there too, but a
+  // stale Inf or NaN times zero would not be), then h_0 into buffer 0
+  const int KBB = KB * XBLK_B;  // bytes of one buffer
+  for (int e = tid; e < 4 * KBB / 16; e += blockDim.x)
+    reinterpret_cast<uint4*>(sH)[e] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  auto sh_at = [&](int which, int buf, int b, int j) {
+    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + (size_t)(j / SK) * XBLK_B + sw128_offset(b, j % SK));
+  };
+  for (int e = tid; e < N * H; e += blockDim.x) {
+    const int b = e / H, j = e % H;
+    *sh_at(0, 0, b, j) = Elem<E>::from_f(h0 != nullptr ? Elem<E>::to_f(h0[state_index(p, d, b, j)]) : 0.0f);
+  }
+  // bytes of one operand's arrival: C CTAs x N rows x 32 units x 2 bytes
+  const uint32_t op_bytes = (uint32_t)C * (uint32_t)N * (uint32_t)(XJ * 2);
+  auto full_bar = [&](int which, int buf) { return su32(&bars[which * 2 + buf]); };
   if (tid == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);  // operand copy landed (one per round)
-    mbar_init(smem_u32(&bars[1]), 1);  // final MMA drain
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);  // operand [round][buffer] arrived
+    mbar_init(smem_u32(&bars[4]), 1);                                // final MMA drain
     for (int rd = 0; rd < 2; ++rd) {
-      uint64_t* b6 = bars + 2 + 6 * rd;
-      mbar_init(smem_u32(&b6[0]), 1);            // accumulator complete (MMA commit)
-      mbar_init(smem_u32(&b6[1]), 8);            // accumulator read (8 gate warps)
-      mbar_init(smem_u32(&b6[2]), 8);            // products staged (8 gate warps)
-      mbar_init(smem_u32(&b6[3]), 8);            // 16-bit copies written (8 gate warps)
-      mbar_init(smem_u32(&b6[4]), (unsigned)C);  // every CTA published, step even
-      mbar_init(smem_u32(&b6[5]), (unsigned)C);  // ... step odd
+      uint64_t* b3 = bars + 5 + 3 * rd;
+      mbar_init(smem_u32(&b3[0]), 1);  // accumulator complete (MMA commit)
+      mbar_init(smem_u32(&b3[1]), 8);  // accumulator read (8 gate warps)
+      mbar_init(smem_u32(&b3[2]), 8);  // products staged (8 gate warps)
     }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // h_0 was written locally: complete buffer 0's first phase; arm the
+    // arrivals of h_1 and of r (.) h_0 before any CTA can push them
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(full_bar(0, 0)) : "memory");
+    if (Tn > 1) mbar_arrive_expect_tx(full_bar(0, 1), op_bytes);
+    if (LBR0 && Tn > 0) mbar_arrive_expect_tx(full_bar(1, 0), op_bytes);
   }
-  // the gate rows were written by ordinary stores; the tensor cores read them
-  // through the async proxy
+  // the gate rows and h_0 were written by ordinary stores; the tensor cores
+  // read them through the async proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -180,11 +200,6 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     hreg[k] = creg[k] = 0.0f;
     lenv[k] = Tn;
   }
-  // address of (buffer, batch row b, unit j) in the 16-bit h copy
-  auto h16_at = [&](int which, int buf, int b, int j) {
-    return reinterpret_cast<E*>(reinterpret_cast<unsigned char*>(h16 + xs_h_block(p, which, buf, d, j / SK, KB)) +
-                                     sw128_offset(b, j % SK));
-  };
 #pragma unroll
   for (int k = 0; k < XPAIRS; ++k) {
     if (!pv[k]) continue;
@@ -199,102 +214,60 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       hreg[k] = h0 != nullptr ? Elem<E>::to_f(h0[si]) : 0.0f;
       creg[k] = (CELL == 0 && c0 != nullptr) ? Elem<E>::to_f(c0[si]) : 0.0f;
     }
-    *h16_at(0, 0, b, pj) = Elem<E>::from_f(pj < H ? hreg[k] : 0.0f);  // h_0 into buffer 0
-  }
-  // k columns past the last CTA's units (up to the 64-wide block) belong to
-  // no CTA: zero them once in both buffers for every row (R is zero there
-  // too, but a stale Inf or NaN times zero would not be)
-  if (rank == C - 1) {
-    const int pad = KB * SK - C * XJ;
-    for (int e = tid; e < pad * XN * 2 * NRND; e += blockDim.x) {
-      const int k = C * XJ + e % pad, b = (e / pad) % XN, buf = (e / (pad * XN)) % 2, which = e / (pad * XN * 2);
-      *h16_at(which, buf, b, k) = Elem<E>::from_f(0.0f);
-    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA's barriers are initialised before any remote arrival (all CTAs
-  // of a cluster run at once and reach this point)
+  // every CTA's barriers are initialised and armed before any push (all
+  // CTAs of a cluster run at once and reach this point)
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   const uint32_t tmem_acc = *tmem_slot;
 
-  const uint32_t bar_full = su32(&bars[0]), bar_drain = su32(&bars[1]);
-  // round rd's barriers: done, free, staged, gather, cluster publication[2]
-  auto rbar = [&](int rd, int i) { return su32(&bars[2 + 6 * rd + i]); };
-  // gate warps: make this CTA's new h copies visible to the async proxy,
-  // gather the 8 warps, then lane q of warp 0 arrives on CTA q's
-  // publication barrier for h_s (one barrier per step parity: a CTA's
-  // arrivals for h_{s+2} come after it saw every arrival for h_{s+1}, each
-  // made after its sender's arrivals for h_s)
-  // round 0 publishes h_s (value = s + 1), round 1 r (.) h of step s
-  // (value = s + 1 too); a round's gather barrier completes once per value
-  auto publish = [&](int rd, unsigned value) {
-    const uint32_t bar_pub = rbar(rd, 3), bar_pubc = rbar(rd, 4);
-    const uint32_t pub_parity = (value - 1u) & 1u;
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_pub) : "memory");
-    if (warp == 0 && lane < C) {
-      if (bar_wait(bar_pub, pub_parity, p.timeout_ns)) {
-        const uint32_t local = bar_pubc + 8u * ((value - 1u) & 1u);  // step value - 1
-        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_to_rank(local, (uint32_t)lane))
-                     : "memory");
-      } else {
-        abort_flag = 1;
-        atomicOr(p.status, 1);
-      }
+  const uint32_t bar_drain = su32(&bars[4]);
+  // round rd's barriers: done, free, staged
+  auto rbar = [&](int rd, int i) { return su32(&bars[5 + 3 * rd + i]); };
+  // push this warp's batch row b of operand `which` (lane = unit, value v)
+  // into buffer buf of every CTA: lanes 8c .. 8c + 7 form the 16-byte
+  // chunk c of the row, lane l sends chunk l % 4 to CTAs l / 4, l / 4 + 8
+  auto push_row = [&](int which, int buf, int b, float v) {
+    const E e = Elem<E>::from_f(v);
+    const uint32_t hv = (uint32_t)(*reinterpret_cast<const unsigned short*>(&e));
+    const int c = lane & 3;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = __shfl_sync(0xffffffffu, hv, 8 * c + 2 * i);
+      const uint32_t hi = __shfl_sync(0xffffffffu, hv, 8 * c + 2 * i + 1);
+      w[i] = lo | (hi << 16);
     }
+    const int k = j0 + 8 * c;  // first unit of the chunk
+    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB + (k / SK) * XBLK_B) + sw128_offset(b, k % SK);
+    const uint32_t bar = full_bar(which, buf);
+    const float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]), __uint_as_float(w[3]));
+    for (int q = lane >> 2; q < C; q += 8) st_async_v4(map_to_rank(dst, (uint32_t)q), x, map_to_rank(bar, (uint32_t)q));
   };
-  if (gate_warp) publish(0, 1u);
 
   const size_t xw_tstride = p.layout == 0 ? (size_t)N * GH : GH;
   const bool has_p = !PLAIN && CELL == 0 && P != nullptr;
   const float clip = PLAIN ? 0.0f : p.clip;
   const bool input_forget = !PLAIN && p.input_forget;
 
-  if (warp == 8) {
-    // ---------------- producer lane: each round's whole operand (h_s, or
-    // r (.) h_s) in one bulk copy, once every CTA of the cluster published it
-    if (lane == 0) {
-      const uint32_t bytes = (uint32_t)KB * XBLK_B;
-      int armed = -1;
-      bool ok = true;
-      for (int s = 0; s < Tn && ok; ++s) {
-        for (int rd = 0; rd < NRND; ++rd) {
-          if (abort_flag ||
-              !bar_wait_cluster(rbar(rd, 4) + 8u * (uint32_t)(s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          // the publishers' generic-proxy stores, acquired above, are read by the async proxy
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          bar_expect(bar_full, bytes);
-          bulk_load(su32(sH), h16 + xs_h_block(p, rd, s & 1, d, 0, KB), bytes, bar_full);
-          armed = (s * NRND + rd) & 1;
-        }
-      }
-      if (!ok) {
-        abort_flag = 1;
-        atomicOr(p.status, 1);
-      }
-      // drain: the copy this CTA issued last must land before it exits
-      if (armed >= 0) bar_wait(bar_full, (uint32_t)armed, p.timeout_ns);
-    }
-  } else if (warp == 9) {
+  if (warp == 9) {
     // ---------------- MMA lane: acc_rd[128 gate rows x 16 batch] = R_rows . operand^T
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(XN) | Elem<E>::kMmaAB;
       const uint64_t adesc0 = desc_sw128(su32(sR));
-      const uint64_t bdesc0 = desc_sw128(su32(sH));
       constexpr uint64_t kK16 = 32 >> 4;
       bool ok = true;
       for (int s = 0; s < Tn && ok; ++s) {
         for (int rd = 0; rd < NRND; ++rd) {
-          if (abort_flag || !bar_wait(bar_full, (uint32_t)((s * NRND + rd) & 1), p.timeout_ns)) {
+          // operand rd of step s (buffer s % 2, its (s / 2)-th arrival)
+          if (abort_flag || !bar_wait(full_bar(rd, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
             ok = false;
             break;
           }
+          // the peers' st.async writes, acquired above, are read by the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           // the gate warps must have read this accumulator of the previous step
           if (s > 0 && !bar_wait(rbar(rd, 1), (uint32_t)((s - 1) & 1), p.timeout_ns)) {
             ok = false;
@@ -302,7 +275,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           }
           tc_fence_after();
           const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
-          uint64_t ad = adesc0, bd = bdesc0;
+          uint64_t ad = adesc0, bd = desc_sw128(su32(sH) + (uint32_t)((rd * 2 + (s & 1)) * KBB));
           for (int kb = 0; kb < KB; ++kb, ad += XBLK_A >> 4, bd += XBLK_B >> 4) {
             tc_mma(tacc, ad, bd, idesc, kb != 0 ? 1u : 0u);
             tc_mma(tacc, ad + kK16, bd + kK16, idesc, 1u);
@@ -320,8 +293,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       tc_commit(bar_drain);
       bar_wait(bar_drain, 0u, p.timeout_ns);
     }
-  } else {
-    // ---------------- gate warps
+  } else if (gate_warp) {
+    // ---------------- gate warps (warp 8 has no role)
     float xv[XPAIRS][G];
     auto load_xw = [&](int s) {
 #pragma unroll
@@ -363,14 +336,14 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     bool ok = true;
     for (int s = 0; s < Tn; ++s) {
       if constexpr (LBR0) {
-        // round 0: z and r; publish r (.) h_prev
+        // round 0: z and r; push r (.) h_prev
         if (!stage(0, s, 0, 2)) {
           ok = false;
           break;
         }
 #pragma unroll
         for (int k = 0; k < XPAIRS; ++k) {
-          if (!pv[k]) continue;
+          if (!pv[k]) continue;  // the same for the whole warp
           const int b = (tid + 256 * k) >> 5;
           float pre[2];
 #pragma unroll
@@ -378,9 +351,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
             pre[g] = ((xv[k][g] + sAcc[((size_t)g * XJ + pu) * XN + b]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
           zr[k][0] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
           zr[k][1] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
-          *h16_at(1, s & 1, b, pj) = Elem<E>::from_f(pj < H ? zr[k][1] * hreg[k] : 0.0f);
+          push_row(1, s & 1, b, pj < H ? zr[k][1] * hreg[k] : 0.0f);
         }
-        publish(1, (unsigned)s + 1u);
       }
       // the last (or only) round: the remaining gate arithmetic
       constexpr int RL = NRND - 1;
@@ -436,10 +408,21 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           if (active) hn = act<GEN, 1>(p, d * A + 0, clip_pre(clip, pre[0]));
         }
         if (pj < H) hreg[k] = hn;
-        if (s + 1 < Tn) *h16_at(0, (s + 1) & 1, b, pj) = Elem<E>::from_f(pj < H ? hn : 0.0f);
         if (Y != nullptr && pj < H) Y[y_index(p, t, d, b, pj)] = Elem<E>::from_f(active ? hn : 0.0f);
       }
-      if (s + 1 < Tn) publish(0, (unsigned)s + 2u);
+      if (s + 1 < Tn) {
+        // arm the arrivals this push lets the peers send: h_{s+2} into
+        // buffer s % 2 (its h_s phase completed before this step's product)
+        // and r (.) h_{s+1} into the second operand's buffer (s + 1) % 2
+        if (tid == 0) {
+          if (s + 2 < Tn) mbar_arrive_expect_tx(full_bar(0, s & 1), op_bytes);
+          if (LBR0) mbar_arrive_expect_tx(full_bar(1, (s + 1) & 1), op_bytes);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < XPAIRS; ++k)
+          if (pv[k]) push_row(0, (s + 1) & 1, (tid + 256 * k) >> 5, pj < H ? hreg[k] : 0.0f);
+      }
       load_xw(s + 1);
     }
     if (!ok) {
@@ -472,7 +455,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
 }
 
 template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
-cudaError_t step_tcs_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, E* h16) {
+cudaError_t step_tcs_launch(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident) {
   auto kern = step_tcs_kernel<CELL, GEN, PLAIN, LBR0, E>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
@@ -499,31 +482,31 @@ cudaError_t step_tcs_launch(const StepParams& p, const StepPlan& plan, cudaStrea
     *resident = (e == cudaSuccess) ? n : 0;
     return e;
   }
-  return cudaLaunchKernelEx(&cfg, kern, p, h16);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int CELL, bool LBR0, typename E>
-cudaError_t step_tcs_cell(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q, E* h16) {
+cudaError_t step_tcs_cell(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* q) {
   const bool plain = !(p.clip > 0.0f) && p.P == nullptr && !p.input_forget;
   if (p.generic_acts)
-    return plain ? step_tcs_launch<CELL, true, true, LBR0, E>(p, plan, s, q, h16)
-                 : step_tcs_launch<CELL, true, false, LBR0, E>(p, plan, s, q, h16);
-  return plain ? step_tcs_launch<CELL, false, true, LBR0, E>(p, plan, s, q, h16)
-               : step_tcs_launch<CELL, false, false, LBR0, E>(p, plan, s, q, h16);
+    return plain ? step_tcs_launch<CELL, true, true, LBR0, E>(p, plan, s, q)
+                 : step_tcs_launch<CELL, true, false, LBR0, E>(p, plan, s, q);
+  return plain ? step_tcs_launch<CELL, false, true, LBR0, E>(p, plan, s, q)
+               : step_tcs_launch<CELL, false, false, LBR0, E>(p, plan, s, q);
 }
 
 template <typename E>
-cudaError_t step_tcs_cells(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, E* hp) {
+cudaError_t step_tcs_cells(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident) {
   switch (p.cell) {
-    case 0: return step_tcs_cell<0, false>(p, plan, s, resident, hp);
-    case 1: return p.lbr ? step_tcs_cell<1, false>(p, plan, s, resident, hp) : step_tcs_cell<1, true>(p, plan, s, resident, hp);
-    default: return step_tcs_cell<2, false>(p, plan, s, resident, hp);
+    case 0: return step_tcs_cell<0, false, E>(p, plan, s, resident);
+    case 1: return p.lbr ? step_tcs_cell<1, false, E>(p, plan, s, resident) : step_tcs_cell<1, true, E>(p, plan, s, resident);
+    default: return step_tcs_cell<2, false, E>(p, plan, s, resident);
   }
 }
 
 }  // namespace
 
 // bfloat16 layers (rk_step_tcs_bf16.cu)
-cudaError_t step_tcs_bf16(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __nv_bfloat16* h16);
+cudaError_t step_tcs_bf16(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident);
 
 }  // namespace rk

@@ -4,8 +4,8 @@
 
 namespace rk {
 
-cudaError_t step_tcs_bf16(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, __nv_bfloat16* h16) {
-  return step_tcs_cells(p, plan, s, resident, h16);
+cudaError_t step_tcs_bf16(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident) {
+  return step_tcs_cells<__nv_bfloat16>(p, plan, s, resident);
 }
 
 }  // namespace rk
