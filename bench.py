@@ -171,7 +171,9 @@ KERNEL_SOURCES = {
     "cluster": ("step_cluster_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
     "grid": ("step_grid_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
     "tensor": ("step_tc_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_proj_tc.cuh", "rk_step_tc.cuh", "rk_step_tc.cu",
-                                  "rk_step_tc_pair.cu", "rk_step_tc_cluster.cu", "rk_step_tcs.cuh")),
+                                  "rk_step_tc_pair.cu", "rk_step_tc_cluster.cu")),
+    "tensor_small": ("step_tcs_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_tc.cuh", "rk_step_tcs.cuh",
+                                         "rk_step_tcs.cu")),
     "proj_tc": ("proj_tc_kernel", ("rk_elem.cuh", "rk_proj_tc.cuh", "rk_proj_tc.cu")),
     "proj_simt": ("projection", ("rk_elem.cuh", "rk_proj.cu")),
 }
@@ -203,7 +205,7 @@ def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, alu_peak: f
     achieved = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
     name, files = KERNEL_SOURCES[kind]
     traffic = profiled_traffic(name, workload, kernel_source_hash(files))
-    if kind in ("tensor", "proj_tc"):
+    if kind in ("tensor", "tensor_small", "proj_tc"):
         peak = float(peaks["bf16_tflops"])
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": name,
@@ -409,6 +411,8 @@ def run_gb300(args):
     pf = plan_fields(plan)
     alu_src = f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz"
     step_kind = pf.get("step", "fast")
+    if step_kind == "tensor" and pf.get("variant") == "small":
+        step_kind = "tensor_small"
     proj_kind = "proj_tc" if pf.get("proj") == "tc" else "proj_simt"
     r_step = kernel_roofline(step_kind, step_flops, step_ms, peaks, alu_peak_tflops, alu_src, name)
     r_proj = kernel_roofline(proj_kind, proj_flops, proj_ms, peaks, alu_peak_tflops, alu_src, name) \

@@ -609,6 +609,13 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
            pl.kind == rk::kStepTensor ? "tensor"
                                       : (pl.kind == rk::kStepClusterFast ? "fast" : (pl.kind == rk::kStepCluster ? "cluster" : "grid")),
            (int)pl.shape, pl.team_ctas, pl.J, pl.nb, pl.teams_per_dir * sp.D, pl.threads, pl.smem, pl.grid);
+  if (pl.kind == rk::kStepTensor) {
+    // which tensor-core kernel: small batch (gate rows as M), cluster team,
+    // or flag-published teams with paired / single k blocks per tile
+    const char* v = pl.nbc == 16 ? "small" : (pl.J == 32 ? "cluster" : (pl.nbc == 64 ? "pairs" : "rows"));
+    const size_t n = strlen(buf);
+    if (n + 1 < (size_t)len) snprintf(buf + n, (size_t)len - n, " variant=%s", v);
+  }
   return RK_OK;
 }
 
