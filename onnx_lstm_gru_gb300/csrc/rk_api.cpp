@@ -253,7 +253,8 @@ FusedProj fused_projection(const rk_handle* h, const rk_problem* p, const StepPl
   const int D = dirs_of(p);
   const int np = h->sms - pl.grid;
   const int counter0 = D * pl.teams_per_dir * ((pl.team_ctas + 7) / 8 * 8);
-  const int groups = (rk::kStateHeader - counter0) / D;
+  // the last D words of the header: the Xw ring's consumption counters
+  const int groups = (rk::kStateHeader - counter0 - D) / D;
   const int mt = (pp.M + 127) / 128;
   if (np < 8 || groups < 1 || mt < 1) return f;
   if (tmA != nullptr && !(rk::projection_tc_supported(pp) && rk::projection_tc_maps(pp, tmA, tmB))) return f;
@@ -723,6 +724,14 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     sp.xw_groups = fz.groups;
     sp.xw_mpg = fz.mpg;
     sp.xw_ready = sp.counters + fz.counter0;
+    // Xw through a ring of 128-row tiles that stays in L2 (used on the
+    // device when every row has the same length; else the whole scratch)
+    // (a step waits for its whole readiness group of fz.mpg tiles, which
+    // must fit the ring next to the tiles still being read)
+    const int mt = (pp.M + 127) / 128;
+    sp.xw_ring = (mt > 2 * rk::kXwRingTiles && fz.mpg <= rk::kXwRingTiles) ? rk::kXwRingTiles : 0;
+    sp.xw_consumers = sp.D > 0 ? pl.grid / sp.D * 8 : 0;
+    sp.xw_done = sp.counters + (rk::kStateHeader - sp.D);
     e = rk::step_tc_entry(sp, fp, stream, nullptr, sp.rhglob, &tmA, &tmB);
   } else {
     e = step_dispatch(p->cell, sp, pl, stream, nullptr);

@@ -11,6 +11,10 @@ namespace rk {
 constexpr int kMaxActs = 6;
 constexpr int kKChunk = 128;      // k is padded to a multiple of 32 lanes x 4 floats
 constexpr int kStateHeader = 256; // floats reserved at the start of the state scratch
+// 128-row tiles of Xw per direction in the ring the tensor-core step kernel
+// uses when it computes the projection itself (16 MB per direction at
+// 4096 columns: it stays in L2)
+constexpr int kXwRingTiles = 8;
                                   // for the grid step kernel's barrier counters
 
 struct ActSlot {
@@ -68,6 +72,9 @@ struct StepParams {
   int step_ctas;       // blocks of the recurrence
   int pj_M, pj_K;      // X rows (S * N) and input size
   int pj_vec;          // float4 stores of Xw
+  int xw_ring;         // tensor-core kernel: Xw ring of this many 128-row tiles per direction (0: whole Xw)
+  int xw_consumers;    // warps that signal each step's Xw loads, per direction
+  unsigned* xw_done;   // [D]: Xw loads signalled (ring slots are reused once every warp is past them)
   int xw_groups;       // readiness counters per direction
   int xw_mpg;          // 128-row tiles of Xw per counter
   unsigned* xw_ready;  // [D][xw_groups]; 4 per (tile, 256 columns) stored

@@ -25,8 +25,10 @@ __global__ void __launch_bounds__(TTHREADS, 1)
     return make_int3(d, (rem / nt) * TBM, (rem % nt) * TBN);
   };
   auto no_signal = [](int, int) {};
+  auto whole = [](int, int m0) { return m0; };
+  auto always_free = [](int, int) { return true; };
   proj_tc_body(&tmA, &tmB, M, N, K, D, Xw, vec_store, status, timeout_ns, tsm, (int)blockIdx.x, (int)gridDim.x,
-               idesc, tile_of, no_signal);
+               idesc, tile_of, no_signal, whole, always_free);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link

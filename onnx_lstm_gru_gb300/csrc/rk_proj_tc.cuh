@@ -128,15 +128,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // The projection's work for one CTA: tiles pb, pb + np, ... of the
 // D * mt * nt tiles, tile_of(tile) giving its (direction, first row, first
 // column), signal(d, m0) called by lane 0 of each epilogue warp once its 32
-// rows of the tile are stored and fenced.  tsm: 1024-byte aligned shared
+// rows of the tile are stored and fenced.  The tile's rows go to rows
+// row_of(d, m0) ... of Xw[d] (m0 for the whole Xw; a ring slot otherwise),
+// after wait_free(d, m0) (called by lane 0 of each epilogue warp) has
+// returned true; false gives up.  tsm: 1024-byte aligned shared
 // memory of kTcSmem - 1024 bytes.  idesc: kIdescBase or-ed with the
 // element type's A/B fields.  Warps 0-5 take the roles; further warps of the
 // block only pass the block-wide barriers.
-template <class TileOf, class Signal>
+template <class TileOf, class Signal, class RowOf, class WaitFree>
 __device__ __forceinline__ void proj_tc_body(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K,
                                              int D, float* __restrict__ Xw, int vec_store, int* status,
                                              long long timeout_ns, unsigned char* tsm, int pb, int np,
-                                             uint32_t idesc, TileOf tile_of, Signal signal) {
+                                             uint32_t idesc, TileOf tile_of, Signal signal, RowOf row_of,
+                                             WaitFree wait_free) {
   unsigned char* sA = tsm;
   unsigned char* sB = tsm + TSTAGES * kStageBytesA;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + TSTAGES * kStageBytesB);
@@ -275,9 +279,16 @@ __device__ __forceinline__ void proj_tc_body(const CUtensorMap* tmA, const CUten
         give_up();
         break;
       }
+      int free_ok = 1;
+      if (lane == 0) free_ok = wait_free(d, m0) ? 1 : 0;
+      __syncwarp();  // lane 0's acquire is ordered before every lane's stores
+      if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+        give_up();
+        break;
+      }
       tc_fence_after();
       const int m = m0 + row;
-      float* orow = Xw + ((size_t)d * M + m) * N;
+      float* orow = Xw + ((size_t)d * M + row_of(d, m0) + row) * N;
 #pragma unroll 1
       for (int c0 = 0; c0 < TBN; c0 += 32) {
         uint32_t r[32];

@@ -242,6 +242,37 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // consumes them (128 rows = time steps, both directions interleaved), each
   // epilogue warp counting its stored rows into the tile's readiness counter
   const int pj_mt = (p.pj_M + ptc::TBM - 1) / ptc::TBM, pj_nt = (G * p.H + ptc::TBN - 1) / ptc::TBN;
+  // Xw through a ring of kXwRingTiles 128-row tiles per direction (it stays
+  // in L2) when every row has the same length L: both directions then read
+  // the tiles strictly one after another, in the order they are produced.
+  // Production index k of tile mi: mi forward, pj_mt - 1 - mi reverse; its
+  // rows go to ring slot k % ring.  The tile of production index k - ring
+  // must have been read by every warp before tile k overwrites it.
+  int ring = 0, ring_len = p.T;
+  if (MODE != 2 && p.fused && p.xw_ring > 0) {
+    bool uniform = true;
+    if (p.lens != nullptr) {
+      auto clamp_len = [&](int v) {
+        v = v < 0 ? 0 : (v > p.S ? p.S : v);
+        return v > p.T ? p.T : v;
+      };
+      ring_len = clamp_len(p.lens[0]);
+      for (int b = 1; b < p.N && uniform; ++b) uniform = clamp_len(p.lens[b]) == ring_len;
+    }
+    ring = uniform ? p.xw_ring : 0;
+  }
+  auto prod_index = [&](int dd, int mi) {
+    const bool rev = p.direction == 1 || (p.direction == 2 && dd == 1);
+    return rev ? pj_mt - 1 - mi : mi;
+  };
+  // the last step that reads a row of tile mi (-1: none), for length ring_len
+  auto last_step = [&](int dd, int mi) {
+    const bool rev = p.direction == 1 || (p.direction == 2 && dd == 1);
+    const int t_lo = (int)(((long long)mi * ptc::TBM) / p.N);
+    const int t_hi = (int)(((long long)(mi + 1) * ptc::TBM - 1) / p.N);
+    if (t_lo >= ring_len) return -1;
+    return rev ? ring_len - 1 - t_lo : (t_hi < ring_len - 1 ? t_hi : ring_len - 1);
+  };
   if constexpr (MODE != 2) {
     if (p.fused && (int)blockIdx.x >= p.step_ctas) {
       auto tile_of = [&](int tile) {
@@ -253,9 +284,31 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       auto signal = [&](int dd, int m0) {
         atomicAdd(p.xw_ready + (size_t)dd * p.xw_groups + (m0 / ptc::TBM) / p.xw_mpg, 1u);
       };
+      auto row_of = [&](int dd, int m0) {
+        return ring ? (prod_index(dd, m0 / ptc::TBM) % ring) * ptc::TBM : m0;
+      };
+      // the slot's previous tile must have been read by every warp of the
+      // direction: each warp counts one per step whose Xw it has loaded
+      auto wait_free = [&](int dd, int m0) -> bool {
+        if (!ring) return true;
+        const int k = prod_index(dd, m0 / ptc::TBM);
+        if (k < ring) return true;
+        const int kp = k - ring;
+        const bool rev = p.direction == 1 || (p.direction == 2 && dd == 1);
+        const int sl = last_step(dd, rev ? pj_mt - 1 - kp : kp);
+        if (sl < 0) return true;
+        const unsigned target = (unsigned)(sl + 1) * (unsigned)p.xw_consumers;
+        const unsigned* cnt = p.xw_done + dd;
+        if (ld_acquire_gpu(cnt) >= target) return true;
+        const unsigned long long t0 = global_ns();
+        for (unsigned it = 1;; ++it) {
+          if (ld_acquire_gpu(cnt) >= target) return true;
+          if ((it & 15u) == 0 && (long long)(global_ns() - t0) > p.timeout_ns) return false;
+        }
+      };
       ptc::proj_tc_body(&tmA, &tmB, p.pj_M, G * p.H, p.pj_K, p.D, const_cast<float*>(p.xw), p.pj_vec, p.status,
                         p.timeout_ns, base, (int)blockIdx.x - p.step_ctas, (int)gridDim.x - p.step_ctas,
-                        ptc::kIdescBase | Elem<E>::kMmaAB, tile_of, signal);
+                        ptc::kIdescBase | Elem<E>::kMmaAB, tile_of, signal, row_of, wait_free);
       return;
     }
   }
@@ -475,6 +528,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
     bool on = grow && s < len && s < Tn;
     const int tt = reverse ? len - 1 - s : s;
     const float* qx = xw_row + (size_t)tt * xw_tstride;
+    if (ring && on) {
+      // the row's place in its tile's ring slot (layout 0: row tt * N + bg)
+      const int m = tt * N + bg, mi = m / ptc::TBM;
+      qx = p.xw + ((size_t)d * p.pj_M + (size_t)(prod_index(d, mi) % ring) * ptc::TBM + (m % ptc::TBM)) * GH;
+    }
     if (MODE != 2 && p.fused && on) {
       // the blocks computing the projection must have stored this row's
       // 128-row tile of Xw for every column (layout 0: row tt * N + bg)
@@ -678,7 +736,14 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   } else {
     // ---------------- gate warps
     float xv[UH * G];
+    // with the Xw ring: each warp counts one per step whose Xw it has loaded
+    auto xw_loaded = [&]() {
+      if (!ring) return;
+      __syncwarp();
+      if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.xw_done + d) : "memory");
+    };
     load_xw(0, xv);
+    xw_loaded();
     bool ok = true;
     // columns of this warp-half's units (w / 4) * SJT / 2 ... of its 32 lanes;
     // without PAIR the thread's own units
@@ -784,6 +849,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
         }
       }
       load_xw(s + 1, xv);
+      xw_loaded();
     }
     if (!ok) {
       abort_flag = 1;

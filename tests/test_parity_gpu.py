@@ -421,6 +421,58 @@ def test_fused_projection_matches_separate(cell, H, N, direction, dtype):
     compare(pr, got, run_oracle(pr, inp), lens)
 
 
+XW_RING_CASES = [
+    # (cell, S, N, H, direction, lengths): 128-row tiles of Xw per direction > 16
+    ("lstm", 40, 64, 576, "bidirectional", "uniform"),   # every row 37 steps: ring
+    ("gru", 60, 40, 640, "reverse", None),                # no lengths: ring
+    ("rnn", 36, 72, 1024, "forward", "uniform"),
+    ("lstm", 40, 64, 576, "bidirectional", "varied"),    # rows of different lengths: whole Xw
+]
+
+
+@pytest.mark.parametrize("cell,S,N,H,direction,lens_kind", XW_RING_CASES)
+def test_fused_projection_xw_ring(cell, S, N, H, direction, lens_kind):
+    """Long layers whose projection runs inside the tensor-core step launch
+    keep Xw in a ring of 8 128-row tiles per direction (it stays in L2) when
+    every row has the same length: a tile is overwritten only after every
+    gate warp of its direction has loaded the steps that read it.  Same tile
+    arithmetic as the projection's own launch: bit-identical outputs; the
+    oracle's within tolerance on sampled batch rows."""
+    pr = rk.Problem(cell, seq=S, batch=N, input=72, hidden=H, direction=direction, dtype="f16",
+                    linear_before_reset=1 if cell == "gru" else 0)
+    assert "proj=fused step=tensor" in layer().plan(pr)
+    rng = np.random.default_rng(S * N + H)
+    lens = None
+    if lens_kind == "uniform":
+        lens = [S - 3] * N
+    elif lens_kind == "varied":
+        lens = list(rng.integers(0, S + 1, N))
+    # weights of scale 0.04: recurrent gain about 0.04 * sqrt(H / 3) < 1, so
+    # 40 steps of Half rounding stay far inside the tolerance (a chaotic
+    # layer would amplify them past any fixed bound)
+    inp = rand_inputs(pr, seed=H + N, lens=lens, scale=0.04)
+    got = run_gpu(pr, inp)
+    sep = run_gpu(pr, inp, flags=rk.RK_SEPARATE_PROJECTION)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], sep[k]), k
+    rows = [0, N // 3, N - 1]
+    sub = rk.Problem(cell, seq=S, batch=len(rows), input=72, hidden=H, direction=direction, dtype="f16",
+                     linear_before_reset=pr.linear_before_reset)
+    sinp = {k: v for k, v in inp.items()}
+    sinp["X"] = inp["X"][:, rows]
+    if lens is not None:
+        sinp["sequence_lens"] = inp["sequence_lens"][rows]
+    for k in ("initial_h", "initial_c"):
+        if k in sinp:
+            sinp[k] = inp[k][:, rows]
+    ref = run_oracle(sub, sinp)
+    gsub = {"Y": got["Y"][:, :, rows], "Y_h": got["Y_h"][:, rows]}
+    if "Y_c" in got:
+        gsub["Y_c"] = got["Y_c"][:, rows]
+    compare(sub, gsub, ref, sinp.get("sequence_lens"))
+
+
 @pytest.mark.parametrize("H,N,direction,layout,opts", [(40, 4, "bidirectional", 0, "plain"),
                                                      (96, 9, "reverse", 1, "full"),
                                                      (200, 16, "forward", 0, "full"),
