@@ -478,9 +478,7 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
     const int nb = std::min(N, 64);
     pl.nb = nb;
     pl.teams_per_dir = (N + nb - 1) / nb;
-    pl.shape = nb <= 4 ? rk::kShapeR8B4 : rk::kShapeR4B8;
     pl.nbc = nb <= 4 ? 4 : 8;
-    const int rpw = nb <= 4 ? 8 : 4;
     const int teams = D * pl.teams_per_dir;
     if (teams > rk::kStateHeader)
       return fail(h, RK_ERR_UNSUPPORTED, "%s: batch %d needs too many grid teams", cell_name(p->cell), N);
@@ -489,6 +487,10 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
       return fail(h, RK_ERR_UNSUPPORTED, "%s: %d teams exceed %d SMs", cell_name(p->cell), teams, h->sms);
     pl.J = (H + per_team - 1) / per_team;
     pl.team_ctas = (H + pl.J - 1) / pl.J;
+    // up to 4 batch rows: 8-row register tiles, or 4-row ones when 8-row
+    // tiles would leave warps of a 256-thread block without rows
+    pl.shape = nb <= 4 ? (G * round_up(pl.J, 8) / 8 < 8 ? rk::kShapeR4B4 : rk::kShapeR8B4) : rk::kShapeR4B8;
+    const int rpw = pl.shape == rk::kShapeR8B4 ? 8 : 4;
     const int Jp = (int)round_up(pl.J, rpw);
     pl.rows_pad = G * Jp;
     pl.threads = (int)std::min<int64_t>(768, std::max<int64_t>(256, 32 * (pl.rows_pad / rpw)));

@@ -35,6 +35,7 @@ enum StepShape : int {
   kShapeR8B1 = 0,  // 8 rows x 1 batch row
   kShapeR4B8 = 1,  // 4 rows x 8 batch rows
   kShapeR8B4 = 2,  // 8 rows x 4 batch rows
+  kShapeR4B4 = 3,  // 4 rows x 4 batch rows (grid kernel: twice the warps of R8B4 on few rows)
 };
 
 struct StepParams {

@@ -66,6 +66,9 @@ cudaError_t step_launch_shape(const StepParams& p, const StepPlan& plan, cudaStr
     case kShapeR8B4:
       if constexpr (GRID) return step_launch_one<CELL, T, GEN, 8, 4, GRID>(p, plan, s, q);
       break;
+    case kShapeR4B4:
+      if constexpr (GRID) return step_launch_one<CELL, T, GEN, 4, 4, GRID>(p, plan, s, q);
+      break;
   }
   return cudaErrorInvalidConfiguration;
 }
