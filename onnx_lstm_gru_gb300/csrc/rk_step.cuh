@@ -111,6 +111,14 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 
 // Wait for an mbarrier phase with a deadline.  Returns false on timeout.
+// One contiguous global -> shared copy on the async proxy (16-byte aligned
+// addresses, size a multiple of 16), counted on mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -466,6 +474,13 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
         const int bl = e / Jc, jl = e % Jc;
         p.hglob[((size_t)d * p.N + b0 + bl) * KP + j0 + jl] = hown[bl * J + jl];
       }
+      // staged rows are copied in whole (H columns each): the columns past
+      // H stay zero from here on (the grid kernel stages h and r.h alike in
+      // its one chunk buffer hs)
+      for (size_t e = tid; e < (size_t)NBC * KP; e += NT) hs[e] = 0.0f;
+      if (tid == 0) mbar_init(smem_u32(&bars[0]), 1);  // staged rows landed
+      // the exchange buffer is written by ordinary stores and read by bulk copies
+      asm volatile("fence.proxy.async.global;" ::: "memory");
     }
   }
 
@@ -475,8 +490,30 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
     alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
   }
 
-  // Stage the batch rows [c0, c0 + NBC) of a global exchange buffer (grid kernel).
-  auto load_chunk = [&](const float* src, int c0) {
+  // Stage the batch rows [c0, c0 + NBC) of a global exchange buffer (grid
+  // kernel): one bulk copy of H floats per row when rows are a whole number
+  // of 16 bytes (rows past the team's batch keep stale values whose sums no
+  // gate reads), else element loads.
+  const bool bulk_rows = (H % 4) == 0;
+  uint32_t stage_phase = 0;
+  auto load_chunk = [&](const float* src, int c0) -> bool {
+    if (bulk_rows) {
+      const int nrows = min(NBC, nbt - c0);
+      if (tid == 0) {
+        // the writers' ordinary stores, acquired by the team barrier, are
+        // read by the async proxy; this block's reads of the previous rows
+        // come before the async proxy rewrites them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(smem_u32(&bars[0]), (uint32_t)nrows * (uint32_t)H * 4u);
+        for (int bl = 0; bl < nrows; ++bl)
+          bulk_copy_g2s(smem_u32(hs + (size_t)bl * KP), src + ((size_t)d * p.N + b0 + c0 + bl) * KP, (uint32_t)H * 4u,
+                        smem_u32(&bars[0]));
+      }
+      const bool ok = mbar_wait_bounded(smem_u32(&bars[0]), stage_phase & 1u, p.timeout_ns);
+      ++stage_phase;
+      return ok;
+    }
     const int nk4 = KP / 4;
     for (int e = tid; e < NBC * nk4; e += NT) {
       const int bl = e / nk4, k = (e % nk4) * 4;
@@ -493,6 +530,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
       }
       *reinterpret_cast<float4*>(hs + (size_t)bl * KP + k) = v;
     }
+    return true;
   };
 
   // Row sums for rows [row0, row0 + nrows) against the current h (or r.h).
@@ -501,7 +539,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
       matvec<RPW, NBC, T>(Rs, KP, row0, nrows, cluster_src, gs, NBC, 0, warp, nwarps, lane);
     } else {
       for (int c0 = 0; c0 < nbt; c0 += NBC) {
-        load_chunk(global_src, c0);
+        if (!load_chunk(global_src, c0) && tid == 0) atomicOr(p.status, 1);  // the barriers after it still pass
         __syncthreads();
         matvec<RPW, NBC, T>(Rs, KP, row0, nrows, hs, gs, nb_ld, c0, warp, nwarps, lane);
         __syncthreads();
@@ -605,6 +643,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
         }
       }
       if constexpr (GRID) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // r.h is read by bulk copies
         alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
         if (!alive) break;
       } else {
@@ -687,6 +726,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
     }
     if (s + 1 < p.T) {
       if constexpr (GRID) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read by bulk copies
         alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
       } else {
         __syncthreads();
