@@ -138,12 +138,13 @@ cudaError_t noalloc_scratch(float** scratch, int** status);
 // cluster) and a ring of `stages` 16 KB stages; the most stages (2..8) that
 // fit in smem_cap bytes (0 if not even 2 fit); and the launch (resident !=
 // nullptr: occupancy query only: co-resident teams, or clusters for a
-// cluster team).  h16 is the Half copy of the exchanged hidden state,
-// 2 x D x teams x 16 KB regions per 128 k.
+// cluster team).  h16 is the 16-bit copy of the exchanged hidden state,
+// 2 x D x teams x 16 KB regions per 128 k (in the state scratch).
 size_t step_tc_smem(int G, int H, int stages, int units);
 // Small-batch variant (at most 16 rows per direction, one cluster of
 // ceil(H / 32) CTAs per direction; plans it with nbc = 16): dynamic shared
-// memory and the launch, same contract as step_tc_entry.
+// memory and the launch, same contract as step_tc_entry (its exchanged h
+// stays in the CTAs' shared memory: h16 is not used).
 size_t step_tcs_smem(int G, int H);
 cudaError_t step_tcs_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 int step_tc_stages(int G, int H, int units, size_t smem_cap);
