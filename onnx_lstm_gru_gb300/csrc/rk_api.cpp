@@ -16,6 +16,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <iterator>
 #include <string>
 
 #include "rk.h"
@@ -40,6 +41,22 @@ struct rk_handle {
   bool profiling = false;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // proj start/end, step start/end
   bool ev_proj = false, ev_step = false;
+  // rk_encode_host: a second stream copies the operands only the step kernel
+  // reads while the first copies X and W and runs the projection
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_ev[2] = {nullptr, nullptr};  // fork from the caller's stream, join before the step
+  // Plans of the last problems encoded (the planner's occupancy queries cost
+  // more host time than a small layer takes on the GPU)
+  struct PlanEntry {
+    bool valid = false;
+    rk_problem key;
+    uint32_t flags = 0;
+    int device = -1;
+    rk::StepParams sp;
+    rk::StepPlan pl;
+  };
+  PlanEntry plans[4];
+  int plan_next = 0;
 };
 
 namespace {
@@ -291,7 +308,7 @@ cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl
 // else the cluster kernel when R fits one cluster's shared memory; else the
 // grid kernel.  RK_PREFER_TENSOR_STEP puts the tensor-core kernels first.
 // `check` asks the occupancy API (needs a device).
-rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
+rk_status plan_step_uncached(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
   const int G = sp->G, D = sp->D, N = sp->N, H = sp->H, KP = sp->KP;
   const int eb = p->dtype == RK_F32 ? 4 : 2;
   const bool lbr0 = p->cell == RK_GRU && !p->linear_before_reset;
@@ -509,6 +526,56 @@ rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan*
   }
 }
 
+// The problem's fields alone (no padding bytes, which the caller may leave
+// uninitialised), for comparing problems byte by byte.
+rk_problem plan_key(const rk_problem* p) {
+  rk_problem k;
+  std::memset(&k, 0, sizeof(k));
+  k.cell = p->cell;
+  k.direction = p->direction;
+  k.dtype = p->dtype;
+  k.layout = p->layout;
+  k.seq = p->seq;
+  k.batch = p->batch;
+  k.input = p->input;
+  k.hidden = p->hidden;
+  k.clip = p->clip;
+  k.input_forget = p->input_forget;
+  k.linear_before_reset = p->linear_before_reset;
+  k.num_acts = p->num_acts;
+  for (int i = 0; i < 6; ++i) k.act[i] = p->act[i];
+  k.max_length = p->max_length;
+  return k;
+}
+
+// plan_step_uncached, remembered per handle: with check set the plan of a
+// problem depends only on its fields, the handle's flags and the device, so
+// a problem seen before takes its plan (and the step parameters the planner
+// filled) from the handle instead of repeating the occupancy queries.
+rk_status plan_step(rk_handle* h, const rk_problem* p, StepParams* sp, StepPlan* out, bool check) {
+  if (!check) return plan_step_uncached(h, p, sp, out, check);
+  const rk_problem key = plan_key(p);
+  for (const auto& e : h->plans) {
+    if (e.valid && e.flags == h->flags && e.device == h->device && std::memcmp(&e.key, &key, sizeof(key)) == 0) {
+      *sp = e.sp;
+      *out = e.pl;
+      return RK_OK;
+    }
+  }
+  const rk_status st = plan_step_uncached(h, p, sp, out, check);
+  if (st == RK_OK) {
+    auto& e = h->plans[h->plan_next];
+    h->plan_next = (h->plan_next + 1) % 4;
+    e.valid = true;
+    e.key = key;
+    e.flags = h->flags;
+    e.device = h->device;
+    e.sp = *sp;
+    e.pl = *out;
+  }
+  return st;
+}
+
 rk_status cuda_fail(rk_handle* h, const rk_problem* p, const char* what, cudaError_t e) {
   return fail(h, RK_ERR_CUDA, "%s: %s: %s (%s)", cell_name(p->cell), what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
@@ -560,6 +627,9 @@ rk_status rk_destroy(rk_handle* h) {
     cudaDeviceSynchronize();
     for (auto& ev : h->ev)
       if (ev) cudaEventDestroy(ev);
+    for (auto& ev : h->copy_ev)
+      if (ev) cudaEventDestroy(ev);
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
     cudaFree(h->status);
     cudaFree(h->xw);
     cudaFree(h->state);
@@ -622,15 +692,14 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
   return RK_OK;
 }
 
-rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, const rk_scratch* scratch,
-                    void* stream_ptr) {
-  if (h == nullptr) return RK_ERR_ARG;
-  h->last_error.clear();
-  rk_status st = validate_all(h, p, ops);
-  if (st != RK_OK) return st;
-  if (p->batch == 0 || p->hidden == 0) return RK_OK;  // nothing is recorded
-  if ((st = ensure_device(h)) != RK_OK) return st;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+namespace {
+
+// The layer on validated operands.  step_wait != nullptr: the stream waits
+// for that event just before the step kernel's launch (the host entry's
+// copies of the operands only the step kernel reads).
+rk_status encode_validated(rk_handle* h, const rk_problem* p, const rk_operands* ops, const rk_scratch* scratch,
+                           cudaStream_t stream, cudaEvent_t step_wait) {
+  rk_status st;
   const int eb = p->dtype == RK_F32 ? 4 : 2;
 
   StepParams sp;
@@ -712,6 +781,10 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
     cudaError_t e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
   }
+  if (step_wait != nullptr) {
+    cudaError_t e = cudaStreamWaitEvent(stream, step_wait, 0);
+    if (e != cudaSuccess) return cuda_fail(h, p, "wait for the operand copies", e);
+  }
   if (h->profiling) cudaEventRecord(h->ev[2], stream);
   cudaError_t e;
   if (fz.on) {
@@ -751,6 +824,19 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, c
   return RK_OK;
 }
 
+}  // namespace
+
+rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops, const rk_scratch* scratch,
+                    void* stream_ptr) {
+  if (h == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  rk_status st = validate_all(h, p, ops);
+  if (st != RK_OK) return st;
+  if (p->batch == 0 || p->hidden == 0) return RK_OK;  // nothing is recorded
+  if ((st = ensure_device(h)) != RK_OK) return st;
+  return encode_validated(h, p, ops, scratch, static_cast<cudaStream_t>(stream_ptr), nullptr);
+}
+
 // The layer with its scratch in the library's fixed device array instead of
 // memory from cudaMalloc, for callers that cannot allocate (see rk.h).
 rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands* ops, void* stream_ptr) {
@@ -779,10 +865,16 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan_h.sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan_h.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return cuda_fail(h, p, "device query", e);
+  plan_h.device = dev;
+  std::copy(std::begin(h->plans), std::end(h->plans), std::begin(plan_h.plans));
+  plan_h.plan_next = h->plan_next;
   StepParams sp;
   fill_params_problem(p, &sp);
   StepPlan pl{};
-  if ((st = plan_step(&plan_h, p, &sp, &pl, true)) != RK_OK) {
+  st = plan_step(&plan_h, p, &sp, &pl, true);
+  std::copy(std::begin(plan_h.plans), std::end(plan_h.plans), std::begin(h->plans));
+  h->plan_next = plan_h.plan_next;
+  if (st != RK_OK) {
     h->last_error = plan_h.last_error;
     return st;
   }
@@ -917,6 +1009,18 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
     }
     h->host_arena_cap = total;
   }
+  if (h->copy_stream == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&h->copy_ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(h, p, "copy stream set-up", e);
+  }
+  // X and W (the projection's operands) on the caller's stream; R, B, the
+  // lengths, initial states and P on the copy stream, forked after the
+  // caller's earlier work and joined just before the step kernel, so they
+  // land while the projection runs
+  cudaError_t e = cudaEventRecord(h->copy_ev[0], stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_stream, h->copy_ev[0], 0);
+  if (e != cudaSuccess) return cuda_fail(h, p, "copy stream fork", e);
   for (int i = 0; i < 11; ++i) {
     if (!items[i].src->ptr) continue;
     const int elem = (i == 4) ? 4 : eb;
@@ -925,18 +1029,29 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
     items[i].dst->length = items[i].bytes / elem;
     if (items[i].input && items[i].bytes > 0) {
       const char* src = static_cast<const char*>(items[i].src->ptr) + items[i].src->offset * elem;
-      cudaError_t e = cudaMemcpyAsync(items[i].dst->ptr, src, (size_t)items[i].bytes, cudaMemcpyHostToDevice, stream);
-      if (e != cudaSuccess) return cuda_fail(h, p, "host-to-device copy", e);
+      e = cudaMemcpyAsync(items[i].dst->ptr, src, (size_t)items[i].bytes, cudaMemcpyHostToDevice,
+                          i < 2 ? stream : h->copy_stream);
+      if (e != cudaSuccess) break;
     }
   }
-  if ((st = rk_encode(h, p, &dev, nullptr, stream_ptr)) != RK_OK) return st;
+  cudaError_t j = cudaEventRecord(h->copy_ev[1], h->copy_stream);
+  if (e != cudaSuccess || j != cudaSuccess) {
+    if (j == cudaSuccess) cudaStreamWaitEvent(stream, h->copy_ev[1], 0);
+    return cuda_fail(h, p, "host-to-device copy", e != cudaSuccess ? e : j);
+  }
+  st = validate_all(h, p, &dev);
+  if (st == RK_OK) st = encode_validated(h, p, &dev, nullptr, stream, h->copy_ev[1]);
+  if (st != RK_OK) {
+    cudaStreamWaitEvent(stream, h->copy_ev[1], 0);  // nothing of the copy stream outlives the call
+    return st;
+  }
   for (int i = 8; i < 11; ++i) {
     if (!items[i].src->ptr || items[i].bytes == 0) continue;
     char* dstp = static_cast<char*>(items[i].src->ptr) + items[i].src->offset * eb;
-    cudaError_t e = cudaMemcpyAsync(dstp, items[i].dst->ptr, (size_t)items[i].bytes, cudaMemcpyDeviceToHost, stream);
+    e = cudaMemcpyAsync(dstp, items[i].dst->ptr, (size_t)items[i].bytes, cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "device-to-host copy", e);
   }
-  cudaError_t e = cudaStreamSynchronize(stream);
+  e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(h, p, "stream synchronize", e);
   return RK_OK;
 }

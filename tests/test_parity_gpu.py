@@ -551,6 +551,49 @@ def test_host_buffer_entry_bfloat16():
         assert torch.equal(t.reshape(-1), dev[n + "_raw"].cpu()), n
 
 
+def test_host_entry_planner_memory_round_robin():
+    """One handle encodes six different layers twice in turn through the host
+    entry (more problems than the handle remembers plans for, so plans are
+    both recalled and recomputed), on a stream of its own with pinned host
+    buffers: every result has the device entry's bits on a fresh handle."""
+    cases = [
+        (rk.Problem("lstm", seq=9, batch=3, input=5, hidden=24), dict(peep=True)),
+        (rk.Problem("gru", direction="bidirectional", seq=7, batch=2, input=8, hidden=40, linear_before_reset=1), {}),
+        (rk.Problem("rnn", direction="reverse", seq=11, batch=5, input=3, hidden=17), {}),
+        (rk.Problem("gru", direction="bidirectional", seq=6, batch=4, input=16, hidden=64, dtype="f16"), {}),
+        (rk.Problem("lstm", direction="bidirectional", seq=5, batch=2, input=8, hidden=32, dtype="bf16",
+                    clip=2.0), {}),
+        (rk.Problem("lstm", seq=4, batch=9, input=6, hidden=300), dict(lens=[4, 1, 3, 0, 2, 4, 4, 1, 2])),
+    ]
+    L = rk.RecurrentLayer()
+    stream = torch.cuda.Stream()
+    want, ins = [], []
+    for i, (pr, kw) in enumerate(cases):
+        inp = rand_inputs(pr, seed=40 + i, **kw)
+        fresh = rk.RecurrentLayer()
+        dt = torch_dtype(pr)
+        shp = pr.shapes()
+        args = {k: (torch.from_numpy(v).cuda() if k == "sequence_lens" else torch.from_numpy(v).to(dt).cuda())
+                for k, v in inp.items()}
+        outs = {n: torch.zeros(shp[n], dtype=dt, device="cuda") for n in ("Y", "Y_h")}
+        fresh.encode(pr, **args, **outs)
+        torch.cuda.synchronize()
+        fresh.poll()
+        fresh.close()
+        want.append({n: t.cpu() for n, t in outs.items()})
+        ins.append({k: (torch.from_numpy(v) if k == "sequence_lens" else torch.from_numpy(v).to(dt)).pin_memory()
+                    for k, v in inp.items()})
+    for rnd in range(2):
+        for i, (pr, _) in enumerate(cases):
+            shp = pr.shapes()
+            outs = {n: torch.full(shp[n], 9.0, dtype=torch_dtype(pr)).pin_memory() for n in ("Y", "Y_h")}
+            L.encode_host(pr, stream=stream, **ins[i], **outs)
+            for n, t in outs.items():
+                assert torch.equal(t, want[i][n]), (rnd, i, n)
+    L.poll()
+    L.close()
+
+
 def test_bounded_wait_gives_up_and_context_survives():
     L = rk.RecurrentLayer()
     s = torch.cuda.current_stream()
