@@ -91,15 +91,24 @@ __global__ void __launch_bounds__(256) proj_simt_kernel(int M, int N, int K, con
 
 // ---------------------------------------------------------------------------
 // Pipelined variant for 16-byte aligned operands (X and W bases 16-byte
-// aligned, K * element size a multiple of 16): 4 stages of 32-deep k tiles
+// aligned, K * element size a multiple of 16): NST stages of 32-deep k tiles
 // are kept in flight with cp.async (16-byte copies, zero-filled past M, N
 // and K), so the loads of later tiles overlap the arithmetic of earlier ones.
-// Tiles are PBM x 64 (PBM = 8, 16, 24 or 32) of Xw per 128-thread CTA;
-// thread (tm, tn) owns rows tm + 8 i and columns tn + 16 j (strided, so the
-// 16-byte shared loads of a quarter warp hit distinct banks and the stores
-// are coalesced).  Each output is still one fused-multiply-add chain in
-// increasing k, whatever the tile height.
-constexpr int PBN = 64, PBK = 32, PSTAGES = 4, PTHREADS = 128;
+// Tiles are PBM x 64 (PBM = 8, 16, 24 or 32) of Xw per CTA, in one of two
+// thread layouts:
+//  - rows (grids of several tiles per SM): 128 threads, thread (tm, tn) owns
+//    rows tm + 8 i and columns tn + 16 j, j < 4 (small CTAs, several per SM,
+//    4 stages);
+//  - columns (grids of at most one tile per SM): 256 threads, warp w owns
+//    columns 8 w ... 8 w + 7 and lane l column 8 w + l % 8 and rows
+//    l / 8 + 4 i (8 warps per SM, 6 stages).  A warp's 16-byte shared loads
+//    then touch 4 rows of X and 8 rows of W, one wavefront each, so shared
+//    memory feeds twice the products per wavefront of a one-column-per-thread
+//    layout with the same warp count (which was bound by shared-load
+//    wavefronts).
+// Either way the 16-byte loads of a quarter warp hit distinct banks, and each
+// output is one fused-multiply-add chain in increasing k.
+constexpr int PBN = 64, PBK = 32;
 
 template <typename T>
 struct PipeElem {
@@ -125,29 +134,43 @@ __device__ __forceinline__ float4 load4_row<float>(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
-template <typename T, int PBM>
-__global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K, const T* __restrict__ X,
-                                                             const T* __restrict__ W, float* __restrict__ Xw) {
+template <bool COLS>
+struct PipeLayout {
+  static constexpr int threads = COLS ? 256 : 128;
+  static constexpr int row_step = COLS ? 4 : 8;  // rows of a thread are r0 + row_step * i
+  static constexpr int cols = COLS ? 1 : 4;      // columns per thread
+};
+
+template <typename T, int PBM, bool COLS, int NST>
+__global__ void __launch_bounds__(PipeLayout<COLS>::threads) proj_pipe_kernel(int M, int N, int K, const T* __restrict__ X,
+                                                                            const T* __restrict__ W, float* __restrict__ Xw) {
   static_assert(PBM % 8 == 0 && PBM >= 8 && PBM <= 32, "tile rows: 8 to 32 in steps of 8");
+  static_assert(NST >= 2, "at least two stages");
   // the step kernel after this one may be launched early (programmatic
   // dependent launch); it waits for this grid before reading Xw
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  using Lay = PipeLayout<COLS>;
+  constexpr int THREADS = Lay::threads, CN = Lay::cols, RS = Lay::row_step;
   constexpr int E = PipeElem<T>::per16, LD = PipeElem<T>::ld;
-  constexpr int RM = PBM / 8;  // rows per thread
+  constexpr int RM = PBM / RS;  // rows per thread
   extern __shared__ __align__(16) unsigned char psm[];
-  T* As = reinterpret_cast<T*>(psm);                    // [PSTAGES][PBM][LD]
-  T* Bs = As + (size_t)PSTAGES * PBM * LD;              // [PSTAGES][PBN][LD]
+  T* As = reinterpret_cast<T*>(psm);                    // [NST][PBM][LD]
+  T* Bs = As + (size_t)NST * PBM * LD;                  // [NST][PBN][LD]
   const int d = blockIdx.z;
   const int m0 = blockIdx.y * PBM, n0 = blockIdx.x * PBN;
-  const int tid = threadIdx.x, tn = tid & 15, tm = tid >> 4;
+  const int tid = threadIdx.x;
+  // first row and column of this thread, and the stride between its columns
+  const int tm = COLS ? (tid & 31) >> 3 : tid >> 4;
+  const int tn = COLS ? (tid >> 5) * 8 + (tid & 7) : tid & 15;
+  constexpr int CS = 16;
   const T* Wd = W + (size_t)d * N * K;
   const int KT = (K + PBK - 1) / PBK;
   constexpr int CPR = PBK / E;                          // 16-byte chunks per tile row
   constexpr int A_CH = PBM * CPR, B_CH = PBN * CPR;
 
   auto issue = [&](int kt) {
-    const int st = kt % PSTAGES, k0 = kt * PBK;
-    for (int c = tid; c < A_CH + B_CH; c += PTHREADS) {
+    const int st = kt % NST, k0 = kt * PBK;
+    for (int c = tid; c < A_CH + B_CH; c += THREADS) {
       const bool isA = c < A_CH;
       const int cc = isA ? c : c - A_CH;
       const int r = cc / CPR, kc = (cc % CPR) * E;
@@ -159,36 +182,36 @@ __global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K
     }
   };
 
-  float acc[RM][4];
+  float acc[RM][CN];
 #pragma unroll
   for (int i = 0; i < RM; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int j = 0; j < CN; ++j) acc[i][j] = 0.0f;
 
 #pragma unroll
-  for (int s = 0; s < PSTAGES - 1; ++s) {
+  for (int s = 0; s < NST - 1; ++s) {
     if (s < KT) issue(s);
     cp_async_commit();
   }
   for (int kt = 0; kt < KT; ++kt) {
-    cp_async_wait<PSTAGES - 2>();
+    cp_async_wait<NST - 2>();
     __syncthreads();
-    if (kt + PSTAGES - 1 < KT) issue(kt + PSTAGES - 1);
+    if (kt + NST - 1 < KT) issue(kt + NST - 1);
     cp_async_commit();
-    const int st = kt % PSTAGES;
+    const int st = kt % NST;
     const T* a = As + (size_t)st * PBM * LD;
     const T* b = Bs + (size_t)st * PBN * LD;
 #pragma unroll
     for (int kk = 0; kk < PBK; kk += 4) {
-      float4 av[RM], bv[4];
+      float4 av[RM], bv[CN];
 #pragma unroll
-      for (int i = 0; i < RM; ++i) av[i] = load4_row<T>(a + (size_t)(tm + 8 * i) * LD + kk);
+      for (int i = 0; i < RM; ++i) av[i] = load4_row<T>(a + (size_t)(tm + RS * i) * LD + kk);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = load4_row<T>(b + (size_t)(tn + 16 * j) * LD + kk);
+      for (int j = 0; j < CN; ++j) bv[j] = load4_row<T>(b + (size_t)(tn + CS * j) * LD + kk);
 #pragma unroll
       for (int i = 0; i < RM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < CN; ++j) {
           float x = acc[i][j];
           x = fmaf(av[i].x, bv[j].x, x);
           x = fmaf(av[i].y, bv[j].y, x);
@@ -202,36 +225,42 @@ __global__ void __launch_bounds__(PTHREADS) proj_pipe_kernel(int M, int N, int K
   float* out = Xw + (size_t)d * M * N;
 #pragma unroll
   for (int i = 0; i < RM; ++i) {
-    const int m = m0 + tm + 8 * i;
+    const int m = m0 + tm + RS * i;
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tn + 16 * j;
+    for (int j = 0; j < CN; ++j) {
+      const int n = n0 + tn + CS * j;
       if (n < N) out[(size_t)m * N + n] = acc[i][j];
     }
   }
 }
 
-template <typename T, int PBM>
+template <typename T, int PBM, bool COLS, int NST>
 cudaError_t launch_pipe(const ProjParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)PSTAGES * (PBM + PBN) * PipeElem<T>::ld * sizeof(T);
-  auto kern = proj_pipe_kernel<T, PBM>;
+  const size_t smem = (size_t)NST * (PBM + PBN) * PipeElem<T>::ld * sizeof(T);
+  auto kern = proj_pipe_kernel<T, PBM, COLS, NST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((p.N + PBN - 1) / PBN), (unsigned)((p.M + PBM - 1) / PBM), (unsigned)p.D);
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-  kern<<<grid, PTHREADS, smem, s>>>(p.M, p.N, p.K, static_cast<const T*>(p.X), static_cast<const T*>(p.W), p.Xw);
+  kern<<<grid, PipeLayout<COLS>::threads, smem, s>>>(p.M, p.N, p.K, static_cast<const T*>(p.X),
+                                                     static_cast<const T*>(p.W), p.Xw);
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool COLS, int NST>
 cudaError_t launch_pipe_rows(const ProjParams& p, cudaStream_t s, int rows) {
   switch (rows) {
-    case 8: return launch_pipe<T, 8>(p, s);
-    case 16: return launch_pipe<T, 16>(p, s);
-    case 24: return launch_pipe<T, 24>(p, s);
-    default: return launch_pipe<T, 32>(p, s);
+    case 8: return launch_pipe<T, 8, COLS, NST>(p, s);
+    case 16: return launch_pipe<T, 16, COLS, NST>(p, s);
+    case 24: return launch_pipe<T, 24, COLS, NST>(p, s);
+    default: return launch_pipe<T, 32, COLS, NST>(p, s);
   }
+}
+
+template <typename T>
+cudaError_t launch_pipe_for(const ProjParams& p, cudaStream_t s, int rows, bool one_wave) {
+  return one_wave ? launch_pipe_rows<T, true, 6>(p, s, rows) : launch_pipe_rows<T, false, 4>(p, s, rows);
 }
 
 // Tile height: the SM that gets the most tiles sets the time, so take the
@@ -263,10 +292,12 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   if (aligned) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int rows = pipe_rows_for(p.M, (long long)((p.N + PBN - 1) / PBN) * p.D, sms);
-    if (p.dtype == 0) return launch_pipe_rows<float>(p, s, rows);
-    if (p.dtype == 2) return launch_pipe_rows<__nv_bfloat16>(p, s, rows);
-    return launch_pipe_rows<__half>(p, s, rows);
+    const long long col_tiles = (long long)((p.N + PBN - 1) / PBN) * p.D;
+    const int rows = pipe_rows_for(p.M, col_tiles, sms);
+    const bool one_wave = col_tiles * ((p.M + rows - 1) / rows) <= sms;
+    if (p.dtype == 0) return launch_pipe_for<float>(p, s, rows, one_wave);
+    if (p.dtype == 2) return launch_pipe_for<__nv_bfloat16>(p, s, rows, one_wave);
+    return launch_pipe_for<__half>(p, s, rows, one_wave);
   }
   dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.D);
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
