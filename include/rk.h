@@ -187,7 +187,14 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops,
 
 /* Same layer with HOST operand pointers: copies the inputs to device buffers
  * owned by the handle (grown on demand), encodes on `stream`, copies the
- * requested outputs back and synchronises the stream before returning. */
+ * requested outputs back and synchronises the stream before returning.  X
+ * and W are copied on `stream`; the operands only the step kernel reads (R,
+ * B, sequence_lens, initial states, P) on a second stream owned by the
+ * handle, which starts after the work already on `stream` and joins it
+ * before the step kernel, so those copies overlap the projection.  When it
+ * returns, success or error, every copy it issued has completed (the host
+ * buffers may be reused at once).  Host memory that is page-locked copies
+ * asynchronously; other host memory is staged by the CUDA runtime. */
 rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* host_ops,
                          void* stream);
 

@@ -1034,22 +1034,32 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
       if (e != cudaSuccess) break;
     }
   }
+  // on an error past this point the copies already issued are waited for,
+  // so that the caller may reuse its host buffers at once
+  auto drain = [&]() {
+    if (cudaStreamWaitEvent(stream, h->copy_ev[1], 0) != cudaSuccess) cudaStreamSynchronize(h->copy_stream);
+    cudaStreamSynchronize(stream);
+  };
   cudaError_t j = cudaEventRecord(h->copy_ev[1], h->copy_stream);
   if (e != cudaSuccess || j != cudaSuccess) {
-    if (j == cudaSuccess) cudaStreamWaitEvent(stream, h->copy_ev[1], 0);
+    if (j != cudaSuccess) cudaStreamSynchronize(h->copy_stream);
+    else drain();
     return cuda_fail(h, p, "host-to-device copy", e != cudaSuccess ? e : j);
   }
   st = validate_all(h, p, &dev);
   if (st == RK_OK) st = encode_validated(h, p, &dev, nullptr, stream, h->copy_ev[1]);
   if (st != RK_OK) {
-    cudaStreamWaitEvent(stream, h->copy_ev[1], 0);  // nothing of the copy stream outlives the call
+    drain();
     return st;
   }
   for (int i = 8; i < 11; ++i) {
     if (!items[i].src->ptr || items[i].bytes == 0) continue;
     char* dstp = static_cast<char*>(items[i].src->ptr) + items[i].src->offset * eb;
     e = cudaMemcpyAsync(dstp, items[i].dst->ptr, (size_t)items[i].bytes, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return cuda_fail(h, p, "device-to-host copy", e);
+    if (e != cudaSuccess) {
+      cudaStreamSynchronize(stream);
+      return cuda_fail(h, p, "device-to-host copy", e);
+    }
   }
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(h, p, "stream synchronize", e);
