@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 from dataclasses import dataclass, field
 from typing import Optional, Sequence
 
@@ -84,6 +85,25 @@ _OPERAND_NAMES = ["X", "W", "R", "B", "sequence_lens", "initial_h", "initial_c",
 
 class rk_operands(ctypes.Structure):
     _fields_ = [(n, rk_tensor) for n in _OPERAND_NAMES]
+
+
+_OPERAND_INDEX = {n: i for i, n in enumerate(_OPERAND_NAMES)}
+# rk_operands as raw bytes: (pointer, offset, length) per operand, packed in
+# one call instead of a ctypes object per operand (the binding's per-layer
+# host cost)
+_OPERANDS_PACK = struct.Struct("=" + "Qqq" * len(_OPERAND_NAMES))
+assert _OPERANDS_PACK.size == ctypes.sizeof(rk_operands)
+
+
+def _pack_operands(entries) -> rk_operands:
+    """rk_operands from (name, pointer, element offset, length) entries."""
+    vals = [0] * (3 * len(_OPERAND_NAMES))
+    for name, ptr, off, n in entries:
+        i = _OPERAND_INDEX.get(name)
+        if i is None:
+            raise KeyError(name)
+        vals[3 * i], vals[3 * i + 1], vals[3 * i + 2] = ptr, off, n
+    return rk_operands.from_buffer_copy(_OPERANDS_PACK.pack(*vals))
 
 
 class rk_scratch(ctypes.Structure):
@@ -286,36 +306,29 @@ def torch_dtype(dtype: str):
     return (torch.float32, torch.float16, torch.bfloat16)[DTYPES[dtype]]
 
 
-def _tensor_ref(t, offset: int = 0) -> rk_tensor:
-    r = rk_tensor()
-    if t is None:
-        return r
-    if not t.is_contiguous():
-        raise ValueError("operands must be contiguous")
-    r.ptr = t.data_ptr()
-    r.offset = 0
-    r.length = t.numel()
-    return r
-
-
-def operands_from_tensors(**tensors) -> rk_operands:
+def operands_from_tensors(_dtype=None, **tensors) -> rk_operands:
     """rk_operands from torch tensors (device memory, contiguous).  A value may
     be a tensor or a (tensor, element_offset) pair; the tensor is then the
-    whole buffer and the operand starts ``element_offset`` elements in."""
-    ops = rk_operands()
+    whole buffer and the operand starts ``element_offset`` elements in.  With
+    _dtype given, every tensor but sequence_lens (int32) must have it."""
+    import torch
+    entries = []
     for name, v in tensors.items():
-        if name not in _OPERAND_NAMES:
+        if name not in _OPERAND_INDEX:
             raise KeyError(name)
         if v is None:
             continue
-        if isinstance(v, tuple):
-            t, off = v
-            ref = _tensor_ref(t)
-            ref.offset = int(off)
-        else:
-            ref = _tensor_ref(v)
-        setattr(ops, name, ref)
-    return ops
+        t, off = (v[0], int(v[1])) if isinstance(v, tuple) else (v, 0)
+        if t is None:
+            continue
+        if _dtype is not None:
+            need = torch.int32 if name == "sequence_lens" else _dtype
+            if t.dtype != need:
+                raise TypeError(f"{name}: expected {need}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError("operands must be contiguous")
+        entries.append((name, t.data_ptr(), off, t.numel()))
+    return _pack_operands(entries)
 
 
 class RecurrentLayer:
@@ -359,15 +372,7 @@ class RecurrentLayer:
     def encode(self, problem: Problem, stream=None, scratch: Optional[rk_scratch] = None, **tensors):
         import torch
         s = stream if stream is not None else torch.cuda.current_stream()
-        want = torch_dtype(problem.dtype)
-        for name, v in tensors.items():
-            t = v[0] if isinstance(v, tuple) else v
-            if t is None:
-                continue
-            need = torch.int32 if name == "sequence_lens" else want
-            if t.dtype != need:
-                raise TypeError(f"{name}: expected {need}, got {t.dtype}")
-        ops = operands_from_tensors(**tensors)
+        ops = operands_from_tensors(torch_dtype(problem.dtype), **tensors)
         self._check(rk_encode(self.handle, problem.to_c(), ops, scratch, s.cuda_stream))
 
     def encode_host(self, problem: Problem, stream=None, **arrays):
@@ -376,7 +381,7 @@ class RecurrentLayer:
         import numpy as np
         import torch
         s = stream if stream is not None else torch.cuda.current_stream()
-        ops = rk_operands()
+        entries = []
         for name, a in arrays.items():
             if a is None:
                 continue
@@ -388,8 +393,8 @@ class RecurrentLayer:
                 if not (isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"]):
                     raise ValueError(f"{name}: host arrays must be C-contiguous numpy arrays")
                 ptr, n = a.ctypes.data, a.size
-            setattr(ops, name, rk_tensor(ptr, 0, n))
-        self._check(rk_encode_host(self.handle, problem.to_c(), ops, s.cuda_stream))
+            entries.append((name, ptr, 0, n))
+        self._check(rk_encode_host(self.handle, problem.to_c(), _pack_operands(entries), s.cuda_stream))
 
     def forward(self, problem: Problem, X, W, R, B=None, sequence_lens=None, initial_h=None,
                 initial_c=None, P=None, want=("Y", "Y_h", "Y_c"), stream=None):

@@ -746,6 +746,7 @@ rk_status encode_validated(rk_handle* h, const rk_problem* p, const rk_operands*
   pp.W = tptr(ops->W, eb);
   pp.Xw = xw;
   pp.dtype = p->dtype;
+  pp.sms = h->sms;
   CUtensorMap tmA{}, tmB{};
   const FusedProj fz = fused_projection(h, p, pl, pp, sp.T > 0 && need_xw > 0, &tmA, &tmB);
   if (sp.T > 0 && need_xw > 0 && !fz.on) {
@@ -890,6 +891,7 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
     pp.W = tptr(ops->W, eb);
     pp.Xw = xw;
     pp.dtype = p->dtype;
+    pp.sms = plan_h.sms;
     const bool tc = !(h->flags & RK_FORCE_SIMT_PROJECTION) && rk::projection_tc_supported(pp);
     e = tc ? rk::launch_projection_tc(pp, status, h->timeout_ns, stream) : rk::launch_projection_simt(pp, stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);

@@ -93,6 +93,7 @@ struct ProjParams {
   const void* W;
   float* Xw;
   int dtype;
+  int sms;             // SMs of the device (0: queried at launch)
 };
 
 struct StepPlan {

@@ -290,8 +290,11 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   const bool aligned = (reinterpret_cast<uintptr_t>(p.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
                        ((size_t)p.K * eb) % 16 == 0 && p.K > 0;
   if (aligned) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int dev = 0, sms = p.sms;
+    if (sms <= 0) {
+      sms = 148;
+      if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
     const long long col_tiles = (long long)((p.N + PBN - 1) / PBN) * p.D;
     const int rows = pipe_rows_for(p.M, col_tiles, sms);
     const bool one_wave = col_tiles * ((p.M + rows - 1) / rows) <= sms;
