@@ -178,6 +178,17 @@ int64_t rk_state_length(const rk_problem* p);
  * the error encode would return, with rk_last_error set. */
 rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops);
 
+/* Host-only check of a HOST copy of sequence_lens (web page "Recurrent
+ * layers", section "Semantics": the kernels read the lengths on the device
+ * and do not validate them -- a negative length runs as 0 steps and one
+ * above seq as seq).  lens points to n int32 values.  Returns RK_OK when
+ * n == batch and every value lies in [0, seq], and also in [0, max_length]
+ * when max_length > 0 (the promise that shortens the step loop); else
+ * RK_ERR_SHAPE with rk_last_error naming the cell, the first offending row
+ * and its value (RK_ERR_ARG for a null handle or problem, or lens == NULL
+ * with n > 0).  Makes no CUDA call. */
+rk_status rk_validate_lengths(rk_handle* h, const rk_problem* p, const int32_t* lens, int64_t n);
+
 /* Enqueue the whole layer on `stream` (a cudaStream_t; NULL = legacy default
  * stream): input projection, then one persistent step kernel that runs every
  * step and writes Y, Y_h, Y_c.  Asynchronous: returns after enqueueing.

@@ -23,7 +23,7 @@ __all__ = [
     "rk_create", "rk_destroy", "rk_encode", "rk_encode_host", "rk_validate", "rk_xw_length",
     "rk_state_length", "rk_status_poll", "rk_set_wait_limit", "rk_last_error", "rk_launch_count",
     "rk_describe_plan", "rk_version", "rk_selftest_timeout", "rk_set_profiling", "rk_last_timings",
-    "rk_encode_noalloc", "RK_OK", "RK_ERR_SHAPE", "RK_ERR_UNSUPPORTED", "RK_ERR_CUDA", "RK_ERR_TIMEOUT", "RK_ERR_OOM", "RK_ERR_ARG",
+    "rk_encode_noalloc", "rk_validate_lengths", "RK_OK", "RK_ERR_SHAPE", "RK_ERR_UNSUPPORTED", "RK_ERR_CUDA", "RK_ERR_TIMEOUT", "RK_ERR_OOM", "RK_ERR_ARG",
     "RK_FORCE_SIMT_PROJECTION", "RK_FORCE_GRID_STEP", "RK_FORCE_GENERAL_STEP", "RK_FORCE_SIMT_STEP",
     "RK_SEPARATE_PROJECTION", "RK_PREFER_TENSOR_STEP", "EXPORTED_SYMBOLS",
 ]
@@ -49,7 +49,7 @@ EXPORTED_SYMBOLS = [
     "rk_version", "rk_create", "rk_destroy", "rk_xw_length", "rk_state_length", "rk_validate",
     "rk_encode", "rk_encode_host", "rk_status_poll", "rk_set_wait_limit", "rk_last_error",
     "rk_launch_count", "rk_describe_plan", "rk_selftest_timeout", "rk_set_profiling", "rk_last_timings",
-    "rk_encode_noalloc",
+    "rk_encode_noalloc", "rk_validate_lengths",
 ]
 
 
@@ -145,6 +145,7 @@ def load(path: Optional[str] = None):
         "rk_selftest_timeout": (ctypes.c_int32, [H, ctypes.c_void_p, ctypes.c_int64]),
         "rk_set_profiling": (ctypes.c_int32, [H, ctypes.c_int32]),
         "rk_encode_noalloc": (ctypes.c_int32, [H, P, O, ctypes.c_void_p]),
+        "rk_validate_lengths": (ctypes.c_int32, [H, P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64]),
         "rk_last_timings": (ctypes.c_int32, [H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     }
     for name, (res, args) in sig.items():
@@ -183,6 +184,14 @@ def rk_state_length(problem: rk_problem) -> int:
 
 def rk_validate(handle: int, problem: rk_problem, ops: rk_operands) -> int:
     return load().rk_validate(handle, ctypes.byref(problem), ctypes.byref(ops))
+
+
+def rk_validate_lengths(handle: int, problem: rk_problem, lens) -> int:
+    """Host check of sequence_lens (a sequence of ints or an int32 array)."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    return load().rk_validate_lengths(handle, ctypes.byref(problem),
+                                      a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), a.size)
 
 
 def rk_encode(handle: int, problem: rk_problem, ops: rk_operands, scratch: Optional[rk_scratch],

@@ -655,6 +655,24 @@ rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops)
   return validate_all(h, p, ops);
 }
 
+rk_status rk_validate_lengths(rk_handle* h, const rk_problem* p, const int32_t* lens, int64_t n) {
+  if (h == nullptr || p == nullptr) return RK_ERR_ARG;
+  h->last_error.clear();
+  rk_status st = validate_problem(h, p);
+  if (st != RK_OK) return st;
+  if (n > 0 && lens == nullptr) return fail(h, RK_ERR_ARG, "%s: sequence_lens: null host pointer", cell_name(p->cell));
+  if (n != p->batch)
+    return fail(h, RK_ERR_SHAPE, "%s: sequence_lens: %lld values for batch %lld", cell_name(p->cell), (long long)n,
+                (long long)p->batch);
+  const int64_t hi = p->max_length > 0 ? std::min<int64_t>(p->max_length, p->seq) : p->seq;
+  for (int64_t b = 0; b < n; ++b) {
+    if (lens[b] < 0 || lens[b] > hi)
+      return fail(h, RK_ERR_SHAPE, "%s: sequence_lens[%lld] = %d outside [0, %lld]%s", cell_name(p->cell),
+                  (long long)b, (int)lens[b], (long long)hi, p->max_length > 0 ? " (max_length)" : " (seq)");
+  }
+  return RK_OK;
+}
+
 rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t len) {
   if (h == nullptr || buf == nullptr || len <= 0) return RK_ERR_ARG;
   rk_status st = validate_problem(h, p);

@@ -155,6 +155,29 @@ def test_null_arguments():
     assert lib.rk_destroy(None) == rk.RK_OK
 
 
+def test_host_length_check(handle):
+    """rk_validate_lengths: every length in [0, seq] (and [0, max_length]
+    when set), one per batch row; messages name the cell, row and value."""
+    p = rk.Problem("gru", seq=10, batch=4, input=3, hidden=8)
+    assert rk.rk_validate_lengths(handle, p.to_c(), [10, 0, 3, 7]) == rk.RK_OK
+    assert rk.rk_validate_lengths(handle, p.to_c(), [10, -1, 3, 7]) == rk.RK_ERR_SHAPE
+    assert "GRU: sequence_lens[1] = -1 outside [0, 10]" in rk.rk_last_error(handle)
+    assert rk.rk_validate_lengths(handle, p.to_c(), [10, 2, 11, 7]) == rk.RK_ERR_SHAPE
+    assert "sequence_lens[2] = 11" in rk.rk_last_error(handle)
+    assert rk.rk_validate_lengths(handle, p.to_c(), [1, 2, 3]) == rk.RK_ERR_SHAPE
+    assert "3 values for batch 4" in rk.rk_last_error(handle)
+    q = rk.Problem("lstm", seq=10, batch=2, input=3, hidden=8, max_length=6)
+    assert rk.rk_validate_lengths(handle, q.to_c(), [6, 0]) == rk.RK_OK
+    assert rk.rk_validate_lengths(handle, q.to_c(), [7, 0]) == rk.RK_ERR_SHAPE
+    assert "(max_length)" in rk.rk_last_error(handle)
+    bad = rk.Problem("lstm", seq=10, batch=2, input=3, hidden=8, max_length=11)
+    assert rk.rk_validate_lengths(handle, bad.to_c(), [1, 1]) == rk.RK_ERR_SHAPE  # the problem itself
+    lib = rk.load()
+    assert lib.rk_validate_lengths(None, ctypes.byref(p.to_c()), None, 0) == rk.RK_ERR_ARG
+    assert lib.rk_validate_lengths(handle, ctypes.byref(p.to_c()), None, 4) == rk.RK_ERR_ARG
+    assert rk.rk_validate_lengths(handle, rk.Problem("rnn", seq=5, batch=0, input=1, hidden=2).to_c(), []) == rk.RK_OK
+
+
 def test_scratch_lengths():
     p = rk.Problem("lstm", seq=80, batch=1, input=256, hidden=256, direction="bidirectional")
     assert rk.rk_xw_length(p.to_c()) == 2 * 80 * 1 * 4 * 256
