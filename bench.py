@@ -162,6 +162,51 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ---------------------------------------------------------------- launch latency
+
+def empty_launch_us(dev, stream, n=400):
+    """Device time per launch of a 1-element kernel issued back to back on
+    the stream: from the host one by one ("stream"), and replayed from a CUDA
+    graph ("graph", no host in the way).  A design with one launch per
+    recurrent step pays at least this per step."""
+    import torch
+    x = torch.zeros(1, device=dev)
+    out = {"stream": None, "graph": None}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            x.add_(1.0)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            x.add_(1.0)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out["stream"] = e0.elapsed_time(e1) * 1e3 / n
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            x.add_(1.0)  # warm-up on the capture stream
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(n):
+                    x.add_(1.0)
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out["graph"] = e0.elapsed_time(e1) * 1e3 / n
+    except RuntimeError:
+        pass
+    return out
+
+
 # ---------------------------------------------------------------- profile summaries
 
 # Source files of each kernel, hashed so a committed ncu summary is only used
@@ -438,6 +483,8 @@ def run_gb300(args):
         pages_ms, _ = PAGES_LAYER_MS[name]
         vs = gflops / (flops / (pages_ms * 1e-3) / 1e9)
 
+    launch_us = empty_launch_us(dev, stream)
+
     line = {
         "metric": METRIC, "value": gflops, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -453,6 +500,9 @@ def run_gb300(args):
         "e2e": {"value": e2e_gflops, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "clocks": clocks, "gpu_launches": launches,
+        # what one dependent launch per step would cost at least on this machine
+        # (a 1-element kernel back to back on the stream), next to us_per_step
+        "empty_launch_us": launch_us,
     }
     if vs is not None:
         line["vs_baseline_note"] = "value / the pages' %.1f ms layer on %s (other hardware: context)" % PAGES_LAYER_MS[name]
