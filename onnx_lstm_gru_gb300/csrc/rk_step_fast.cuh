@@ -75,6 +75,30 @@ struct RFrag {
     v.y = Elem<T>::pair_from_f(e[2], e[3]);
   }
 };
+// bfloat16: the float32 value of bfloat16 bits b is b << 16, so a packed pair
+// unpacks with a shift and a mask.  Written as volatile asm so that the
+// compiler keeps the unpacking inside the step loop: hoisted out of it (R is
+// loop-invariant) it would hold every fragment twice and spill.
+template <>
+struct RFrag<__nv_bfloat16> {
+  uint2 v;
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    uint32_t lo, hi;
+    asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(u));
+    asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(u));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+  }
+  __device__ __forceinline__ float4 get() const {
+    const float2 a = unpack(v.x);
+    const float2 b = unpack(v.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  // the values come from the stored tensor, so the rounding is exact
+  __device__ __forceinline__ void set(const float e[4]) {
+    v.x = Elem<__nv_bfloat16>::pair_from_f(e[0], e[1]);
+    v.y = Elem<__nv_bfloat16>::pair_from_f(e[2], e[3]);
+  }
+};
 template <>
 struct RFrag<float> {
   float4 v;
