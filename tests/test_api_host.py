@@ -178,6 +178,26 @@ def test_host_length_check(handle):
     assert rk.rk_validate_lengths(handle, rk.Problem("rnn", seq=5, batch=0, input=1, hidden=2).to_c(), []) == rk.RK_OK
 
 
+def test_operand_table_packing():
+    """The binding packs rk_operands in one call: every field lands where the
+    C struct has it, tuples carry an element offset, dtypes are checked."""
+    import torch
+    t = {n: torch.zeros(3 + i, dtype=torch.int32 if n == "sequence_lens" else torch.float32)
+         for i, n in enumerate(rk._OPERAND_NAMES)}
+    ops = rk.operands_from_tensors(torch.float32, **{n: ((v, 2) if n == "R" else v) for n, v in t.items()})
+    for i, n in enumerate(rk._OPERAND_NAMES):
+        f = getattr(ops, n)
+        assert f.ptr == t[n].data_ptr() and f.length == 3 + i and f.offset == (2 if n == "R" else 0), n
+    partial = rk.operands_from_tensors(X=t["X"], Y_c=None)
+    assert partial.X.ptr == t["X"].data_ptr() and partial.W.ptr is None and partial.Y_c.ptr is None
+    with pytest.raises(TypeError):
+        rk.operands_from_tensors(torch.float16, X=t["X"])
+    with pytest.raises(KeyError):
+        rk.operands_from_tensors(Q=t["X"])
+    with pytest.raises(ValueError):
+        rk.operands_from_tensors(X=torch.zeros(4, 4).t())
+
+
 def test_scratch_lengths():
     p = rk.Problem("lstm", seq=80, batch=1, input=256, hidden=256, direction="bidirectional")
     assert rk.rk_xw_length(p.to_c()) == 2 * 80 * 1 * 4 * 256
