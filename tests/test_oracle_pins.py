@@ -227,6 +227,50 @@ def test_rnn_hidden1_relu_and_clip():
     np.testing.assert_array_equal(out["Y"].reshape(3), [0.25, -0.25, 0.25])
 
 
+def test_lstm_activation_slots_by_direction():
+    """Bidirectional LSTM, I = H = 1, one step from zero state, x = 1, R = 0,
+    no bias, Affine activations with a different (alpha, beta) in each of the
+    six slots (f, g, h of direction 0, then of direction 1).  Worked by hand
+    in dyadic numbers, so exact: direction 0 with f = (1/2, 1/4), g = (2, -1),
+    h = (-1, 1/2) and W = (i 1, o 1/2, f 3, c 3/4): i = 3/4, c~ = 1/2,
+    c = 3/8, o = 1/2, h = 1/2 * (1/2 - 3/8) = 1/16.  Direction 1 with
+    f = (1/4, 1/2), g = (-1, 1/4), h = (4, 0): i = 3/4, c~ = -1/2, c = -3/8,
+    o = 5/8, h = 5/8 * (-3/2) = -15/16.  Swapping g and h, or giving one
+    direction the other's slots, changes every one of these values."""
+    acts = [("affine", 0.5, 0.25), ("affine", 2.0, -1.0), ("affine", -1.0, 0.5),
+            ("affine", 0.25, 0.5), ("affine", -1.0, 0.25), ("affine", 4.0, 0.0)]
+    s = spec("lstm", direction="bidirectional", activations=acts)
+    W = np.array([1.0, 0.5, 3.0, 0.75] * 2).reshape(2, 4, 1)
+    out = oracle.layer(s, np.ones((1, 1, 1)), W, np.zeros((2, 4, 1)))
+    assert out["Y_c"].reshape(2).tolist() == [0.375, -0.375]
+    assert out["Y_h"].reshape(2).tolist() == [0.0625, -0.9375]
+    assert out["Y"].reshape(2).tolist() == [0.0625, -0.9375]
+
+
+def test_gru_activation_slots_by_direction():
+    """Bidirectional GRU (linear_before_reset = 1), I = H = 1, one step, x = 1,
+    h0 = 1, W = (z 1, r 1, h 1/4), R = (0, 0, 1/2), no bias, Affine slots
+    (f, g of direction 0, then of direction 1), worked by hand: direction 0,
+    f = (1/2, 0), g = (2, 1/2): z = r = 1/2, pre_h = 1/4 + 1/2 * 1/2 = 1/2,
+    h~ = 3/2, h = 1/2 * 3/2 + 1/2 * 1 = 5/4.  Direction 1, f = (1/4, 1/2),
+    g = (-1, 0): z = r = 3/4, pre_h = 1/4 + 3/4 * 1/2 = 5/8, h~ = -5/8,
+    h = 1/4 * -5/8 + 3/4 = 19/32."""
+    acts = [("affine", 0.5, 0.0), ("affine", 2.0, 0.5), ("affine", 0.25, 0.5), ("affine", -1.0, 0.0)]
+    s = spec("gru", direction="bidirectional", linear_before_reset=1, activations=acts)
+    W = np.array([1.0, 1.0, 0.25] * 2).reshape(2, 3, 1)
+    R = np.array([0.0, 0.0, 0.5] * 2).reshape(2, 3, 1)
+    out = oracle.layer(s, np.ones((1, 1, 1)), W, R, initial_h=np.ones((2, 1, 1)))
+    assert out["Y_h"].reshape(2).tolist() == [1.25, 0.59375]
+
+
+def test_rnn_activation_slot_by_direction():
+    """Bidirectional RNN, one slot per direction: x = 1, W = 1/4, R = 0,
+    Affine(2, 0) forward gives 1/2, Affine(-1, 1/2) backward gives 1/4."""
+    s = spec("rnn", direction="bidirectional", activations=[("affine", 2.0, 0.0), ("affine", -1.0, 0.5)])
+    out = oracle.layer(s, np.ones((1, 1, 1)), np.full((2, 1, 1), 0.25), np.zeros((2, 1, 1)))
+    assert out["Y_h"].reshape(2).tolist() == [0.5, 0.25]
+
+
 # ---------------------------------------------------------------- torch special case
 
 def _torch_module(cell, I, H, bidirectional, batch_first):
