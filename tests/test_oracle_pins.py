@@ -468,6 +468,23 @@ def test_options():
     assert np.abs(f1["Y"] - base["Y"]).max() > 1e-3
 
 
+def test_lstm_clip_after_peepholes_exact():
+    """LSTM, I = H = 1, one step, x = 1, h0 = 0, c0 = 2, clip 1/2, identity
+    (Affine(1, 0)) in every slot, W = (i 1/4, o 1/4, f 1/4, c 2), R = 0, no
+    bias, P = (i 1, o -4, f -1).  By hand: pre_i = 1/4 + 1 * 2 = 9/4 -> clipped
+    1/2; pre_f = 1/4 - 2 -> -1/2; the candidate 2 -> 1/2 (clip covers it);
+    c = -1/2 * 2 + 1/2 * 1/2 = -3/4 (the state itself is not clipped); pre_o =
+    1/4 - 4 * (-3/4) = 13/4 with the new c -> 1/2; h = 1/2 * (-3/4) = -3/8.
+    Clipping before the peepholes, the old c in the o peephole, an unclipped
+    candidate or a clipped state each change these numbers."""
+    s = spec("lstm", clip=0.5, activations=[("affine", 1.0, 0.0)] * 3)
+    out = oracle.layer(s, np.ones((1, 1, 1)), np.array([0.25, 0.25, 0.25, 2.0]).reshape(1, 4, 1),
+                       np.zeros((1, 4, 1)), initial_c=np.full((1, 1, 1), 2.0),
+                       P=np.array([1.0, -4.0, -1.0]).reshape(1, 3))
+    assert out["Y_c"].item() == -0.75
+    assert out["Y_h"].item() == -0.375
+
+
 def test_gru_forms_coincide_when_reset_gate_is_one():
     """With the r gate forced to 1 (a huge r bias) and Rb_h = 0 the two
     linear_before_reset forms are the same expression."""
