@@ -209,6 +209,24 @@ def test_gru_hidden1_closed_form(lbr):
     assert abs(math.tanh(other) - math.tanh(pre_h)) > 1e-3
 
 
+def test_gru_lbr0_reset_applies_per_source_unit():
+    """GRU with linear_before_reset = 0 and H = 2 (torch has no such form):
+    the candidate's product is R_h . (r (.) h_prev), so unit j's sum weighs
+    h_prev[k] by r[k], the reset gate of the SOURCE unit k.  Identity
+    (Affine(1, 0)) activations, one step, x = 1, h0 = (1, 2), no bias,
+    W_z = (1/2, 1/4), W_r = (1/2, 2), W_h = 0, R = 0 except
+    R_h = [[1, 1/2], [1/4, 1]].  By hand: r (.) h0 = (1/2, 4);
+    pre_h = (1/2 + 2, 1/8 + 4) = (5/2, 33/8); h = (1 - z) h~ + z h0 =
+    (1/2 * 5/2 + 1/2, 3/4 * 33/8 + 1/2) = (7/4, 115/32).  Weighting by r[j]
+    instead, or reading R_h transposed, changes both values."""
+    s = spec("gru", hidden=2, linear_before_reset=0, activations=[("affine", 1.0, 0.0)] * 2)
+    W = np.array([0.5, 0.25, 0.5, 2.0, 0.0, 0.0]).reshape(1, 6, 1)
+    R = np.zeros((1, 6, 2))
+    R[0, 4:6] = [[1.0, 0.5], [0.25, 1.0]]
+    out = oracle.layer(s, np.ones((1, 1, 1)), W, R, initial_h=np.array([1.0, 2.0]).reshape(1, 1, 2))
+    assert out["Y_h"].reshape(2).tolist() == [1.75, 115.0 / 32.0]
+
+
 def test_rnn_hidden1_relu_and_clip():
     """RNN with Relu: h1 = relu(w*x1 + r*h0 + b), h2 = relu(w*x2 + r*h1 + b).
     A clip of 0.25 clamps the pre-activation before the activation."""
@@ -440,6 +458,19 @@ def test_seq0_gives_initial_state_and_len0_gives_zero():
     a3 = dict(a1, sequence_lens=np.array([0, 3], dtype=np.int32))
     out3 = oracle.layer(s1, **a3)
     np.testing.assert_array_equal(out2["Y"], out3["Y"])
+
+
+def test_out_of_range_lengths_clamp():
+    """A negative length runs as 0 steps and one above seq as seq (the
+    kernels read lengths unvalidated, so the oracle fixes the same reading)."""
+    rng = np.random.default_rng(19)
+    s = spec("lstm", direction="bidirectional", seq=5, batch=3, input=2, hidden=3)
+    a = rand_inputs(rng, s, with_p=True)
+    got = oracle.layer(s, **dict(a, sequence_lens=np.array([-3, 99, 2], dtype=np.int32)))
+    want = oracle.layer(s, **dict(a, sequence_lens=np.array([0, 5, 2], dtype=np.int32)))
+    for k in ("Y", "Y_h", "Y_c"):
+        np.testing.assert_array_equal(got[k], want[k])
+    assert not want["Y"][:, :, 0].any() and not want["Y_h"][:, 0].any()
 
 
 def test_options():
