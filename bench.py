@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-sub", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--sub-cpu-budget", type=float, default=2.0,
+                    help="seconds of oracle work for each other workload's cpu_baseline")
     ap.add_argument("--seq-cut", type=int, default=None,
                     help="profiling aid: the workload with its sequence cut to this many steps (workload name gets "
                          "a _seqN suffix; not the headline configuration)")
@@ -112,54 +115,139 @@ def sum_over_ranks(x: float, world: int, device=None) -> float:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """SM clock and clock-event reasons sampled every ~2 ms on a thread while
+    the benchmark runs, through NVML's read-only queries (libnvidia-ml, loaded
+    with ctypes); nvidia-smi polling every 200 ms where NVML cannot be loaded.
+    ``mark()`` opens a named window (a timed region) and ``window(name)``
+    summarises the samples taken inside it."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid=None):
+    def __init__(self, uuid=None, period_s=0.002):
         self.uuid = str(uuid) if uuid is not None else None
-        self.proc = None
+        self.period = period_s
+        self.samples = []          # (t, sm_mhz, reasons bitmask)
+        self.windows = {}          # name -> [t0, t1]
+        self.sm_max = None
+        self.source = None
+        self._stop = None
+        self._thread = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            u = self.uuid if self.uuid.startswith("GPU-") else "GPU-" + self.uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            idx = int((os.environ.get("CUDA_VISIBLE_DEVICES") or "0").split(",")[0] or 0)
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                raise OSError("no NVML device handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1: SM clock domain
+            self.sm_max = float(mx.value)
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
 
     def start(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            import ctypes
+            lib, h, reasons_fn = self._nvml()
+            self.source = "nvml, %.0f ms" % (self.period * 1e3)
+            self._stop = threading.Event()
+
+            def run():
+                clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    a = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+                    b = reasons_fn(h, ctypes.byref(rs))
+                    if a == 0:
+                        self.samples.append((time.perf_counter(), float(clk.value), int(rs.value) if b == 0 else 0))
+                    self._stop.wait(self.period)
+            self._thread = threading.Thread(target=run, daemon=True)
+            self._thread.start()
+        except (OSError, AttributeError):
+            self._start_smi()
+        time.sleep(0.05)
+
+    def _start_smi(self):
+        self.source = "nvidia-smi, 200 ms"
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                           "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
-            self.proc = None
+            self._proc = None
+        self._t0 = time.perf_counter()
         time.sleep(0.3)
 
+    def mark(self, name):
+        self.windows[name] = [time.perf_counter(), None]
+
+    def end(self, name):
+        self.windows[name][1] = time.perf_counter()
+
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = []
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 10:
-                rows.append(parts)
-        mine = [r for r in rows if self.uuid and self.uuid in r[1]]
-        if mine:
-            rows = mine
-        elif len({r[0] for r in rows}) > 1:
-            rows = [r for r in rows if r[0] == rows[0][0]]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
-        # "under load": samples at or above half the highest clock seen
-        hi = max(sm) if sm else 0.0
+        if self._thread is not None:
+            time.sleep(2 * self.period)
+            self._stop.set()
+            self._thread.join(timeout=2)
+        elif self._proc is not None:
+            time.sleep(0.25)
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            rows = [[p.strip() for p in line.split(",")] for line in out.splitlines()]
+            rows = [r for r in rows if len(r) >= 10]
+            mine = [r for r in rows if self.uuid and self.uuid in r[1]]
+            rows = mine or [r for r in rows if rows and r[0] == rows[0][0]]
+            bits = {6: 0x8, 7: 0x40, 8: 0x20, 9: 0x4}
+            t = self._t0
+            for r in rows:
+                t += 0.2
+                try:
+                    sm = float(r[2])
+                    self.sm_max = float(r[3])
+                except ValueError:
+                    continue
+                self.samples.append((t, sm, sum(b for i, b in bits.items() if r[i].lower() == "active")))
+
+    def window(self, name=None):
+        """Clock record of the samples inside window `name` (all samples when
+        None or when the window caught fewer than 3): median SM clock of the
+        samples under load (at least half the highest clock seen), max clock,
+        the clock-event reasons seen, sample counts."""
+        sel = self.samples
+        scope = "whole run"
+        if name in self.windows and self.windows[name][1] is not None:
+            t0, t1 = self.windows[name]
+            inside = [x for x in self.samples if t0 <= x[0] <= t1]
+            if len(inside) >= 3 or self._thread is None:
+                sel, scope = inside, "timed region"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
+        sm = [x[1] for x in sel]
+        hi = max(sm)
         load = [v for v in sm if v >= 0.5 * hi] or sm
-        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        mask = 0
+        for x in sel:
+            mask |= x[2]
+        reasons = sorted(v for b, v in self.REASONS.items() if mask & b)
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": self.sm_max, "reasons": reasons,
+                "samples": len(sel), "samples_under_load": len(load), "scope": scope, "source": self.source}
 
 
 # ---------------------------------------------------------------- launch latency
@@ -207,6 +295,63 @@ def empty_launch_us(dev, stream, n=400):
     return out
 
 
+# ---------------------------------------------------------------- peaks measured in the run
+
+def measure_fp32_peak(dev, stream):
+    """float32 FMA throughput of the SMs: a kernel of independent fused
+    multiply-adds only (libfmapeak.so, built next to the library), 8 blocks
+    of 256 threads per SM, best of 10 launches timed with CUDA events on the
+    launching stream.  Returns TFLOP/s."""
+    import ctypes
+    import torch
+    from onnx_lstm_gru_gb300 import _build
+    lib = ctypes.CDLL(_build.PROBE_LIB)
+    lib.rk_probe_fma_flops.restype = ctypes.c_double
+    lib.rk_probe_fma_flops.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.rk_probe_fma_launch.restype = ctypes.c_int
+    lib.rk_probe_fma_launch.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads, iters = sms * 8, 256, 2048
+    out = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+    flops = lib.rk_probe_fma_flops(blocks, threads, iters)
+    best = None
+    for i in range(13):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rc = lib.rk_probe_fma_launch(out.data_ptr(), blocks, threads, iters, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if rc != 0:
+            raise RuntimeError(f"FMA peak probe launch failed: cudaError {rc}")
+        if i >= 3:
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+    return flops / (best * 1e-3) / 1e12
+
+
+def measure_tensor_peak(dev, stream, dtype):
+    """Dense tensor-core throughput of torch.matmul at 8192^3 (2 * 8192^3
+    FLOPs) in `dtype`, best of 10 after 3 warm-ups, CUDA events on the
+    stream: the same recipe as the driver's measured bf16 peak."""
+    import torch
+    n = 8192
+    with torch.cuda.stream(stream):
+        a = torch.randn(n, n, device=dev).to(dtype)
+        b = torch.randn(n, n, device=dev).to(dtype)
+        best = None
+        for i in range(13):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            c = a @ b
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+        del a, b, c
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- profile summaries
 
 # Source files of each kernel, hashed so a committed ncu summary is only used
@@ -241,25 +386,6 @@ def plan_fields(plan: str) -> dict:
     return dict(kv.split("=", 1) for kv in plan.split() if "=" in kv)
 
 
-def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, alu_peak: float, alu_src: str,
-                    workload: str) -> dict:
-    """Roofline entry of one kernel: tensor-core kernels against the measured
-    dense bf16 rate (fp16 has the same nominal dense rate), FP32 SIMT kernels
-    against the FP32 FMA rate derived from the SM count and clock."""
-    fp16 = "_f16" in workload
-    achieved = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
-    name, files = KERNEL_SOURCES[kind]
-    traffic = profiled_traffic(name, workload, kernel_source_hash(files))
-    if kind in ("tensor", "tensor_small", "proj_tc"):
-        peak = float(peaks["bf16_tflops"])
-        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic, "kernel": name,
-                "peak_source": "measured dense bf16 burst" +
-                               ("; fp16 runs at the same nominal dense rate" if fp16 else "")}
-    return {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s", "frac": achieved / alu_peak,
-            "traffic": traffic, "kernel": name, "peak_source": alu_src}
-
-
 def profiled_traffic(kernel: str, workload: str, source_hash: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
     summary, or None if there is none or the kernel source changed since."""
@@ -272,6 +398,24 @@ def profiled_traffic(kernel: str, workload: str, source_hash: str):
     if not m or not hs or hs.group(1) != source_hash:
         return None
     return float(m.group(1))
+
+
+def kernel_roofline(kind: str, flops: float, ms: float, peaks: dict, workload: str, dtype: str) -> dict:
+    """Roofline entry of one kernel: tcgen05 kernels against the measured
+    dense tensor rate of their operand type (fp16 or bf16), float32 SIMT
+    kernels (and 16-bit layers on SIMT kernels, whose arithmetic is float32)
+    against the measured float32 FMA rate."""
+    achieved = flops / (ms * 1e-3) / 1e12 if ms > 0 else 0.0
+    name, files = KERNEL_SOURCES[kind]
+    traffic = profiled_traffic(name, workload, kernel_source_hash(files))
+    if kind in ("tensor", "tensor_small", "proj_tc"):
+        key = "bf16" if dtype == "bf16" else "f16"
+        peak, src = peaks[key]
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": name, "peak_source": src}
+    peak, src = peaks["f32"]
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic, "kernel": name, "peak_source": src}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -340,8 +484,140 @@ def oracle_sample_rate(w, budget_s: float):
 
 # ---------------------------------------------------------------- the GPU arm
 
-def run_gb300(args):
+# the other layer shapes of the benchmark's configuration list, each measured
+# in the same run as a record of its own (the line's config stays the headline)
+SUB_WORKLOADS = ["lstm_fwd_s8_b1_i16_h16_f32", "bigru_s128_b8_i512_h512_f16_lbr0",
+                 "bigru_s128_b8_i512_h512_f16_lbr1", "revlstm_peep_clip_s200_b4_i128_h1024_f32",
+                 "bilstm_s512_b64_i1024_h1024_f16"]
+L2_NOTE = "GPU arm: L2 flushed between timed layer runs (256 MiB write, untimed)"
+
+
+def config_of(name, pr, world):
+    """The config object of both arms' JSON lines (same keys and values)."""
+    return {"workload": name, "cell": pr.cell, "direction": pr.direction, "seq": pr.seq, "batch": pr.batch,
+            "input": pr.input, "hidden": pr.hidden, "layout": pr.layout, "tensor_dtype": pr.dtype,
+            "l2": L2_NOTE, "parallelism": f"replicas x{world}"}
+
+
+class Measured:
+    """One workload measured on the GPU: the timed layer runs, the per-kernel
+    durations, the algorithmic work and the clocks seen meanwhile (the
+    window spans the timed runs and the kernel-timing runs of the same
+    layer); rooflines are attached once the peaks are known."""
+
+
+def measure_workload(rk, workloads, name, w, steps, warmup, n_prof, dev, stream, flush, sampler, world, keep=False):
     import numpy as np
+    import torch
+    pr = w.problem
+    inp = workloads.make_inputs(w)
+    tdt = rk.torch_dtype(pr.dtype)
+
+    def host_tensor(k, v):
+        # bfloat16 inputs arrive as float32 arrays of bfloat16 numbers: exact cast
+        t = torch.from_numpy(v)
+        return t if k == "sequence_lens" else t.to(tdt)
+
+    dev_in = {k: host_tensor(k, v).to(dev) for k, v in inp.items()}
+    shp = pr.shapes()
+    outs = {n: torch.empty(shp[n], dtype=tdt, device=dev) for n in w.outputs if not (n == "Y_c" and pr.cell != "lstm")}
+    layer = rk.RecurrentLayer()
+    plan = layer.plan(pr)
+
+    def run_once():
+        layer.encode(pr, stream=stream, **dev_in, **outs)
+
+    for _ in range(max(3, warmup)):
+        flush.zero_()
+        run_once()
+    torch.cuda.synchronize()
+    layer.poll(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    launches0 = layer.launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(name)
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        run_once()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = layer.launches() - launches0
+    layer.poll(stream)
+    times = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    ms_local = sum(times) / len(times)
+    ms = max_over_ranks(ms_local, world, dev)
+
+    # per-kernel durations (events recorded by the library around its launches)
+    rk.rk_set_profiling(layer.handle, True)
+    kproj, kstep = [], []
+    for _ in range(n_prof):
+        flush.zero_()
+        run_once()
+        a, b = rk.rk_last_timings(layer.handle)
+        kproj.append(a)
+        kstep.append(b)
+    rk.rk_set_profiling(layer.handle, False)
+    sampler.end(name)  # the clock window covers the timed runs and these
+    m = Measured()
+    m.name, m.w, m.pr, m.inp, m.plan = name, w, pr, inp, plan
+    m.ms_local, m.ms, m.launches, m.steps = ms_local, ms, launches, steps
+    m.proj_ms = statistics.mean(kproj) if kproj and kproj[0] >= 0 else 0.0
+    m.step_ms = statistics.mean(kstep)
+    m.flops = workloads.algorithmic_flops(pr, inp.get("sequence_lens"))
+    D, G, H = pr.num_directions, pr.gates, pr.hidden
+    lens = inp.get("sequence_lens")
+    tot_len = pr.seq * pr.batch if lens is None else int(np.clip(lens, 0, pr.seq).sum())
+    m.step_flops = 2.0 * tot_len * G * H * H * D
+    m.proj_flops = 2.0 * pr.seq * pr.batch * pr.input * G * H * D
+    if m.proj_ms <= 0.0:  # projection computed inside the step kernel's launch
+        m.step_flops += m.proj_flops
+    pf = plan_fields(plan)
+    m.step_kind = pf.get("step", "fast")
+    if m.step_kind == "tensor" and pf.get("variant") == "small":
+        m.step_kind = "tensor_small"
+    m.proj_kind = "proj_tc" if pf.get("proj") == "tc" else "proj_simt"
+    m.cbytes = workloads.compulsory_bytes(pr, {**inp, **{n: None for n in outs}})
+    m.clocks = sampler.window(name)
+    if keep:
+        m.layer, m.dev_in, m.outs, m.host_tensor = layer, dev_in, outs, host_tensor
+    else:
+        layer.close()
+        del dev_in, outs
+    return m
+
+
+def rooflines(m, peaks, hbm_gbs, peak_src):
+    """(roofline of the dominant kernel with the other kernel under
+    'others', whole-layer roofline) of a measured workload."""
+    r_step = kernel_roofline(m.step_kind, m.step_flops, m.step_ms, peaks, m.name, m.pr.dtype)
+    r_proj = kernel_roofline(m.proj_kind, m.proj_flops, m.proj_ms, peaks, m.name, m.pr.dtype) \
+        if m.proj_ms > 0 else None
+    dom = r_step if (r_proj is None or m.step_ms >= m.proj_ms) else r_proj
+    dom = dict(dom, others=[r for r in (r_step, r_proj) if r is not None and r is not dom])
+    # whole layer: max(FLOPs at the peak of the unit each kernel runs on,
+    # compulsory bytes at HBM bandwidth) / measured layer time
+    t_flops = m.step_flops / (r_step["peak"] * 1e12) + (m.proj_flops / (r_proj["peak"] * 1e12) if r_proj else 0.0)
+    t_bytes = m.cbytes / (hbm_gbs * 1e9)
+    layer = {"t_roofline_us": max(t_flops, t_bytes) * 1e6, "t_measured_us": m.ms_local * 1e3,
+             "frac": max(t_flops, t_bytes) / (m.ms_local * 1e-3), "flops": m.flops, "compulsory_bytes": m.cbytes,
+             "hbm_gbs": hbm_gbs, "hbm_source": peak_src}
+    return dom, layer
+
+
+def sub_record(m, peaks, hbm_gbs, peak_src, world, cpu):
+    dom, layer = rooflines(m, peaks, hbm_gbs, peak_src)
+    return {"config": config_of(m.name, m.pr, world), "plan": m.plan, "steps": m.steps, "ms_per_layer": m.ms,
+            "us_per_step": m.ms * 1e3 / max(m.pr.seq, 1), "steps_per_s": m.pr.seq / (m.ms * 1e-3) * world,
+            "gflops": m.flops * world / (m.ms * 1e-3) / 1e9,
+            "kernels_ms": {"projection": m.proj_ms, "step": m.step_ms}, "roofline": dom, "layer_roofline": layer,
+            "clocks": m.clocks, "gpu_launches": m.launches, "cpu_baseline": cpu}
+
+
+def run_gb300(args):
     import torch
     import onnx_lstm_gru_gb300 as rk
     from onnx_lstm_gru_gb300 import workloads
@@ -356,79 +632,29 @@ def run_gb300(args):
     if args.seq_cut:
         w = dataclasses.replace(w, problem=dataclasses.replace(w.problem, seq=min(args.seq_cut, w.problem.seq)))
         name = f"{name}_seq{w.problem.seq}"
-    pr = w.problem
-    inp = workloads.make_inputs(w)
-    tdt = rk.torch_dtype(pr.dtype)
-
-    def host_tensor(k, v):
-        # bfloat16 inputs arrive as float32 arrays of bfloat16 numbers: exact cast
-        t = torch.from_numpy(v)
-        return t if k == "sequence_lens" else t.to(tdt)
-
-    dev_in = {k: host_tensor(k, v).to(dev) for k, v in inp.items()}
-    shp = pr.shapes()
-    outs = {n: torch.empty(shp[n], dtype=tdt, device=dev) for n in w.outputs if not (n == "Y_c" and pr.cell != "lstm")}
-    layer = rk.RecurrentLayer()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    plan = layer.plan(pr)
-
-    def run_once():
-        layer.encode(pr, stream=stream, **dev_in, **outs)
-
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        run_once()
-    torch.cuda.synchronize()
-    layer.poll(stream)
-
     sampler = ClockSampler(getattr(torch.cuda.get_device_properties(dev), "uuid", None))
-    if rank == 0:
-        sampler.start()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    launches0 = layer.launches()
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        run_once()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    launches = layer.launches() - launches0
-    clocks = sampler.stop() if rank == 0 else None
-    layer.poll(stream)
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_local = sum(times) / len(times)
-    ms = max_over_ranks(ms_local, world, dev)
-    flops = workloads.algorithmic_flops(pr, inp.get("sequence_lens"))
-    total_flops = sum_over_ranks(flops, world, dev)
-    gflops = total_flops / (ms * 1e-3) / 1e9
+    sampler.start()
 
-    # per-kernel durations (events recorded by the library around its launches)
-    rk.rk_set_profiling(layer.handle, True)
-    kproj, kstep = [], []
-    for _ in range(max(20, min(args.steps, 200))):
-        flush.zero_()
-        run_once()
-        a, b = rk.rk_last_timings(layer.handle)
-        kproj.append(a)
-        kstep.append(b)
-    rk.rk_set_profiling(layer.handle, False)
-    proj_ms = statistics.mean(kproj) if kproj and kproj[0] >= 0 else 0.0
-    step_ms = statistics.mean(kstep)
+    # the headline workload: the line's value
+    main = measure_workload(rk, workloads, name, w, args.steps, args.warmup, max(20, min(args.steps, 200)), dev,
+                            stream, flush, sampler, world, keep=True)
+    pr, inp, layer = main.pr, main.inp, main.layer
+    total_flops = sum_over_ranks(main.flops, world, dev)
+    gflops = total_flops / (main.ms * 1e-3) / 1e9
 
     # e2e through the host-buffer entry point (copies inside the timed region)
+    tdt = rk.torch_dtype(pr.dtype)
+    shp = pr.shapes()
     n_e2e = args.e2e_steps or max(3, min(args.steps, 300))
     pinned_in = {}
     for k, v in inp.items():
-        hv = host_tensor(k, v)
+        hv = main.host_tensor(k, v)
         t = torch.empty(hv.shape, dtype=hv.dtype, pin_memory=True)
         t.copy_(hv)
         pinned_in[k] = t
-    pinned_out = {n: torch.empty(shp[n], dtype=tdt, pin_memory=True) for n in outs}
+    pinned_out = {n: torch.empty(shp[n], dtype=tdt, pin_memory=True) for n in main.outs}
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
     d2h = sum(t.numel() * t.element_size() for t in pinned_out.values())
     for _ in range(3):
@@ -440,73 +666,75 @@ def run_gb300(args):
     e2e_s = (time.perf_counter() - t0) / n_e2e
     e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e_gflops = total_flops / e2e_s / 1e9
+    layer.close()
+    del main.dev_in, main.outs
 
-    peaks, peak_src = load_peaks()
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak_tflops = sm_count * 128 * 2 * sm_max * 1e6 / 1e12  # FP32 FMA lanes x 2 x max clock
-    D, G, H = pr.num_directions, pr.gates, pr.hidden
-    lens = inp.get("sequence_lens")
-    import numpy as _np
-    tot_len = pr.seq * pr.batch if lens is None else int(_np.clip(lens, 0, pr.seq).sum())
-    step_flops = 2.0 * tot_len * G * H * H * D
-    proj_flops = 2.0 * pr.seq * pr.batch * pr.input * G * H * D
-    if proj_ms <= 0.0:  # projection fused into the step kernel
-        step_flops += proj_flops
-    pf = plan_fields(plan)
-    alu_src = f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz"
-    step_kind = pf.get("step", "fast")
-    if step_kind == "tensor" and pf.get("variant") == "small":
-        step_kind = "tensor_small"
-    proj_kind = "proj_tc" if pf.get("proj") == "tc" else "proj_simt"
-    r_step = kernel_roofline(step_kind, step_flops, step_ms, peaks, alu_peak_tflops, alu_src, name)
-    r_proj = kernel_roofline(proj_kind, proj_flops, proj_ms, peaks, alu_peak_tflops, alu_src, name) \
-        if proj_ms > 0 else None
-    roofline = r_step if (r_proj is None or step_ms >= proj_ms) else r_proj
-    roofline = dict(roofline, others=[r for r in (r_step, r_proj) if r is not None and r is not roofline])
-    # whole-layer roofline: max(FLOPs at peak, compulsory bytes at HBM) / measured time
-    cbytes = workloads.compulsory_bytes(pr, {**inp, **{n: None for n in outs}})
-    # FLOPs at the peak of the unit each kernel runs on
-    t_flops = step_flops / (r_step["peak"] * 1e12) + (proj_flops / (r_proj["peak"] * 1e12) if r_proj else 0.0)
-    t_bytes = cbytes / (float(peaks["hbm_gbs"]) * 1e9)
-    layer_roofline = {"t_roofline_us": max(t_flops, t_bytes) * 1e6, "t_measured_us": ms_local * 1e3,
-                      "frac": max(t_flops, t_bytes) / (ms_local * 1e-3), "flops": flops, "compulsory_bytes": cbytes,
-                      "hbm_gbs": float(peaks["hbm_gbs"]), "peak_source": peak_src}
+    # the other configurations, one record each
+    subs = []
+    if not args.no_sub and not args.seq_cut:
+        sub_steps = max(1, min(args.steps, 50))
+        for sname in SUB_WORKLOADS:
+            if sname == name:
+                continue
+            subs.append(measure_workload(rk, workloads, sname, workloads.WORKLOADS[sname], sub_steps,
+                                         max(3, min(args.warmup, 5)), max(10, min(sub_steps, 20)), dev, stream,
+                                         flush, sampler, world))
+    launch_us = empty_launch_us(dev, stream)
 
+    # peaks measured in this run: the float32 FMA rate and the dense fp16
+    # tensor rate; dense bf16 from the driver's measurement
+    file_peaks, file_src = load_peaks()
+    sampler.mark("fp32_peak")
+    fp32 = measure_fp32_peak(dev, stream)
+    sampler.end("fp32_peak")
+    sampler.mark("f16_peak")
+    f16 = measure_tensor_peak(dev, stream, torch.float16)
+    sampler.end("f16_peak")
+    sampler.stop()
+    peaks = {"f32": (fp32, "measured in this run: float32 FMA kernel, best of 10"),
+             "f16": (f16, "measured in this run: torch.matmul fp16 8192^3, best of 10"),
+             "bf16": (float(file_peaks["bf16_tflops"]), f"{file_src}: dense bf16 burst (MEASURED_PEAKS.json)")}
+    hbm_gbs = float(file_peaks["hbm_gbs"])
+    peaks_rec = {"fp32_tflops": fp32, "fp32_clocks": sampler.window("fp32_peak"), "f16_tflops": f16,
+                 "f16_clocks": sampler.window("f16_peak"), "bf16_tflops": peaks["bf16"][0],
+                 "hbm_gbs": hbm_gbs, "source": {k: v[1] for k, v in peaks.items()}}
+
+    roofline, layer_roofline = rooflines(main, peaks, hbm_gbs, file_src)
     cpu = None
+    sub_cpu = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc = oracle_sample_rate(w, args.cpu_budget)
         cpu = {"value": rate, "unit": "GFLOP/s", "cores": 1, "kind": "oracle", "sample": desc}
+        for m in subs:
+            r, d = oracle_sample_rate(m.w, args.sub_cpu_budget)
+            sub_cpu[m.name] = {"value": r, "unit": "GFLOP/s", "cores": 1, "kind": "oracle", "sample": d}
 
     vs = None
     if name in PAGES_LAYER_MS:
         pages_ms, _ = PAGES_LAYER_MS[name]
-        vs = gflops / (flops / (pages_ms * 1e-3) / 1e9)
-
-    launch_us = empty_launch_us(dev, stream)
+        vs = gflops / (main.flops / (pages_ms * 1e-3) / 1e9)
 
     line = {
         "metric": METRIC, "value": gflops, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": main.ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": vs, "dtype": "f32" if pr.dtype == "f32" else f"{pr.dtype} storage, f32 arithmetic",
         "data": "synthetic (seeded numpy PCG64, random weights)",
-        "config": {"workload": name, "cell": pr.cell, "direction": pr.direction, "seq": pr.seq, "batch": pr.batch,
-                   "input": pr.input, "hidden": pr.hidden, "layout": pr.layout, "tensor_dtype": pr.dtype,
-                   "l2": "flushed between timed layer runs (256 MiB write, untimed)",
-                   "parallelism": f"replicas x{world}", "plan": plan},
-        "us_per_step": ms * 1e3 / max(pr.seq, 1), "steps_per_s": pr.seq / (ms * 1e-3) * world,
-        "kernels_ms": {"projection": proj_ms, "step": step_ms},
+        "config": config_of(name, pr, world), "plan": main.plan,
+        "us_per_step": main.ms * 1e3 / max(pr.seq, 1), "steps_per_s": pr.seq / (main.ms * 1e-3) * world,
+        "kernels_ms": {"projection": main.proj_ms, "step": main.step_ms},
         "roofline": roofline, "layer_roofline": layer_roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_gflops, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
-        "clocks": clocks, "gpu_launches": launches,
+        "clocks": main.clocks, "gpu_launches": main.launches,
+        "peaks": peaks_rec,
+        # the other configurations of the benchmark list, measured in this run
+        "workloads": {m.name: sub_record(m, peaks, hbm_gbs, file_src, world, sub_cpu.get(m.name)) for m in subs},
         # what one dependent launch per step would cost at least on this machine
         # (a 1-element kernel back to back on the stream), next to us_per_step
         "empty_launch_us": launch_us,
     }
     if vs is not None:
         line["vs_baseline_note"] = "value / the pages' %.1f ms layer on %s (other hardware: context)" % PAGES_LAYER_MS[name]
-    layer.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -539,7 +767,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded numpy PCG64, random weights)", "config": {"workload": name},
+            "data": "synthetic (seeded numpy PCG64, random weights)", "config": config_of(name, w.problem, world),
             "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": (f"each step: one oracle run of the workload cut to {seq_cut} of "
                                         f"{w.problem.seq} steps, {len(sample.rows)} of {w.problem.batch} rows")},

@@ -150,32 +150,53 @@ typedef struct rk_scratch {
 
 typedef struct rk_handle rk_handle;
 
-/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+/* Version of this ABI (major * 10000 + minor * 100 + patch).  No counterpart
+ * on the pages (their version is a package version). */
 int32_t rk_version(void);
 
-/* Create a handle.  No CUDA call is made until the first encode, so this
- * works without a GPU.  flags: the rk_create flag bits above.  *out receives
- * the handle. */
+/* Create a handle: the kernel family object of the web page "Recurrent
+ * layers" (`new RecurrentKernels(device)` in its C# example), which keeps the
+ * scratch it grows on demand (paragraph "Scratch").  The device is the CUDA
+ * device current at the first encode; no CUDA call is made until then, so
+ * this works without a GPU.  flags: the rk_create flag bits above (kernel
+ * choices; the pages' GpuKernelMode has no counterpart here since every
+ * kernel is deterministic, section "Arithmetic and determinism").  *out
+ * receives the handle, owned by the caller until rk_destroy.  Returns
+ * RK_ERR_ARG for out == NULL, RK_ERR_OOM if the host allocation fails. */
 rk_status rk_create(rk_handle** out, uint32_t flags);
 
 /* Wait for the handle's work on the streams it used, free its scratch and the
- * handle.  NULL is accepted. */
+ * handle (the disposal of the C# example's `using var rnn` on the web page
+ * "Recurrent layers"; the scratch is the family's own, paragraph "Scratch").
+ * NULL is accepted.  Caller-owned tensors and caller-placed scratch are not
+ * touched. */
 rk_status rk_destroy(rk_handle* h);
 
-/* Floats of projection scratch the problem needs (XwLength): D * S * N * G * H
- * for S, N > 0, else 0.  Returns -1 for an invalid problem. */
+/* Floats of projection scratch the problem needs: RecurrentKernels.XwLength
+ * of the web page "Recurrent layers", paragraph "Scratch" (the float32 Xw of
+ * section "How a layer runs", step 1): D * S * N * G * H for S, N > 0, else
+ * 0.  Host only.  Returns -1 for an invalid problem (p == NULL included). */
 int64_t rk_xw_length(const rk_problem* p);
 
-/* Floats of state scratch the problem needs (StateLength): 256 barrier
- * words, the double-buffered hidden state exchanged between blocks of the
- * step kernel, 2 * D * N * KP, and a region for r (.) h or the 16-bit copies
- * of h used by the tensor cores, D * (N + 128) * KP (KP = hidden rounded up to a
- * multiple of 128).  Returns -1 for an invalid problem. */
+/* Floats of state scratch the problem needs: StateLength of the web page
+ * "Recurrent layers", paragraph "Scratch".  The pages' state holds every
+ * step's output; here, where the steps run inside one kernel, it holds 256
+ * barrier words, the double-buffered hidden state exchanged between blocks of
+ * the step kernel, 2 * D * N * KP, and a region for r (.) h or the 16-bit
+ * copies of h used by the tensor cores, D * (N + 128) * KP (KP = hidden
+ * rounded up to a multiple of 128).  Host only.  Returns -1 for an invalid
+ * problem. */
 int64_t rk_state_length(const rk_problem* p);
 
-/* Host-only validation of a problem and its operands (sizes, offsets,
- * extents, options legal for the cell); makes no CUDA call.  Returns RK_OK or
- * the error encode would return, with rk_last_error set. */
+/* Host-only validation of a problem and its operands: the checks of the web
+ * page "Recurrent layers", paragraph "Scratch" (sizes, offsets and shapes in
+ * safe 64-bit arithmetic, an error naming LSTM / GRU / RNN and the argument)
+ * and section "Semantics", last item (peepholes, input_forget, initial_c and
+ * Y_c only for an LSTM, linear_before_reset only for a GRU; anything else is
+ * an error).  Makes no CUDA call.  Returns RK_OK, RK_ERR_SHAPE (the pages'
+ * GpuKernelShapeException), RK_ERR_UNSUPPORTED (sizes past 32-bit indexing)
+ * or RK_ERR_ARG (null handle, problem or operand list), with rk_last_error
+ * set. */
 rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops);
 
 /* Host-only check of a HOST copy of sequence_lens (web page "Recurrent
@@ -190,13 +211,24 @@ rk_status rk_validate(rk_handle* h, const rk_problem* p, const rk_operands* ops)
 rk_status rk_validate_lengths(rk_handle* h, const rk_problem* p, const int32_t* lens, int64_t n);
 
 /* Enqueue the whole layer on `stream` (a cudaStream_t; NULL = legacy default
- * stream): input projection, then one persistent step kernel that runs every
- * step and writes Y, Y_h, Y_c.  Asynchronous: returns after enqueueing.
- * scratch may be NULL.  All operand pointers are device pointers. */
+ * stream): `rnn.Encode(encoder, problem, tensors)` of the web page "Recurrent
+ * layers" (C# example), computing section "How a layer runs" steps 1-4 with
+ * the arithmetic of section "Arithmetic and determinism" and the rules of
+ * section "Semantics": the input projection, then one persistent step kernel
+ * that sets up the state, runs every step and writes Y, Y_h, Y_c.
+ * Asynchronous: returns after enqueueing.  scratch may be NULL (the handle's
+ * own, grown on demand) or place both regions (paragraph "Scratch").  All
+ * operand pointers are caller-owned device pointers, read or written only by
+ * the enqueued kernels.  Errors: the checks of rk_validate (nothing is
+ * launched); RK_ERR_UNSUPPORTED when no step kernel can be resident; RK_ERR_OOM
+ * when growing the scratch fails; RK_ERR_CUDA when a launch fails.  Batch = 0
+ * or hidden = 0 records nothing; Seq = 0 writes only Y_h / Y_c (the initial
+ * states or zeros). */
 rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops,
                     const rk_scratch* scratch, void* stream);
 
-/* Same layer with HOST operand pointers: copies the inputs to device buffers
+/* Same layer with HOST operand pointers (no counterpart on the pages, whose
+ * tensors are always device buffers): copies the inputs to device buffers
  * owned by the handle (grown on demand), encodes on `stream`, copies the
  * requested outputs back and synchronises the stream before returning.  X
  * and W are copied on `stream`; the operands only the step kernel reads (R,
@@ -209,17 +241,25 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops,
 rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* host_ops,
                          void* stream);
 
-/* Synchronise `stream`, read and clear the device status word of the handle:
- * RK_OK, or RK_ERR_TIMEOUT if a bounded barrier wait of the grid step kernel
- * gave up during a previous encode. */
+/* Synchronise `stream`, read and clear the device status word of the handle
+ * (and, once rk_encode_noalloc has run on the handle, the status word of its
+ * fixed array): RK_OK, or RK_ERR_TIMEOUT if a bounded device wait of a step
+ * kernel or of the tensor-core projection gave up during a previous encode;
+ * the outputs of that encode are then undefined.  The web page "Recurrent
+ * layers" has no counterpart: its design waits on nothing inside a launch
+ * (one pass per step, paragraph "Why a pass per step"), while this library's
+ * persistent kernels wait on the device, each wait bounded so that a launch
+ * that cannot finish reports RK_ERR_TIMEOUT instead of hanging. */
 rk_status rk_status_poll(rk_handle* h, void* stream);
 
-/* Nanoseconds (measured on the GPU's global timer) a device-side wait of the
+/* (No counterpart on the pages; see rk_status_poll.)
+ * Nanoseconds (measured on the GPU's global timer) a device-side wait of the
  * step kernel may spin before it gives up, sets the status word and lets the
  * kernel wind down; default 2e9 (2 s).  limit must be >= 1. */
 rk_status rk_set_wait_limit(rk_handle* h, int64_t limit);
 
-/* Run the step kernels' bounded device waits against a grid barrier and an
+/* (No counterpart on the pages; see rk_status_poll.)
+ * Run the step kernels' bounded device waits against a grid barrier and an
  * mbarrier that nothing completes (one CTA, no other memory touched): each
  * must give up after timeout_ns and set the handle's status word.  Returns
  * RK_OK once the check kernel is enqueued on `stream`; rk_status_poll then
@@ -247,11 +287,16 @@ rk_status rk_selftest_timeout(rk_handle* h, void* stream, int64_t timeout_ns);
  * which keeps the previous call's contents: the call clears what must start
  * at zero (barrier counters, status word).  Calls whose work overlaps on the
  * GPU (other streams, other host threads) race on the array and give
- * undefined results: order them on one stream.  A device wait that gives up
- * is not reported to rk_status_poll on this path. */
+ * undefined results: order them on one stream.  Both resets are enqueued
+ * before the call's first kernel, so after the call the array's status word
+ * holds the give-ups of both kernels: rk_status_poll on the same handle reads
+ * and clears it (RK_ERR_TIMEOUT: the outputs of that call are undefined).
+ * With rk_set_profiling on, the call records its projection and step events
+ * like rk_encode. */
 rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands* ops, void* stream);
 
-/* Kernel timing for measurement: with enabled != 0 every later encode records
+/* (No counterpart on the pages, which time whole layers.)
+ * Kernel timing for measurement: with enabled != 0 every later encode records
  * CUDA events (on its stream) around its projection launch and its step
  * launch; rk_last_timings then waits for them and returns the two durations
  * of the most recent encode in milliseconds (-1 for a launch that did not
@@ -259,14 +304,21 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
 rk_status rk_set_profiling(rk_handle* h, int32_t enabled);
 rk_status rk_last_timings(rk_handle* h, float* projection_ms, float* step_ms);
 
-/* Message of the last failed call on this handle ("" if none).  The string
- * belongs to the handle. */
+/* Message of the last failed call on this handle ("" if none): the text the
+ * web page "Recurrent layers" gives its shape errors (paragraph "Scratch":
+ * it names LSTM / GRU / RNN and the argument), e.g. "GRU: R: offset 0 +
+ * extent 768 exceeds buffer length 5".  The string belongs to the handle and
+ * stays valid until its next call. */
 const char* rk_last_error(const rk_handle* h);
 
-/* Number of kernels this handle has launched so far (all encodes). */
+/* Number of kernels this handle has launched so far (all encodes): the
+ * evidence that a layer costs a fixed number of launches whatever its
+ * sequence length, where the web page "Recurrent layers" spends one pass per
+ * step (section "How a layer runs", step 3; paragraph "What a step costs"). */
 uint64_t rk_launch_count(const rk_handle* h);
 
-/* Describe the plan encode would use for a problem (for logs and tests): a
+/* (No counterpart on the pages.)
+ * Describe the plan encode would use for a problem (for logs and tests): a
  * NUL-terminated text such as "proj=simt_f32 step=cluster16 nb=1 ..." written
  * into buf (at most len bytes).  Host only. */
 rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t len);

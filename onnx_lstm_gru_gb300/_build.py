@@ -17,6 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "librk.so")
+# measurement aid of the benchmark (float32 FMA peak), its own shared object
+PROBE_SRC = os.path.join(PKG, "probe", "fma_peak.cu")
+PROBE_LIB = os.path.join(BUILD, "libfmapeak.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -79,6 +82,13 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
         if r.returncode != 0:
             raise RuntimeError(f"link of librk.so failed:\n{r.stderr}")
         os.replace(tmp, LIB)
+    if not os.path.exists(PROBE_LIB) or os.path.getmtime(PROBE_LIB) < os.path.getmtime(PROBE_SRC):
+        tmp = PROBE_LIB + f".{os.getpid()}.tmp"
+        cmd = [nvcc, *ARCH, *CFLAGS, "-shared", PROBE_SRC, "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"build of libfmapeak.so failed:\n{r.stderr}")
+        os.replace(tmp, PROBE_LIB)
     return LIB
 
 

@@ -32,6 +32,9 @@ struct rk_handle {
   int sms = 152;
   int smem_optin = 232448;
   int* status = nullptr;
+  // status word of the fixed array rk_encode_noalloc last used (device
+  // address; null until that entry point has run on this handle)
+  int* noalloc_status = nullptr;
   float* xw = nullptr;
   size_t xw_cap = 0;
   float* state = nullptr;
@@ -691,7 +694,7 @@ rk_status rk_describe_plan(rk_handle* h, const rk_problem* p, char* buf, int64_t
     return RK_OK;
   }
   if ((st = plan_step(h, p, &sp, &pl, have_dev)) != RK_OK) return st;
-  const bool tc = p->dtype != RK_F32 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input % 8 == 0;
+  const bool tc = p->dtype != RK_F32 && !(h->flags & RK_FORCE_SIMT_PROJECTION) && p->input > 0 && p->input % 8 == 0;
   rk::ProjParams pp{};
   pp.M = (int)(p->seq * p->batch);
   const bool fused = fused_projection(h, p, pl, pp, p->seq > 0 && p->input > 0, nullptr, nullptr).on;
@@ -899,6 +902,14 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   }
   float* state = scratch;            // 256-byte aligned start of the array
   float* xw = scratch + need_state;  // after the state region
+  // the array keeps the previous call's contents: the barrier counters and
+  // the status word must start at zero, before either kernel can touch them
+  // (the tensor-core projection also reports a wait that gave up there)
+  e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return cuda_fail(h, p, "scratch reset", e);
+  h->noalloc_status = status;
+  h->ev_proj = h->ev_step = false;
   if (sp.T > 0 && need_xw > 0) {
     rk::ProjParams pp{};
     pp.M = (int)(p->seq * p->batch);
@@ -910,9 +921,12 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
     pp.Xw = xw;
     pp.dtype = p->dtype;
     pp.sms = plan_h.sms;
+    if (h->profiling) cudaEventRecord(h->ev[0], stream);
     const bool tc = !(h->flags & RK_FORCE_SIMT_PROJECTION) && rk::projection_tc_supported(pp);
     e = tc ? rk::launch_projection_tc(pp, status, h->timeout_ns, stream) : rk::launch_projection_simt(pp, stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "projection launch", e);
+    if (h->profiling) cudaEventRecord(h->ev[1], stream);
+    h->ev_proj = h->profiling;
     h->launches += 1;
   }
   sp.R = tptr(ops->R, eb);
@@ -930,16 +944,14 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
   sp.status = status;
   sp.timeout_ns = h->timeout_ns;
-  // the array keeps the previous call's contents: the barrier counters and
-  // the status word must start at zero
-  e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return cuda_fail(h, p, "scratch reset", e);
+  if (h->profiling) cudaEventRecord(h->ev[2], stream);
   e = step_dispatch(p->cell, sp, pl, stream, nullptr);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return cuda_fail(h, p, "step kernel launch", e);
   }
+  if (h->profiling) cudaEventRecord(h->ev[3], stream);
+  h->ev_step = h->profiling;
   h->launches += 1;
   return RK_OK;
 }
@@ -1088,12 +1100,17 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
 
 rk_status rk_status_poll(rk_handle* h, void* stream_ptr) {
   if (h == nullptr) return RK_ERR_ARG;
-  if (!h->dev_ready) return RK_OK;
+  if (!h->dev_ready && h->noalloc_status == nullptr) return RK_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  int v = 0;
+  int v = 0, w = 0;
   cudaError_t e = cudaStreamSynchronize(stream);
-  if (e == cudaSuccess) e = cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
+  if (e == cudaSuccess && h->dev_ready) e = cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h->dev_ready) e = cudaMemset(h->status, 0, sizeof(int));
+  // the fixed array of rk_encode_noalloc has a status word of its own
+  if (e == cudaSuccess && h->noalloc_status != nullptr)
+    e = cudaMemcpy(&w, h->noalloc_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h->noalloc_status != nullptr) e = cudaMemset(h->noalloc_status, 0, sizeof(int));
+  v |= w;
   if (e != cudaSuccess) {
     h->last_error = std::string("recurrent: status poll: ") + cudaGetErrorName(e);
     return RK_ERR_CUDA;

@@ -682,3 +682,123 @@ def test_tensor_core_step_kernel(cell, H, N, direction, layout, opts, dtype):
     for k in got:
         if k.endswith("_raw"):
             assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
+
+
+# ------------------------------------------------------------------ lengths out of range and an empty input
+
+# Every step-kernel family, each as (flags, cell / size overrides, the plan
+# text that proves which kernel ran).  The recurrent-layers page ("Semantics")
+# runs a length above Seq as Seq, a length of 0 as no step (Y_h = Y_c = 0);
+# a negative length is read as 0.  The kernels clamp the lengths they read on
+# the device, so every family is given all of these at once.
+FAMILIES = {
+    "fast": (0, dict(N=6, H=40), "step=fast"),
+    "cluster": (rk.RK_FORCE_GENERAL_STEP, dict(N=6, H=40), "step=cluster"),
+    "grid": (rk.RK_FORCE_GRID_STEP, dict(N=6, H=40), "step=grid"),
+    "tensor_small": (TC, dict(N=9, H=96), "variant=small"),
+    "tensor_cluster": (TC, dict(N=40, H=128), "variant=cluster"),
+    "tensor_pairs": (TC | rk.RK_SEPARATE_PROJECTION, dict(N=16, H=576), "variant=pairs"),
+    "tensor_rows": (TC | rk.RK_SEPARATE_PROJECTION, dict(N=130, H=96), "variant=rows"),
+    "tensor_fused": (TC, dict(N=16, H=576), "proj=fused step=tensor"),
+}
+FAMILY_DTYPES = {"fast": ("f32", "f16"), "cluster": ("f32", "f16"), "grid": ("f32", "bf16")}
+TENSOR_ONLY_CELLS = ("lstm", "gru1", "rnn")  # GRU lbr 0 with many rows runs on the SIMT cluster kernel
+
+
+def _family_cases():
+    out = []
+    for fam in FAMILIES:
+        dts = FAMILY_DTYPES.get(fam, ("f16",))
+        cells = ("lstm", "gru0", "gru1", "rnn") if fam in FAMILY_DTYPES or fam == "tensor_small" else TENSOR_ONLY_CELLS
+        for dt in dts:
+            for c in cells:
+                out.append((fam, dt, c))
+    return out
+
+
+def out_of_range_lengths(S, N):
+    """Negative, zero, in-range, exactly Seq and above-Seq lengths, cycled over N rows."""
+    pattern = [-3, S + 4, 0, 2, S, S - 1, -1, 1, 2 * S + 9, S // 2]
+    return [pattern[i % len(pattern)] for i in range(N)]
+
+
+def family_scale(pr):
+    # weights of scale a give a recurrent gain of about a * sqrt(H / 3); keep
+    # it below 1 so the 16-bit roundings of h are not amplified past the
+    # tolerance (a chaotic layer would defeat any fixed bound)
+    return min(0.15, float(np.sqrt(2.0 / pr.hidden)))
+
+
+def family_problem(fam, dtype, cellkey, S=7, I=24, direction="bidirectional"):
+    flags, kw, want = FAMILIES[fam]
+    cell = cellkey[:3] if cellkey.startswith("gru") else cellkey
+    lbr = 1 if cellkey == "gru1" else 0
+    pr = rk.Problem(cell, seq=S, batch=kw["N"], input=I, hidden=kw["H"], direction=direction, dtype=dtype,
+                    linear_before_reset=lbr)
+    return pr, flags, want
+
+
+@pytest.mark.parametrize("fam,dtype,cellkey", _family_cases())
+def test_out_of_range_lengths_every_kernel(fam, dtype, cellkey):
+    """sequence_lens holding negative values, 0, in-range values, Seq and
+    values above Seq: every step-kernel family matches the oracle (which
+    clamps the same way) element by element, with Y exactly 0 past each
+    clamped length and Y_h / Y_c = 0 for rows of length <= 0."""
+    pr, flags, want = family_problem(fam, dtype, cellkey)
+    assert want in layer(flags).plan(pr), layer(flags).plan(pr)
+    lens = out_of_range_lengths(pr.seq, pr.batch)
+    inp = rand_inputs(pr, seed=500 + pr.batch + pr.hidden, lens=lens, scale=family_scale(pr))
+    got = run_gpu(pr, inp, flags=flags)
+    compare(pr, got, run_oracle(pr, inp), lens)
+    dead = np.clip(lens, 0, pr.seq) == 0
+    yh = got["Y_h"] if pr.layout == 1 else got["Y_h"].transpose(1, 0, 2)  # [N, D, H]
+    assert np.all(yh[dead] == 0.0), "rows of length <= 0 end with Y_h = 0"
+
+
+@pytest.mark.parametrize("fam,dtype,cellkey", _family_cases())
+def test_empty_input_every_kernel(fam, dtype, cellkey):
+    """A layer with input size 0: X and W are empty, every xw term is the
+    empty sum 0, so the recurrence runs on R, the biases and the initial
+    state alone.  Matches the oracle on every step-kernel family."""
+    pr, flags, want = family_problem(fam, dtype, cellkey, I=0)
+    plan = layer(flags).plan(pr)
+    assert want.replace("proj=fused ", "") in plan, plan
+    lens = [pr.seq - (i % 3) for i in range(pr.batch)]
+    inp = rand_inputs(pr, seed=600 + pr.batch + pr.hidden, lens=lens, scale=family_scale(pr))
+    assert inp["X"].size == 0 and inp["W"].size == 0
+    got = run_gpu(pr, inp, flags=flags)
+    compare(pr, got, run_oracle(pr, inp), lens)
+    assert np.all(np.isfinite(got["Y"]))
+
+
+@pytest.mark.parametrize("lens_kind", ["all_above_seq", "mixed"])
+def test_fused_projection_xw_ring_out_of_range_lengths(lens_kind):
+    """The tensor-core launch that computes its own projection keeps Xw in an
+    L2 ring only when every row has the same length after clamping: every
+    length above Seq (all clamp to Seq) takes the ring, a mix of negative,
+    zero and above-Seq lengths takes the whole scratch.  Both are
+    bit-identical to the projection's own launch and match the oracle on
+    sampled rows."""
+    S, N, H = 40, 64, 576
+    pr = rk.Problem("lstm", seq=S, batch=N, input=72, hidden=H, direction="bidirectional", dtype="f16")
+    assert "proj=fused step=tensor" in layer().plan(pr)
+    if lens_kind == "all_above_seq":
+        lens = [S + 1 + (i % 5) for i in range(N)]
+    else:
+        lens = out_of_range_lengths(S, N)
+    inp = rand_inputs(pr, seed=S + N + H, lens=lens, scale=0.04)
+    got = run_gpu(pr, inp)
+    sep = run_gpu(pr, inp, flags=rk.RK_SEPARATE_PROJECTION)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], sep[k]), k
+    rows = [0, 1, 2, 4, N - 1]
+    sub = rk.Problem("lstm", seq=S, batch=len(rows), input=72, hidden=H, direction="bidirectional", dtype="f16")
+    sinp = dict(inp)
+    sinp["X"] = inp["X"][:, rows]
+    sinp["sequence_lens"] = inp["sequence_lens"][rows]
+    for k in ("initial_h", "initial_c"):
+        sinp[k] = inp[k][:, rows]
+    ref = run_oracle(sub, sinp)
+    gsub = {"Y": got["Y"][:, :, rows], "Y_h": got["Y_h"][:, rows], "Y_c": got["Y_c"][:, rows]}
+    compare(sub, gsub, ref, sinp["sequence_lens"])
