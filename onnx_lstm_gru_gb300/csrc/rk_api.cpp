@@ -286,6 +286,15 @@ FusedProj fused_projection(const rk_handle* h, const rk_problem* p, const StepPl
   return f;
 }
 
+// Floats at the start of the state scratch that must be zero when the step
+// kernel starts: the header (barrier counters, readiness counters), and for
+// the tensor-core kernel with teams of 16-unit CTAs its region counters.
+int64_t zeroed_state_floats(const StepPlan& pl, int D) {
+  int64_t n = rk::kStateHeader;
+  if (pl.kind == rk::kStepTensor && pl.J == 16) n += (int64_t)D * pl.teams_per_dir * rk::kTcRegionLines * 32;
+  return n;
+}
+
 // Launch (or, with resident != nullptr, size) the step kernel of a plan.
 cudaError_t step_dispatch(int32_t cell, const StepParams& sp, const StepPlan& pl, cudaStream_t stream, int* resident) {
   if (pl.kind == rk::kStepTensor) return rk::step_tc_entry(sp, pl, stream, resident, sp.rhglob);
@@ -800,7 +809,7 @@ rk_status encode_validated(rk_handle* h, const rk_problem* p, const rk_operands*
   sp.status = h->status;
   sp.timeout_ns = h->timeout_ns;
   if (pl.kind == rk::kStepGrid || pl.kind == rk::kStepTensor) {
-    cudaError_t e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
+    cudaError_t e = cudaMemsetAsync(state, 0, (size_t)zeroed_state_floats(pl, sp.D) * sizeof(float), stream);
     if (e != cudaSuccess) return cuda_fail(h, p, "barrier reset", e);
   }
   if (step_wait != nullptr) {
@@ -905,7 +914,7 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   // the array keeps the previous call's contents: the barrier counters and
   // the status word must start at zero, before either kernel can touch them
   // (the tensor-core projection also reports a wait that gave up there)
-  e = cudaMemsetAsync(state, 0, rk::kStateHeader * sizeof(float), stream);
+  e = cudaMemsetAsync(state, 0, (size_t)zeroed_state_floats(pl, sp.D) * sizeof(float), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), stream);
   if (e != cudaSuccess) return cuda_fail(h, p, "scratch reset", e);
   h->noalloc_status = status;

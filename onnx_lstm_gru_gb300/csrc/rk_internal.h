@@ -15,6 +15,10 @@ constexpr int kStateHeader = 256; // floats reserved at the start of the state s
 // uses when it computes the projection itself (16 MB per direction at
 // 4096 columns: it stays in L2)
 constexpr int kXwRingTiles = 8;
+// Region counters of the tensor-core step kernel's teams (16 units per CTA):
+// lines of 32 words per team, one per region of 128 k, placed at the start of
+// the state scratch's exchange area and zeroed before each launch.
+constexpr int kTcRegionLines = 32;
                                   // for the grid step kernel's barrier counters
 
 struct ActSlot {
