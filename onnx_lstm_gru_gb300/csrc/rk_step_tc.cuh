@@ -129,6 +129,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   d |= (uint64_t)2 << 61;
   return d;
 }
+// TMEM columns to allocate for `cols` accumulator columns: a power of two, at least 32.
+__host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t cols) {
+  uint32_t n = 32;
+  while (n < cols) n <<= 1;
+  return n;
+}
 // kind::f16, D float32, both K-major, M = 128, N = n; the A/B type fields
 // (Half or bfloat16, Elem<E>::kMmaAB) are or-ed in by the caller.
 __device__ __forceinline__ uint32_t idesc_f16(int n) {
@@ -232,9 +238,13 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   constexpr int UH = PAIR ? SJT / 4 : SJT / 2;  // units per gate thread: 4 or 8
   constexpr int NCOL = UH * G;         // accumulator values per gate thread
   constexpr int BPR = PAIR ? 2 : 1;    // k blocks per region
-  constexpr uint32_t kOddCol = SJT * 4;  // odd-block accumulator (>= NR columns after the even one)
-  constexpr uint32_t kTmemCols = 2 * kOddCol;  // 128 or 256
-  static_assert(NR <= (int)kOddCol && 2 * kOddCol <= 512, "accumulators fit the allocation");
+  // odd-block accumulator right after the even one, so that with paired
+  // blocks one MMA of N = 2 NR (R's blocks 2r and 2r + 1 are adjacent in
+  // shared memory) fills both
+  constexpr uint32_t kOddCol = PAIR ? (uint32_t)NR : (uint32_t)SJT * 4;
+  constexpr uint32_t kTmemCols = tmem_cols_for(2 * kOddCol);  // a power of two >= 32
+  static_assert(NR <= (int)kOddCol && 2 * kOddCol <= kTmemCols && kTmemCols <= 512, "accumulators fit the allocation");
+  static_assert(!PAIR || (NR % 8 == 0 && 2 * NR <= 256), "paired product: N = 2 NR, whole 8-row swizzle groups");
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   // projection of the layer computed by the blocks past the recurrence's
@@ -677,6 +687,13 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       // only the start-address field (address / 16, bits 0-13) differs
       // between the MMAs' descriptors; every address stays below 256 KB
       const uint32_t idesc = idesc_f16(NR) | Elem<E>::kMmaAB;
+      // paired blocks with an even block count: every region has both
+      // blocks, and one N = 2 NR product per 16 k fills the even and the odd
+      // accumulator at once (fewer, wider MMAs: the issue cost per MMA
+      // hardly grows with N); each accumulator gets the same products in
+      // the same order as with two N = NR products
+      const bool wide = PAIR && (KB % 2 == 0);
+      const uint32_t idesc2 = idesc_f16(2 * NR) | Elem<E>::kMmaAB;
       const uint64_t adesc0 = desc_sw128(su32(sRing));
       const uint64_t bdesc0 = desc_sw128(su32(sR));
       constexpr uint64_t kK16 = 32 >> 4;                      // 16 elements of k
@@ -706,6 +723,18 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
           // the first MMA of each accumulator in a step overwrites it; with
           // an odd number of k blocks the last region has no odd block, and
           // it may come first in this CTA's order
+          if (wide) {
+            tc_mma(tmem_acc, ad, bd, idesc2, pos != 0 ? 1u : 0u);
+            tc_mma(tmem_acc, ad + kK16, bd + kK16, idesc2, 1u);
+            tc_mma(tmem_acc, ad + 2 * kK16, bd + 2 * kK16, idesc2, 1u);
+            tc_mma(tmem_acc, ad + 3 * kK16, bd + 3 * kK16, idesc2, 1u);
+            tc_commit(su32(&bars[SMAXST + st]));
+            if (++st == NST) {
+              st = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
           tc_mma(tmem_acc, ad, bd, idesc, pos != 0 ? 1u : 0u);
           tc_mma(tmem_acc, ad + kK16, bd + kK16, idesc, 1u);
           tc_mma(tmem_acc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
