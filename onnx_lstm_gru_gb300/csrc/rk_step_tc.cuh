@@ -209,11 +209,6 @@ __host__ __device__ inline TcSmem tc_smem_layout(int G, int H, int stages, int s
 __device__ __forceinline__ size_t h16_region(const StepParams& p, int buf, int d, int team_in_dir, int region, int NREG) {
   return ((((size_t)buf * p.D + d) * p.teams_per_dir + team_in_dir) * NREG + region) * (size_t)(SSTAGE / 2);
 }
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -487,9 +482,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
   // each CTA published h_s after its own copies of h_{s-1}, the buffer being
   // overwritten, had landed.  Each counter sits on a 128-byte line of its own
   // (in the state scratch after the header, zeroed before the launch): the
-  // team's CTAs poll them all every step, and counters that shared a line
-  // were measured to delay their detection (median 2.3 against 1.8 us after
-  // the last release on the bidirectional 512 x 64 x 1024 Half layer).
+  // team's CTAs poll them all every step, and per-CTA flags that shared two
+  // lines were measured to delay their detection (median 2.3 against 1.8 us
+  // after the last release on the bidirectional 512 x 64 x 1024 Half layer).
   constexpr int RPB = SK * BPR / SJT;  // CTAs owning one region: 4 or 8 (a multiple of 4)
   unsigned* rctr = p.hglob == nullptr ? nullptr
                                       : reinterpret_cast<unsigned*>(p.hglob) + (size_t)team * kTcRegionLines * 32;
@@ -606,8 +601,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
 
   if (warp == 8) {
     // ---------------- producer warp: lane l polls the counter of region l
-    // (relaxed loads; an acquire fence once it is complete), then one bulk
-    // copy per ready region, in this CTA's order
+    // with acquire loads (as fast as relaxed ones here, while a relaxed poll
+    // followed by an acquire fence cost about 0.8 us more per detection),
+    // then one bulk copy per ready region, in this CTA's order
     int armed[SMAXST];
     for (int i = 0; i < SMAXST; ++i) armed[i] = -1;
     int st = 0;
@@ -631,8 +627,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
         bool rd = true;
         if (!CLU && lane < NREG && !((taken >> lane) & 1u)) {
           const int owners = min(C, (lane + 1) * RPB) - lane * RPB;
-          rd = ld_relaxed_gpu(rctr + (size_t)lane * 32) >= (unsigned)owners * want;
-          if (rd) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          rd = ld_acquire_gpu(rctr + (size_t)lane * 32) >= (unsigned)owners * want;
         }
         const unsigned ready = __ballot_sync(0xffffffffu, rd) | taken;
         int end = pos;
