@@ -263,6 +263,206 @@ cudaError_t launch_pipe_for(const ProjParams& p, cudaStream_t s, int rows, bool 
   return one_wave ? launch_pipe_rows<T, true, 6>(p, s, rows) : launch_pipe_rows<T, false, 4>(p, s, rows);
 }
 
+// ---------------------------------------------------------------------------
+// Small grids (web page "Matrix multiplication (Gemm)", section "Small grids
+// and few rows").  A product whose tiles cannot fill the GPU leaves most SMs
+// idle while each busy one walks a long k; both variants below fix the order
+// in which an element's terms are added, so results stay bit-identical from
+// run to run.
+//
+// Split k: each CTA owns a TM x 32 tile of Xw and its 8 warps split k into 4
+// ranges (a multiple of 32 terms, at least 64 each) x 2 column halves.  Warp
+// (r, c) copies its range of the tile's X rows (shared with the other half)
+// and W columns into shared memory with cp.async, chains every one of its
+// TM / 8 x 4 outputs over its range in increasing k, and stores the range
+// sums; then each output is the sum of its 4 range sums in range order.  The
+// ranges replace the page's scratch planes and second pass by shared memory
+// inside the CTA, so the whole product is still one launch.
+constexpr int SPLIT_RANGES = 4, SPLIT_TN = 32, SPLIT_THREADS = 2 * SPLIT_RANGES * 32;
+
+template <typename T>
+struct SplitLayout {
+  static constexpr int pad = 16 / (int)sizeof(T);  // 16 bytes between rows: X rows of a quarter warp hit distinct banks
+};
+
+// Dynamic shared memory of the split-k kernel.
+template <typename T>
+size_t split_smem(int TM, int K) {
+  const size_t ld = (size_t)K + SplitLayout<T>::pad;
+  return ((size_t)TM + SPLIT_TN) * ld * sizeof(T) + (size_t)SPLIT_RANGES * TM * SPLIT_TN * sizeof(float);
+}
+
+template <typename T, int TM>
+__global__ void __launch_bounds__(SPLIT_THREADS) proj_split_kernel(int M, int N, int K, const T* __restrict__ X,
+                                                                   const T* __restrict__ W, float* __restrict__ Xw) {
+  static_assert(TM % 8 == 0 && TM >= 8 && TM <= 40, "tile rows: 8 to 40 in steps of 8");
+  // the step kernel after this one may be launched early (programmatic
+  // dependent launch); it waits for this grid before reading Xw
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ __align__(16) unsigned char ssm[];
+  constexpr int E = 16 / (int)sizeof(T);  // elements per 16-byte copy
+  constexpr int RI = TM / 8;              // rows per lane
+  const int LD = K + SplitLayout<T>::pad;
+  T* Xs = reinterpret_cast<T*>(ssm);                    // [TM][LD]
+  T* Ws = Xs + (size_t)TM * LD;                         // [32][LD]
+  float* Ps = reinterpret_cast<float*>(Ws + (size_t)SPLIT_TN * LD);  // [ranges][TM][32]
+  const int d = blockIdx.z;
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * SPLIT_TN;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = warp >> 1, ch = warp & 1;  // k range, column half
+  // range r: [k0, k1), ranges a multiple of 32 terms (the last may be shorter)
+  const int KR = ((K + SPLIT_RANGES - 1) / SPLIT_RANGES + 31) & ~31;
+  const int k0 = min(K, r * KR), k1 = min(K, k0 + KR);
+  const T* Wd = W + (size_t)d * N * K;
+  // copies: X rows of this column half's parity, W columns of this half
+  const int nch = (k1 - k0) / E;  // K is a multiple of E
+  for (int c = lane; c < (TM / 2 + 16) * nch; c += 32) {
+    const int row = c / nch, kk = k0 + (c % nch) * E;
+    const bool isX = row < TM / 2;
+    const int rr = isX ? 2 * row + ch : ch * 16 + (row - TM / 2);
+    const int g = (isX ? m0 : n0) + rr;
+    const bool ok = g < (isX ? M : N);
+    const T* src = (isX ? X : Wd) + (size_t)(ok ? g : 0) * K + kk;
+    T* dst = (isX ? Xs : Ws) + (size_t)rr * LD + kk;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(ok ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  // the two warps of range r read each other's X rows
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + r) : "memory");
+  const int rr0 = lane >> 2, cc = lane & 3;
+  float acc[RI][4];
+#pragma unroll
+  for (int i = 0; i < RI; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int k = k0; k < k1; k += 4) {
+    float4 xv[RI], wv[4];
+#pragma unroll
+    for (int i = 0; i < RI; ++i) xv[i] = load4_row<T>(Xs + (size_t)(rr0 + 8 * i) * LD + k);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wv[j] = load4_row<T>(Ws + (size_t)(ch * 16 + cc + 4 * j) * LD + k);
+#pragma unroll
+    for (int i = 0; i < RI; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float a = acc[i][j];
+        a = fmaf(xv[i].x, wv[j].x, a);
+        a = fmaf(xv[i].y, wv[j].y, a);
+        a = fmaf(xv[i].z, wv[j].z, a);
+        a = fmaf(xv[i].w, wv[j].w, a);
+        acc[i][j] = a;
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < RI; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) Ps[((size_t)r * TM + rr0 + 8 * i) * SPLIT_TN + ch * 16 + cc + 4 * j] = acc[i][j];
+  __syncthreads();
+  float* out = Xw + (size_t)d * M * N;
+  for (int e = tid; e < TM * SPLIT_TN; e += SPLIT_THREADS) {
+    const int row = e / SPLIT_TN, col = e % SPLIT_TN;
+    const int m = m0 + row, n = n0 + col;
+    if (m >= M || n >= N) continue;
+    float v = Ps[(size_t)row * SPLIT_TN + col];
+#pragma unroll
+    for (int q = 1; q < SPLIT_RANGES; ++q) v += Ps[((size_t)q * TM + row) * SPLIT_TN + col];
+    out[(size_t)m * N + n] = v;
+  }
+}
+
+template <typename T, int TM>
+cudaError_t launch_split_tm(const ProjParams& p, cudaStream_t s) {
+  const size_t smem = split_smem<T>(TM, p.K);
+  auto kern = proj_split_kernel<T, TM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.N + SPLIT_TN - 1) / SPLIT_TN), (unsigned)((p.M + TM - 1) / TM), (unsigned)p.D);
+  kern<<<grid, SPLIT_THREADS, smem, s>>>(p.M, p.N, p.K, static_cast<const T*>(p.X), static_cast<const T*>(p.W), p.Xw);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_split(const ProjParams& p, cudaStream_t s, int tm) {
+  switch (tm) {
+    case 8: return launch_split_tm<T, 8>(p, s);
+    case 16: return launch_split_tm<T, 16>(p, s);
+    case 24: return launch_split_tm<T, 24>(p, s);
+    case 32: return launch_split_tm<T, 32>(p, s);
+    default: return launch_split_tm<T, 40>(p, s);
+  }
+}
+
+// Tile height of the split-k kernel: the smallest (8 to 40 rows) whose tiles
+// fit one wave of one CTA per SM and whose operands fit shared memory; 0 when
+// none does (or k is too short to cut into 4 ranges of at least 64 terms).
+int split_rows_for(const ProjParams& p, int sms, int eb) {
+  if (p.K < SPLIT_RANGES * 64) return 0;
+  const long long col_tiles = (long long)((p.N + SPLIT_TN - 1) / SPLIT_TN) * p.D;
+  for (int tm = 8; tm <= 40; tm += 8) {
+    const long long tiles = col_tiles * ((p.M + tm - 1) / tm);
+    const size_t smem = eb == 4 ? split_smem<float>(tm, p.K) : split_smem<__half>(tm, p.K);
+    if (tiles <= sms && smem <= 200 * 1024) return tm;
+  }
+  return 0;
+}
+
+// Few rows: at most four rows of X (a layer of one or a few steps of a small
+// batch, e.g. decoding one step at a time).  W is stored N x K, so, as the
+// page does for that storage, a CTA owns 8 columns, one warp per column, and
+// the 32 lanes read consecutive k (lane l takes k = 128 i + 4 l ... + 3, four
+// consecutive terms per 8- or 16-byte load): W is streamed once.  Every lane
+// chains its terms in increasing k, and one lane per row adds the 32 lane
+// sums in lane order through shared memory.
+template <typename T, int MR>
+__global__ void __launch_bounds__(256) proj_rows_kernel(int M, int N, int K, const T* __restrict__ X,
+                                                        const T* __restrict__ W, float* __restrict__ Xw) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float sums[8][MR][32];
+  const int d = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp;
+  float acc[MR];
+#pragma unroll
+  for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
+  if (n < N) {
+    const T* wrow = W + ((size_t)d * N + n) * K;
+    for (int k = 4 * lane; k < K; k += 128) {
+      const float4 w = load4_row<T>(wrow + k);
+#pragma unroll
+      for (int m = 0; m < MR; ++m) {
+        if (m >= M) break;
+        const float4 x = load4_row<T>(X + (size_t)m * K + k);
+        float a = acc[m];
+        a = fmaf(x.x, w.x, a);
+        a = fmaf(x.y, w.y, a);
+        a = fmaf(x.z, w.z, a);
+        a = fmaf(x.w, w.w, a);
+        acc[m] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MR; ++m) sums[warp][m][lane] = acc[m];
+  __syncwarp();
+  if (n < N && lane < M) {
+    float v = sums[warp][lane][0];
+    for (int l = 1; l < 32; ++l) v += sums[warp][lane][l];
+    Xw[((size_t)d * M + lane) * N + n] = v;
+  }
+}
+
+template <typename T>
+cudaError_t launch_rows(const ProjParams& p, cudaStream_t s) {
+  dim3 grid((unsigned)((p.N + 7) / 8), (unsigned)p.D, 1);
+  if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+  proj_rows_kernel<T, 4><<<grid, 256, 0, s>>>(p.M, p.N, p.K, static_cast<const T*>(p.X), static_cast<const T*>(p.W),
+                                               p.Xw);
+  return cudaGetLastError();
+}
+
 // Tile height: the SM that gets the most tiles sets the time, so take the
 // height (8 to 32 rows) that minimises rows x tiles-per-SM, counting 4 rows'
 // worth of fixed cost per tile (the loads of W, the prologue).  A grid just
@@ -289,11 +489,25 @@ cudaError_t launch_projection_simt(const ProjParams& p, cudaStream_t s) {
   const int eb = p.dtype == 0 ? 4 : 2;
   const bool aligned = (reinterpret_cast<uintptr_t>(p.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
                        ((size_t)p.K * eb) % 16 == 0 && p.K > 0;
+  // few rows: 4-element loads need 4-element alignment of both bases and of K
+  const bool aligned4 = (reinterpret_cast<uintptr_t>(p.X) % (4 * eb) == 0) &&
+                        (reinterpret_cast<uintptr_t>(p.W) % (4 * eb) == 0) && p.K % 4 == 0 && p.K > 0;
+  if (p.M <= 4 && aligned4) {
+    if (p.dtype == 0) return launch_rows<float>(p, s);
+    if (p.dtype == 2) return launch_rows<__nv_bfloat16>(p, s);
+    return launch_rows<__half>(p, s);
+  }
   if (aligned) {
     int dev = 0, sms = p.sms;
     if (sms <= 0) {
       sms = 148;
       if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int tm = split_rows_for(p, sms, eb);
+    if (tm > 0) {
+      if (p.dtype == 0) return launch_split<float>(p, s, tm);
+      if (p.dtype == 2) return launch_split<__nv_bfloat16>(p, s, tm);
+      return launch_split<__half>(p, s, tm);
     }
     const long long col_tiles = (long long)((p.N + PBN - 1) / PBN) * p.D;
     const int rows = pipe_rows_for(p.M, col_tiles, sms);

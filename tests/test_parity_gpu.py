@@ -802,3 +802,58 @@ def test_fused_projection_xw_ring_out_of_range_lengths(lens_kind):
     ref = run_oracle(sub, sinp)
     gsub = {"Y": got["Y"][:, :, rows], "Y_h": got["Y_h"][:, rows], "Y_c": got["Y_c"][:, rows]}
     compare(sub, gsub, ref, sinp["sequence_lens"])
+
+
+# ------------------------------------------------------------------ small-grid projection forms
+
+def projection_case(S, N, I, H, dtype, direction="bidirectional", seed=0, flags=rk.RK_FORCE_SIMT_PROJECTION):
+    """RNN with Affine(1, 0), R = 0 and no bias: Y[t] = x_t . W^T, the
+    projection alone, compared with the oracle's projection."""
+    pr = rk.Problem("rnn", seq=S, batch=N, input=I, hidden=H, direction=direction, dtype=dtype,
+                    activations=[("affine", 1.0, 0.0)] * (2 if direction == "bidirectional" else 1))
+    D = pr.num_directions
+    rng = np.random.default_rng(seed + S * 7 + I)
+    inp = {"X": workloads.cast(rng.uniform(-1, 1, (S, N, I)), dtype),
+           "W": workloads.cast(rng.uniform(-0.2, 0.2, (D, H, I)), dtype),
+           "R": workloads.cast(np.zeros((D, H, H)), dtype)}
+    got = run_gpu(pr, inp, outputs=("Y",), flags=flags)
+    want = oracle.projection(inp["X"].astype(np.float64).reshape(S * N, I), inp["W"].astype(np.float64))
+    ref = {"Y": want.reshape(D, S, N, H).transpose(1, 0, 2, 3)}
+    compare(pr, got, ref)
+    return got
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("S,N,I,H", [(1, 1, 4, 3), (1, 4, 256, 100), (2, 2, 1000, 37), (3, 1, 128, 1024),
+                                     (4, 1, 36, 200)])
+def test_few_rows_projection(S, N, I, H, dtype):
+    """At most four rows of X (S * N <= 4): the projection streams W once, a
+    warp per column with its lanes on consecutive k, lane sums added in lane
+    order ("Matrix multiplication (Gemm)", section "Small grids and few
+    rows").  Matches the oracle's projection; two runs give the same bits."""
+    a = projection_case(S, N, I, H, dtype)
+    b = projection_case(S, N, I, H, dtype)
+    assert torch.equal(a["Y_raw"], b["Y_raw"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("S,N,I,H", [(80, 1, 256, 1024), (5, 7, 512, 100), (37, 1, 264, 64), (9, 9, 256, 333)])
+def test_split_k_projection(S, N, I, H, dtype):
+    """A grid of tiles that cannot fill the GPU over k >= 256: k in 4 ranges
+    per CTA, each output the sum of its range sums in range order (the Gemm
+    page's split k, inside one launch).  Ragged rows and columns; matches the
+    oracle's projection; two runs give the same bits."""
+    a = projection_case(S, N, I, H, dtype)
+    b = projection_case(S, N, I, H, dtype)
+    assert torch.equal(a["Y_raw"], b["Y_raw"])
+
+
+@pytest.mark.parametrize("cell", ["lstm", "gru", "rnn"])
+def test_single_step_layers_use_few_rows_projection(cell):
+    """Layers of one step and a batch of up to four (one step of a decoder):
+    the whole layer through the few-rows projection matches the oracle."""
+    for N in (1, 3):
+        pr = rk.Problem(cell, seq=1, batch=N, input=64, hidden=48, direction="bidirectional",
+                        linear_before_reset=1 if cell == "gru" else 0)
+        inp = rand_inputs(pr, seed=90 + N, lens=[1] * N, peep=True)
+        compare(pr, run_gpu(pr, inp), run_oracle(pr, inp), [1] * N)
