@@ -22,8 +22,8 @@
 //   2. forms its row sums (each lane chains its terms in increasing k, then a
 //      fixed shuffle tree folds the 32 lanes), so runs are bit-identical,
 //   3. gathers each unit's gate sums into lane u by shuffles and does the gate
-//      arithmetic there (h, c, biases, peepholes and the next step's xw,
-//      prefetched one step ahead, all in registers),
+//      arithmetic there (h, c, biases, peepholes and the step's xw,
+//      prefetched two steps ahead, all in registers),
 //   4. writes Y and pushes its U new h values into every CTA of the cluster.
 // No barrier inside a CTA: the only synchronisation is the byte-counting
 // mbarrier of each h (and r.h) exchange.  Every wait is bounded by a deadline
@@ -417,13 +417,26 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
   // dependent launch): everything above only reads operands the projection
   // does not touch; wait for it before the first Xw read.
   grid_dependency_wait();
-  float xv[G];
-  load_xw(0, xv);
+  // xw of the next two steps in flight: the load issued at the end of step s
+  // is used at step s + 2.  One step ahead was too little for the direction
+  // whose Xw rows sit in the other die's L2 (its row sums waited on the load:
+  // about 1,450 against 1,190 cycles per step on the bidirectional 80 x 1 x
+  // 256 layer), and a copy between two register sets would wait on it too,
+  // so even and odd steps each keep their own set.  The variants with the
+  // longest rows of R (KV = 4) keep one step ahead: two sets and the
+  // unrolled loop would spill there.
+  constexpr bool XW2 = KV <= 2;
+  constexpr int kAhead = XW2 ? 2 : 1;
+  float xa[G], xb[G];
+  load_xw(0, xa);
+  if constexpr (XW2) load_xw(1, xb);
 
   // ---------------- the steps
-  for (int s = 0; s < Tn; ++s) {
+  // one step; xv holds step s's xw and is refilled with step s + kAhead's;
+  // false when a wait gave up (the warp leaves the loop)
+  auto step = [&](int s, float (&xv)[G]) -> bool {
     const int cur = s & 1, nxt = cur ^ 1;
-    if (s >= 1 && !wait(&bars[cur], (uint32_t)(((s - 1) >> 1) & 1))) break;
+    if (s >= 1 && !wait(&bars[cur], (uint32_t)(((s - 1) >> 1) & 1))) return false;
     // h_s has arrived, so every warp of every CTA is past step s-1: the fills
     // h_{s-1} of bars[nxt] and r.h_{s-1} of bars[2 + nxt] are complete and
     // the next ones can be announced
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
         const float z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[0] + sz) + wbv[0]) + rbv[0]));
         const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, ((xv[1] + sr) + wbv[1]) + rbv[1]));
         push(r * hreg, 1, cur);
-        if (!wait(&bars[2 + cur], (uint32_t)((s >> 1) & 1))) break;
+        if (!wait(&bars[2 + cur], (uint32_t)((s >> 1) & 1))) return false;
         const float v2 = rowsums<2 * U, U, T, KV>(Rr, rhs + (size_t)cur * KP, lane);
         const float sh = __shfl_sync(0xffffffffu, v2, row_lane<U>(ul));
         const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, ((xv[2] + sh) + wbv[2]) + rbv[2]));
@@ -493,7 +506,17 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
     hreg = hn;
     if (s + 1 < Tn) push(hn, 0, nxt);
     if (ybase != nullptr) store_elem<T>(ybase + (size_t)t * ystride, active ? hn : 0.0f);
-    load_xw(s + 1, xv);
+    load_xw(s + kAhead, xv);
+    return true;
+  };
+  if constexpr (XW2) {
+    for (int s = 0; s < Tn; s += 2) {
+      if (!step(s, xa)) break;
+      if (s + 1 < Tn && !step(s + 1, xb)) break;
+    }
+  } else {
+    for (int s = 0; s < Tn; ++s)
+      if (!step(s, xa)) break;
   }
 
   // ---------------- outputs: zero Y past the loop, final states
