@@ -106,6 +106,24 @@ struct RFrag<float> {
   __device__ __forceinline__ void set(const float e[4]) { v = make_float4(e[0], e[1], e[2], e[3]); }
 };
 
+// Fragment of 4 consecutive k of one row of R (elements k0 .. k0 + 3 of
+// `row`): one 16-byte (float32) or 8-byte (16-bit) load when the four are
+// inside the row and aligned, else element loads with zeros past H.  The
+// prologue's R loads are what the step kernel spends before its first step.
+template <typename T>
+__device__ __forceinline__ void load_frag(RFrag<T>& f, const T* row, int k0, int H, bool ok) {
+  const T* src = row + k0;
+  if (ok && k0 + 3 < H && (reinterpret_cast<uintptr_t>(src) % (4 * sizeof(T))) == 0) {
+    if constexpr (sizeof(T) == 4) f.v = __ldg(reinterpret_cast<const float4*>(src));
+    else f.v = __ldg(reinterpret_cast<const uint2*>(src));
+    return;
+  }
+  float e[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) e[q] = (ok && k0 + q < H) ? load_elem<T>(src + q) : 0.0f;
+  f.set(e);
+}
+
 __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
                "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(bar)
@@ -272,13 +290,7 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
       const bool ok = g < G && u < Uc;
       const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int k = (c * 8 + gi) * 4;
-        float e[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
-        Rg[rho][c].set(e);
-      }
+      for (int c = 0; c < NCH; ++c) load_frag<T>(Rg[rho][c], row, (c * 8 + gi) * 4, H, ok);
     }
   } else {
 #pragma unroll
@@ -288,13 +300,7 @@ __global__ void __launch_bounds__(U == 2 ? 512 : 256, 1) step_fast_kernel(const 
       const bool ok = g < G && u < Uc;
       const T* row = R + ((size_t)d * GH + (size_t)g * H + j0 + wu0 + u) * H;
 #pragma unroll
-      for (int kc = 0; kc < KV; ++kc) {
-        const int k = (kc * 32 + lane) * 4;
-        float e[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) e[q] = (ok && k + q < H) ? load_elem<T>(row + k + q) : 0.0f;
-        Rr[i][kc].set(e);
-      }
+      for (int kc = 0; kc < KV; ++kc) load_frag<T>(Rr[i][kc], row, (kc * 32 + lane) * 4, H, ok);
     }
   }
   for (int e = tid; e < 2 * KP; e += blockDim.x) {
