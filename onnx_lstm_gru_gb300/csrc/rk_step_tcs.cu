@@ -4,7 +4,22 @@
 
 namespace rk {
 
-size_t step_tcs_smem(int G, int H) { return xs_layout(G, H).total; }
+// Dynamic shared memory of a CTA: the layout, padded so that no more CTAs
+// share an SM than their TMEM allocations fit at once.  A CTA beyond that
+// would wait in tcgen05.alloc for another to free its columns, and within a
+// cluster the others may be waiting for it.
+size_t step_tcs_smem(int G, int H) {
+  const size_t need = xs_layout(G, H).total;
+  const int per_sm = (int)(512u / tcs_tmem_cols(H));  // allocations that fit an SM's 512 columns
+  int dev = 0, sm_smem = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || sm_smem <= 0) {
+    cudaGetLastError();
+    sm_smem = 233472;  // 228 KB
+  }
+  const size_t floor = (size_t)sm_smem / (size_t)(per_sm + 1) + 1;
+  return need > floor ? need : floor;
+}
 
 cudaError_t step_tcs_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void*) {
   // the exchanged operand lives in the CTAs' shared memory, not in scratch

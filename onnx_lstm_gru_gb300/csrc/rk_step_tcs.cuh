@@ -12,8 +12,8 @@
 //
 // With a small batch the product is turned around: the MMA's M = 128 rows
 // are this CTA's gate rows (row g * 32 + u for gate g, unit u of its 32
-// units; rows past G * 32 are zero) held in shared memory for the whole
-// layer, and its N = 16 columns are the direction's batch rows, so the
+// units; rows past G * 32 are zero) held in TMEM as the MMA's A operand for
+// the whole layer, and its N = 16 columns are the direction's batch rows, so the
 // exchanged operand is only 16 rows of h (2 KB per 64 k).  A team is one
 // direction, one cluster of ceil(H / 32) CTAs.  Every CTA keeps the whole
 // 16-bit operand, double-buffered, in its own shared memory in the layout
@@ -51,19 +51,49 @@ namespace {
 constexpr int XN = 16;         // MMA N: a direction's batch rows, padded
 constexpr int XJ = 32;         // hidden units per CTA
 constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at most
-constexpr int XBLK_A = 128 * 128;  // bytes of one 64-k block of the gate rows
 constexpr int XBLK_B = XN * 128;   // bytes of one 64-k block of h
+constexpr uint32_t XACC_COLS = 32;  // TMEM columns of the two accumulators (2 rounds x 16)
 
-// Shared memory: [gate rows: KB x 16 KB][operands: [h, r (.) h][2 buffers]
-// [KB x 2 KB]][staged products [4][32][16] floats][barriers][biases]
+// TMEM columns the kernel allocates for hidden size H: the accumulators,
+// then the CTA's gate rows as the MMA's A operand (lane = gate row, one
+// column per two k), a power of two.
+__host__ __device__ inline uint32_t tcs_tmem_cols(int H) {
+  const int KB = (H + SK - 1) / SK;
+  return tmem_cols_for(XACC_COLS + (uint32_t)KB * (SK / 2));
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes from 32 registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// D (TMEM) += A (TMEM: lane = row of A, k packed two per column) . B^T
+// (shared memory, descriptor), kind::f16, cta_group::1.
+__device__ __forceinline__ void tc_mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Shared memory: [operands: [h, r (.) h][2 buffers][KB x 2 KB]][staged
+// products [4][32][16] floats][barriers][biases].  The gate rows live in TMEM.
 struct XsSmem {
-  size_t r, h, acc, bar, bias, total;
+  size_t h, acc, bar, bias, total;
 };
 __host__ __device__ inline XsSmem xs_layout(int G, int H) {
   XsSmem L{};
   const int KB = (H + SK - 1) / SK;
   size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
-  L.r = o;    o += (size_t)KB * XBLK_A;
   L.h = o;    o += (size_t)2 * 2 * KB * XBLK_B;
   L.acc = o;  o += (size_t)4 * XJ * XN * 4;
   L.bar = o;  o += 256;
@@ -79,11 +109,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   constexpr int NRND = LBR0 ? 2 : 1;  // products per step
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
-  constexpr uint32_t kTmemCols = 32;  // accumulator: 128 lanes x 16 columns
+  // accumulators (columns 0 .. 31), then the gate rows (A operand)
+  const uint32_t kTmemCols = tcs_tmem_cols(p.H);
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const XsSmem L = xs_layout(G, p.H);
-  unsigned char* sR = base + (L.r - 1024);
   unsigned char* sH = base + (L.h - 1024);
   float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));  // [g][u][b]
   // operand arrived [round][buffer], drain, then per round: done, free, staged
@@ -111,27 +141,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   const E* c0 = static_cast<const E*>(p.c0);
   E* Y = static_cast<E*>(p.Y);
 
-  // ---------------- prologue: gate rows (row g * 32 + u), 16 bytes at a time
-  const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
-  for (int e = tid; e < KB * 128 * (SK / 8); e += blockDim.x) {
-    const int kb = e / (128 * (SK / 8));
-    const int rem = e % (128 * (SK / 8));
-    const int r = rem / (SK / 8), kk = (rem % (SK / 8)) * 8;
-    const int g = r / XJ, u = r % XJ, k = kb * SK + kk;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (g < G && j0 + u < H && k < H) {
-      const E* src = R + ((size_t)d * GH + (size_t)g * H + j0 + u) * H + k;
-      if (r_vec) {
-        v = __ldg(reinterpret_cast<const uint4*>(src));
-      } else {
-        __align__(16) E t8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t8[i] = src[i];
-        v = *reinterpret_cast<const uint4*>(t8);
-      }
-    }
-    *reinterpret_cast<uint4*>(sR + (size_t)kb * XBLK_A + sw128_offset(r, kk)) = v;
-  }
+  // ---------------- prologue: biases, peepholes, operand buffers, barriers, TMEM
   for (int e = tid; e < G * XJ; e += blockDim.x) {
     const int g = e / XJ, u = e % XJ;
     const bool ok = j0 + u < H && Bias != nullptr;
@@ -176,14 +186,56 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     if (Tn > 1) mbar_arrive_expect_tx(full_bar(0, 1), op_bytes);
     if (LBR0 && Tn > 0) mbar_arrive_expect_tx(full_bar(1, 0), op_bytes);
   }
-  // the gate rows and h_0 were written by ordinary stores; the tensor cores
-  // read them through the async proxy
+  // h_0 was written by ordinary stores; the tensor cores read it through
+  // the async proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // The gate rows (row g * 32 + u for gate g, unit u; zero past G * 32
+  // rows, past H units and past H in k) go to TMEM once, as the MMA's A
+  // operand: lane = row, column XACC_COLS + k / 2 holding k and k + 1.
+  // From shared memory every MMA re-read its 4 KB of A there (the MMA's
+  // cost tracks its operand bytes at these small N); from TMEM only the 512
+  // bytes of h are read.  Warp w stores the rows of lane quarter w % 4 and
+  // the 64-k blocks kb with kb % 2 == w / 4, one block (32 columns) at a time.
+  if (warp < 8) {
+    const int q = warp & 3;
+    const int g = q, u = lane;  // row 32 q + lane
+    const bool row_ok = g < G && j0 + u < H;
+    const E* rrow = R + ((size_t)d * GH + (size_t)(row_ok ? g : 0) * H + (row_ok ? j0 + u : 0)) * H;
+    const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
+    const uint32_t trow = *tmem_slot + ((uint32_t)(32 * q) << 16) + XACC_COLS;
+    for (int kb = warp >> 2; kb < KB; kb += 2) {
+      uint32_t v[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = kb * SK + 8 * c;  // H is a multiple of 8: a chunk is wholly in or past H
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok && k < H) {
+          if (r_vec) {
+            w = __ldg(reinterpret_cast<const uint4*>(rrow + k));
+          } else {
+            __align__(16) E t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = rrow[k + i];
+            w = *reinterpret_cast<const uint4*>(t8);
+          }
+        }
+        v[4 * c + 0] = w.x;
+        v[4 * c + 1] = w.y;
+        v[4 * c + 2] = w.z;
+        v[4 * c + 3] = w.w;
+      }
+      tmem_st32(trow + (uint32_t)(kb * (SK / 2)), v);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   }
 
   // gate threads: pair i = tid + 256 k is (unit i % 32, batch row i / 32)
@@ -256,7 +308,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     // ---------------- MMA lane: acc_rd[128 gate rows x 16 batch] = R_rows . operand^T
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(XN) | Elem<E>::kMmaAB;
-      const uint64_t adesc0 = desc_sw128(su32(sR));
+      const uint32_t ta0 = tmem_acc + XACC_COLS;  // the gate rows: 8 columns per 16 k
       constexpr uint64_t kK16 = 32 >> 4;
       bool ok = true;
       for (int s = 0; s < Tn && ok; ++s) {
@@ -275,12 +327,13 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           }
           tc_fence_after();
           const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
-          uint64_t ad = adesc0, bd = desc_sw128(su32(sH) + (uint32_t)((rd * 2 + (s & 1)) * KBB));
-          for (int kb = 0; kb < KB; ++kb, ad += XBLK_A >> 4, bd += XBLK_B >> 4) {
-            tc_mma(tacc, ad, bd, idesc, kb != 0 ? 1u : 0u);
-            tc_mma(tacc, ad + kK16, bd + kK16, idesc, 1u);
-            tc_mma(tacc, ad + 2 * kK16, bd + 2 * kK16, idesc, 1u);
-            tc_mma(tacc, ad + 3 * kK16, bd + 3 * kK16, idesc, 1u);
+          uint32_t ta = ta0;
+          uint64_t bd = desc_sw128(su32(sH) + (uint32_t)((rd * 2 + (s & 1)) * KBB));
+          for (int kb = 0; kb < KB; ++kb, ta += SK / 2, bd += XBLK_B >> 4) {
+            tc_mma_ts(tacc, ta, bd, idesc, kb != 0 ? 1u : 0u);
+            tc_mma_ts(tacc, ta + 8, bd + kK16, idesc, 1u);
+            tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idesc, 1u);
+            tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idesc, 1u);
           }
           tc_commit(rbar(rd, 0));  // accumulator rd of step s complete
         }
