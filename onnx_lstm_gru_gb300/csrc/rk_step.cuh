@@ -338,8 +338,12 @@ __device__ __forceinline__ bool team_barrier(unsigned* ctr, unsigned target, lon
                                              int* flag_smem) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
+    // arrive with release semantics (the CTA's writes, ordered before this
+    // thread by the __syncthreads above, are covered); poll with acquire
+    // loads, which order every later read -- a full fence before a relaxed
+    // add and another after the poll cost 5 % more per step on the reverse
+    // LSTM 200 x 4 x 1024 layer
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
     int ok = 1;
     if (ld_acquire_gpu(ctr) < target) {
       const unsigned long long t0 = global_ns();
@@ -351,7 +355,6 @@ __device__ __forceinline__ bool team_barrier(unsigned* ctr, unsigned target, lon
         }
       }
     }
-    __threadfence();
     *flag_smem = ok;
   }
   __syncthreads();
