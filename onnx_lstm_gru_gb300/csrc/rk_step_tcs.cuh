@@ -86,7 +86,8 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint
 }
 
 // Shared memory: [operands: [h, r (.) h][2 buffers][KB x 2 KB]][staged
-// products [4][32][16] floats][barriers][biases].  The gate rows live in TMEM.
+// products [4 gates][16 rows][32 units] floats][barriers][biases].  The gate
+// rows live in TMEM.
 struct XsSmem {
   size_t h, acc, bar, bias, total;
 };
@@ -115,7 +116,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const XsSmem L = xs_layout(G, p.H);
   unsigned char* sH = base + (L.h - 1024);
-  float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));  // [g][u][b]
+  // staged products [g][b][u]: a gate thread's row b is warp-uniform and its
+  // unit is the lane, so its reads are 32 consecutive floats (the layout
+  // [g][u][b] had lanes 16 floats apart: 16-way bank conflicts)
+  float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));
   // operand arrived [round][buffer], drain, then per round: done, free, staged
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
@@ -369,11 +373,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       if (warp >= g0 && warp < g1) {
         uint32_t v[XN];
         tmem_ld<XN>(tmem_acc + ((uint32_t)(warp * 32) << 16) + (uint32_t)(rd * XN), v);
-        float4* dst = reinterpret_cast<float4*>(sAcc + ((size_t)warp * XJ + lane) * XN);
 #pragma unroll
-        for (int i = 0; i < XN / 4; ++i)
-          dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                               __uint_as_float(v[4 * i + 3]));
+        for (int b = 0; b < XN; ++b) sAcc[((size_t)warp * XN + b) * XJ + lane] = __uint_as_float(v[b]);
       }
       // the accumulator may be overwritten by the next step's product
       tc_fence_before();
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           float pre[2];
 #pragma unroll
           for (int g = 0; g < 2; ++g)
-            pre[g] = ((xv[k][g] + sAcc[((size_t)g * XJ + pu) * XN + b]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
+            pre[g] = ((xv[k][g] + sAcc[((size_t)g * XN + b) * XJ + pu]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
           zr[k][0] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
           zr[k][1] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
           push_row(1, s & 1, b, pj < H ? zr[k][1] * hreg[k] : 0.0f);
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         float rec[G], pre[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          rec[g] = (LBR0 && g < 2) ? 0.0f : sAcc[((size_t)g * XJ + pu) * XN + b];
+          rec[g] = (LBR0 && g < 2) ? 0.0f : sAcc[((size_t)g * XN + b) * XJ + pu];
           pre[g] = ((xv[k][g] + rec[g]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
         }
         float hn = hreg[k];
