@@ -357,12 +357,12 @@ def measure_tensor_peak(dev, stream, dtype):
 # Source files of each kernel, hashed so a committed ncu summary is only used
 # while the kernel it measured is unchanged.
 KERNEL_SOURCES = {
-    "fast": ("step_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_fast.cuh", "rk_step_launch.cuh")),
-    "cluster": ("step_cluster_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
-    "grid": ("step_grid_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
-    "tensor": ("step_tc_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_proj_tc.cuh", "rk_step_tc.cuh", "rk_step_tc.cu",
-                                  "rk_step_tc_pair.cu", "rk_step_tc_cluster.cu")),
-    "tensor_small": ("step_tcs_kernel", ("rk_elem.cuh", "rk_step.cuh", "rk_step_tc.cuh", "rk_step_tcs.cuh",
+    "fast": ("step_kernel", ("rk_elem.cuh", "rk_step_common.cuh", "rk_step_fast.cuh")),
+    "cluster": ("step_cluster_kernel", ("rk_elem.cuh", "rk_step_common.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
+    "grid": ("step_grid_kernel", ("rk_elem.cuh", "rk_step_common.cuh", "rk_step.cuh", "rk_step_launch.cuh")),
+    "tensor": ("step_tc_kernel", ("rk_elem.cuh", "rk_step_common.cuh", "rk_proj_tc.cuh", "rk_step_tc.cuh",
+                                  "rk_step_tc.cu", "rk_step_tc_pair.cu", "rk_step_tc_cluster.cu")),
+    "tensor_small": ("step_tcs_kernel", ("rk_elem.cuh", "rk_step_common.cuh", "rk_step_tc.cuh", "rk_step_tcs.cuh",
                                          "rk_step_tcs.cu")),
     "proj_tc": ("proj_tc_kernel", ("rk_elem.cuh", "rk_proj_tc.cuh", "rk_proj_tc.cu")),
     "proj_simt": ("projection", ("rk_elem.cuh", "rk_proj.cu")),

@@ -181,11 +181,12 @@ int64_t rk_xw_length(const rk_problem* p);
 /* Floats of state scratch the problem needs: StateLength of the web page
  * "Recurrent layers", paragraph "Scratch".  The pages' state holds every
  * step's output; here, where the steps run inside one kernel, it holds 256
- * barrier words, the double-buffered hidden state exchanged between blocks of
- * the step kernel, 2 * D * N * KP, and a region for r (.) h or the 16-bit
- * copies of h used by the tensor cores, D * (N + 128) * KP (KP = hidden
- * rounded up to a multiple of 128).  Host only.  Returns -1 for an invalid
- * problem. */
+ * counter words, the grid step kernel's team counters, 64 per direction and
+ * group of up to 64 batch rows, the double-buffered hidden state
+ * exchanged between blocks of the step kernel, 2 * D * N * KP, and a region
+ * for r (.) h or the 16-bit copies of h used by the tensor cores,
+ * D * (N + 128) * KP (KP = hidden rounded up to a multiple of 128).  Host
+ * only.  Returns -1 for an invalid problem. */
 int64_t rk_state_length(const rk_problem* p);
 
 /* Host-only validation of a problem and its operands: the checks of the web
@@ -259,7 +260,7 @@ rk_status rk_status_poll(rk_handle* h, void* stream);
 rk_status rk_set_wait_limit(rk_handle* h, int64_t limit);
 
 /* (No counterpart on the pages; see rk_status_poll.)
- * Run the step kernels' bounded device waits against a grid barrier and an
+ * Run the step kernels' bounded device waits against a release counter and an
  * mbarrier that nothing completes (one CTA, no other memory touched): each
  * must give up after timeout_ns and set the handle's status word.  Returns
  * RK_OK once the check kernel is enqueued on `stream`; rk_status_poll then

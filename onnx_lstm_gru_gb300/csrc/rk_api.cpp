@@ -207,10 +207,15 @@ int64_t xw_len(const rk_problem* p) {
   return (int64_t)dirs_of(p) * p->seq * p->batch * gates_of(p->cell) * p->hidden;
 }
 int64_t kp_of(const rk_problem* p) { return round_up(std::max<int64_t>(p->hidden, 1), rk::kKChunk); }
+// Counter words of the grid step kernel (teams of up to 64 batch rows).
+int64_t grid_counter_words(const rk_problem* p) {
+  return (int64_t)dirs_of(p) * ((p->batch + 63) / 64) * rk::kGridCounterWordsPerTeam;
+}
 int64_t state_len(const rk_problem* p) {
-  // barrier counters, the double-buffered float32 h of the grid kernel, and a
-  // region for r.h (grid kernel) or the 16-bit copies of h (tensor-core kernel)
-  return rk::kStateHeader + 2 * (int64_t)dirs_of(p) * p->batch * kp_of(p) +
+  // counters, the grid kernel's team counters, the double-buffered float32
+  // h of the grid kernel, and a region for r.h (grid kernel) or the 16-bit
+  // copies of h (tensor-core kernel)
+  return rk::kStateHeader + grid_counter_words(p) + 2 * (int64_t)dirs_of(p) * p->batch * kp_of(p) +
          (int64_t)dirs_of(p) * (p->batch + 128) * kp_of(p);
 }
 
@@ -292,7 +297,21 @@ FusedProj fused_projection(const rk_handle* h, const rk_problem* p, const StepPl
 int64_t zeroed_state_floats(const StepPlan& pl, int D) {
   int64_t n = rk::kStateHeader;
   if (pl.kind == rk::kStepTensor && pl.J == 16) n += (int64_t)D * pl.teams_per_dir * rk::kTcRegionLines * 32;
+  if (pl.kind == rk::kStepGrid) n += (int64_t)D * pl.teams_per_dir * rk::kGridCounterWordsPerTeam;
   return n;
+}
+
+// The step kernel's pointers into the state scratch: the header, then (grid
+// kernel) its team counters, then the exchange buffers.
+void assign_state(rk::StepParams& sp, const StepPlan& pl, float* state) {
+  sp.counters = reinterpret_cast<unsigned*>(state);
+  float* exchange = state + rk::kStateHeader;
+  if (pl.kind == rk::kStepGrid) {
+    sp.team_ctrs = reinterpret_cast<unsigned*>(exchange);
+    exchange += (size_t)sp.D * pl.teams_per_dir * rk::kGridCounterWordsPerTeam;
+  }
+  sp.hglob = exchange;
+  sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
 }
 
 // Launch (or, with resident != nullptr, size) the step kernel of a plan.
@@ -522,7 +541,10 @@ rk_status plan_step_uncached(rk_handle* h, const rk_problem* p, StepParams* sp, 
     const int rpw = pl.shape == rk::kShapeR8B4 ? 8 : 4;
     const int Jp = (int)round_up(pl.J, rpw);
     pl.rows_pad = G * Jp;
-    pl.threads = (int)std::min<int64_t>(768, std::max<int64_t>(256, 32 * (pl.rows_pad / rpw)));
+    // computing warps (a warp per row group, up to the kernel's thread
+    // budget) and one warp that stages the exchanged rows
+    const int max_threads = pl.shape == rk::kShapeR4B4 ? 512 : 640;
+    pl.threads = (int)std::min<int64_t>(max_threads - 32, std::max<int64_t>(256, 32 * (pl.rows_pad / rpw))) + 32;
     pl.grid = teams * pl.team_ctas;
     if (!finish(pl))
       return fail(h, RK_ERR_UNSUPPORTED, "%s: R slice of %d rows x %d does not fit shared memory", cell_name(p->cell),
@@ -803,9 +825,7 @@ rk_status encode_validated(rk_handle* h, const rk_problem* p, const rk_operands*
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
-  sp.counters = reinterpret_cast<unsigned*>(state);
-  sp.hglob = state + rk::kStateHeader;
-  sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
+  assign_state(sp, pl, state);
   sp.status = h->status;
   sp.timeout_ns = h->timeout_ns;
   if (pl.kind == rk::kStepGrid || pl.kind == rk::kStepTensor) {
@@ -948,9 +968,7 @@ rk_status rk_encode_noalloc(rk_handle* h, const rk_problem* p, const rk_operands
   sp.Yh = tptr_mut(ops->Y_h, eb);
   sp.Yc = tptr_mut(ops->Y_c, eb);
   sp.xw = xw;
-  sp.counters = reinterpret_cast<unsigned*>(state);
-  sp.hglob = state + rk::kStateHeader;
-  sp.rhglob = sp.hglob + (size_t)2 * sp.D * sp.N * sp.KP;
+  assign_state(sp, pl, state);
   sp.status = status;
   sp.timeout_ns = h->timeout_ns;
   if (h->profiling) cudaEventRecord(h->ev[2], stream);

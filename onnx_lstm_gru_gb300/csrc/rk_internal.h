@@ -19,7 +19,10 @@ constexpr int kXwRingTiles = 8;
 // lines of 32 words per team, one per region of 128 k, placed at the start of
 // the state scratch's exchange area and zeroed before each launch.
 constexpr int kTcRegionLines = 32;
-                                  // for the grid step kernel's barrier counters
+// Counters of the grid step kernel: per team one for h and one for r.h (GRU,
+// linear_before_reset = 0), each on a line of 32 words of its own, placed
+// after the state header and zeroed before each launch.
+constexpr int kGridCounterWordsPerTeam = 2 * 32;
 
 struct ActSlot {
   int kind;
@@ -87,6 +90,7 @@ struct StepParams {
   float* hglob;        // [2][D*N][KP]
   float* rhglob;       // [D*N][KP]
   unsigned* counters;  // one per team, zero at launch
+  unsigned* team_ctrs; // kStepGrid: [teams][2][32] release counters of h and r.h, zero at launch
   int* status;         // device status word (bit 1: timeout)
   long long timeout_ns;
 };

@@ -1,6 +1,7 @@
 // rk_plan.cu -- shared-memory size of a step-kernel plan (computed from the
 // same layout function the kernel uses to carve its shared memory), and the
 // self-test of the step kernels' bounded waits.
+#include "rk_step.cuh"
 #include "rk_step_fast.cuh"
 
 namespace rk {
@@ -13,14 +14,13 @@ size_t step_smem_for(const StepParams& p, const StepPlan& plan) {
   return smem_layout(p, plan.rows_pad, plan.nbc, nb_ld, grid, eb).total;
 }
 
-// One CTA waits on a grid-barrier counter that can never reach its target and
-// on an mbarrier phase that nothing completes.  Both waits are the ones the
-// step kernel uses; each must give up after timeout_ns and set the status.
+// One CTA waits on a region counter that can never reach its target and on
+// an mbarrier phase that nothing completes.  Both waits are the ones the
+// step kernels use; each must give up after timeout_ns and set the status.
 __global__ void selftest_timeout_kernel(unsigned* counter, int* status, long long timeout_ns) {
-  __shared__ int flag;
   __shared__ __align__(8) uint64_t bar;
-  // the counter target is 2 arrivals but only this CTA arrives
-  team_barrier(counter, 2u, timeout_ns, status, &flag);
+  // the counter must reach 1 but nothing raises it
+  if (threadIdx.x == 0 && !counter_wait_bounded(counter, 1u, timeout_ns)) atomicOr(status, 1);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

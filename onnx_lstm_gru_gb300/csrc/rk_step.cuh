@@ -30,217 +30,20 @@
 //     st.async and the peer's mbarrier counts the bytes, so a step needs no
 //     cluster-wide barrier, only that CTA's wait for its own buffer.
 //   - kStepGrid: a team spans up to all SMs (cooperative launch); the new h
-//     goes to a double-buffered global array (L2 resident) and a counter
-//     barrier with a bounded, timed wait orders the steps.
+//     goes to a double-buffered global array (L2 resident) and each CTA
+//     raises the team's counter with a release add.  A staging warp per CTA
+//     polls the counter with acquire loads from the moment its CTA's products
+//     are done (while the other warps do the gate arithmetic) and bulk-copies
+//     the rows into shared memory as soon as every CTA has published; the
+//     other warps wait only for the copies to land.  No CTA barrier spans the
+//     team's exchange.
 // Every wait is bounded by a deadline on %globaltimer; a wait that runs out
 // sets bit 0 of the status word and the kernel winds down without hanging.
 #pragma once
 
-#include <cstdint>
-
-#include "rk_elem.cuh"
-#include "rk_internal.h"
+#include "rk_step_common.cuh"
 
 namespace rk {
-
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init_cluster() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
-      "r"(__float_as_uint(v.w)), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void st_async_b32(uint32_t addr, float v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
-               "r"(__float_as_uint(v)), "r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait until the grids this one depends on (programmatic dependent launch)
-// have completed and their writes are visible; returns at once otherwise.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Let the next kernel on the stream, if launched as a programmatic
-// dependent, start being scheduled.
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Wait for an mbarrier phase with a deadline.  Returns false on timeout.
-// One contiguous global -> shared copy on the async proxy (16-byte aligned
-// addresses, size a multiple of 16), counted on mbarrier `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (unsigned it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0 && (long long)(global_ns() - t0) > timeout_ns) return false;
-  }
-}
-
-// ------------------------------------------------------------------ element access
-template <typename T>
-__device__ __forceinline__ float load_elem(const T* p) { return Elem<T>::to_f(*p); }
-
-template <typename T>
-__device__ __forceinline__ void store_elem(T* p, float v) { *p = Elem<T>::from_f(v); }
-
-// 4 consecutive R elements from shared memory as floats (16-byte aligned rows).
-template <typename T>
-__device__ __forceinline__ float4 load4_smem(const T* p) { return load4_16(p); }
-template <>
-__device__ __forceinline__ float4 load4_smem<float>(const float* p) {
-  return *reinterpret_cast<const float4*>(p);
-}
-
-// ------------------------------------------------------------------ activations
-// sigmoid(x) = 1 / (1 + e^-x) and tanh(x) = 1 - 2 / (e^(2x) + 1), written from
-// these identities over the __expf intrinsic and the __fdividef fast
-// division.  In float32 both stay within about 1e-6 of the exact value
-// (__expf is within a few ulp for the arguments that matter, and the forms
-// saturate to 0 / +-1 where the exponential overflows); the parity tests hold
-// them to the oracle.
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float tanh_fast(float x) { return 1.0f - __fdividef(2.0f, __expf(2.0f * x) + 1.0f); }
-
-// The eleven ONNX activations (the pages name them; formulas from the ONNX
-// operator definitions).  Comparisons are written so that NaN passes through.
-__device__ __forceinline__ float act_eval(int kind, float a, float b, float x) {
-  switch (kind) {
-    case 0: return sigmoid_fast(x);
-    case 1: return tanh_fast(x);
-    case 2: return x > 0.0f ? x : (x <= 0.0f ? 0.0f : x);
-    case 3: return a * x + b;
-    case 4: return x >= 0.0f ? x : (x < 0.0f ? a * x : x);
-    case 5: return x > a ? x : (x <= a ? 0.0f : x);
-    case 6: return a * tanh_fast(b * x);
-    case 7: {
-      const float y = a * x + b;
-      return y < 0.0f ? 0.0f : (y > 1.0f ? 1.0f : y);
-    }
-    case 8: return x >= 0.0f ? x : (x < 0.0f ? a * expm1f(x) : x);
-    case 9: return x / (1.0f + fabsf(x));
-    case 10: return x > 20.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
-    default: return __int_as_float(0x7fffffff);
-  }
-}
-
-// Slot `slot` of direction d.  GEN = false compiles in the ONNX defaults.
-template <bool GEN, int DEFAULT_KIND>
-__device__ __forceinline__ float act(const StepParams& p, int idx, float x) {
-  if constexpr (GEN) {
-    return act_eval(p.acts[idx].kind, p.acts[idx].alpha, p.acts[idx].beta, x);
-  } else {
-    return act_eval(DEFAULT_KIND, 0.0f, 0.0f, x);
-  }
-}
-
-__device__ __forceinline__ float clip_pre(float c, float x) {
-  if (c > 0.0f) {
-    if (x > c) return c;
-    if (x < -c) return -c;
-  }
-  return x;
-}
-
-// ------------------------------------------------------------------ indexing
-__device__ __forceinline__ size_t y_index(const StepParams& p, int t, int d, int b, int j) {
-  return p.layout == 0 ? (((size_t)t * p.D + d) * p.N + b) * p.H + j
-                       : (((size_t)b * p.S + t) * p.D + d) * p.H + j;
-}
-__device__ __forceinline__ size_t state_index(const StepParams& p, int d, int b, int j) {
-  return p.layout == 0 ? ((size_t)d * p.N + b) * p.H + j : ((size_t)b * p.D + d) * p.H + j;
-}
-__device__ __forceinline__ size_t xw_index(const StepParams& p, int d, int t, int b, int g, int j) {
-  const size_t m = p.layout == 0 ? (size_t)t * p.N + b : (size_t)b * p.S + t;
-  return (((size_t)d * p.S * p.N + m) * p.G + g) * p.H + j;
-}
-
-// ------------------------------------------------------------------ shuffle tree
-// Combine N per-lane partial sums across the 32 lanes of a warp.  At each
-// level the lanes whose bit is set keep the upper half of the values and the
-// others the lower half, so after the levels lane L holds the full sum of
-// value index xreduce_index<N>(L) (duplicated across the lanes that differ
-// only in bits below 32/N).  Fixed order: deterministic.
-template <int N, int O>
-__device__ __forceinline__ void xreduce(float* v, int lane) {
-  if constexpr (N > 1) {
-    constexpr int H2 = N / 2;
-    const bool up = (lane & O) != 0;
-#pragma unroll
-    for (int i = 0; i < H2; ++i) {
-      const float send = up ? v[i] : v[i + H2];
-      const float keep = up ? v[i + H2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-    }
-    if constexpr (O > 1) xreduce<H2, O / 2>(v, lane);
-  } else {
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-    if constexpr (O > 1) xreduce<1, O / 2>(v, lane);
-  }
-}
-template <int N>
-__device__ __forceinline__ int xreduce_index(int lane) {
-  int idx = 0, n = N;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (n > 1) {
-      n >>= 1;
-      if (lane & o) idx += n;
-    }
-  }
-  return idx;
-}
 
 // Row sums gs[(row0 + r) * gs_ld + col0 + b] = sum_k Rs[row0 + r][k] * hsrc[b][k]
 // for rows [row0, row0 + nrows) (nrows a multiple of RPW) and NBC batch rows.
@@ -285,27 +88,11 @@ __device__ __forceinline__ void matvec(const T* __restrict__ Rs, int KP, int row
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int CELL>
-struct CellInfo;
-template <>
-struct CellInfo<0> {  // LSTM: gates i, o, f, c; activations f, g, h
-  static constexpr int G = 4, A = 3;
-};
-template <>
-struct CellInfo<1> {  // GRU: gates z, r, h; activations f, g
-  static constexpr int G = 3, A = 2;
-};
-template <>
-struct CellInfo<2> {  // RNN: one gate; activation f
-  static constexpr int G = 1, A = 1;
-};
-
 // Shared-memory layout of one CTA (all offsets in bytes, 16-byte aligned).
 struct SmemLayout {
-  size_t Rs, hs, rhs, gs, hown, cs, zs, stage, rstage, wb, rb, pp, lens, bar, total;
+  size_t Rs, hs, rhs, gs, hown, cs, zs, stage, rstage, wb, rb, pp, lens, xs, bar, total;
 };
 
-__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 __host__ __device__ inline SmemLayout smem_layout(const StepParams& p, int rows_pad, int nbc, int nb, bool grid,
                                                   int elem_bytes) {
@@ -327,48 +114,22 @@ __host__ __device__ inline SmemLayout smem_layout(const StepParams& p, int rows_
   L.rb = o;   o = align16(o + (size_t)p.G * Jp * 4);
   L.pp = o;   o = align16(o + (size_t)3 * Jp * 4);
   L.lens = o; o = align16(o + (size_t)nb * 4);
+  L.xs = o;   o = align16(o + (size_t)nb * p.J * p.G * 4);  // each pair's Xw of the step (prefetched)
   L.bar = o;  o = align16(o + 4 * 8);
   L.total = o;
   return L;
 }
 
-// Bounded barrier of one team of the grid kernel.  Counter `ctr` only grows;
-// the n-th barrier of the launch waits for team_ctas * n arrivals.
-__device__ __forceinline__ bool team_barrier(unsigned* ctr, unsigned target, long long timeout_ns, int* status,
-                                             int* flag_smem) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // arrive with release semantics (the CTA's writes, ordered before this
-    // thread by the __syncthreads above, are covered); poll with acquire
-    // loads, which order every later read -- a full fence before a relaxed
-    // add and another after the poll cost 5 % more per step on the reverse
-    // LSTM 200 x 4 x 1024 layer
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
-    int ok = 1;
-    if (ld_acquire_gpu(ctr) < target) {
-      const unsigned long long t0 = global_ns();
-      for (unsigned it = 1; ld_acquire_gpu(ctr) < target; ++it) {
-        if ((it & 31u) == 0 && (long long)(global_ns() - t0) > timeout_ns) {
-          atomicOr(status, 1);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    *flag_smem = ok;
-  }
-  __syncthreads();
-  return *flag_smem != 0;
-}
-
-// Threads per CTA the kernel is compiled for (registers are budgeted for it).
-template <int RPW, int NBC>
+// Threads per CTA the kernel is compiled for (registers are budgeted for it:
+// the grid kernel's 32-value tiles get 96 registers a thread, room for the
+// staging warp's state without spilling the tile).
+template <int RPW, int NBC, bool GRID>
 struct MaxThreads {
-  static constexpr int value = (RPW * NBC >= 32) ? 768 : 512;
+  static constexpr int value = (RPW * NBC >= 32) ? (GRID ? 640 : 768) : 512;
 };
 
 template <int CELL, typename T, bool GEN, int RPW, int NBC, bool GRID>
-__global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(const StepParams p) {
+__global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_kernel(const StepParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
@@ -389,6 +150,23 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
   // row stride of gs: the team's batch rows rounded up to whole chunks
   const int nb_ld = GRID ? ((p.nb + NBC - 1) / NBC) * NBC : NBC;
   const bool has_p = CELL == 0 && p.P != nullptr;
+  // the direction's activation slots f, g, h (generic activations), read once
+  ActSlot af{}, ag{}, ah{};
+  if constexpr (GEN) {
+    af = p.acts[d * A + 0];
+    if constexpr (A > 1) ag = p.acts[d * A + 1];
+    if constexpr (A > 2) ah = p.acts[d * A + 2];
+  }
+  // grid kernel: the last warp stages the exchanged rows, the others compute
+  // (tid_c: the thread's index among the computing threads, past every pair
+  // for the staging warp)
+  const bool producer = GRID && warp == nwarps - 1;
+  const int NTc = GRID ? NT - 32 : NT;
+  const int tid_c = producer ? (1 << 30) : tid;
+  // grid kernel: the team's release counters for h and for r.h, each on a
+  // 128-byte line of its own
+  unsigned* ctr_h = GRID ? p.team_ctrs + (size_t)team * kGridCounterWordsPerTeam : nullptr;
+  unsigned* ctr_rh = GRID ? ctr_h + 32 : nullptr;
 
   const SmemLayout L = smem_layout(p, p.rows_pad, NBC, nb_ld, GRID, (int)sizeof(T));
   T* Rs = reinterpret_cast<T*>(smem + L.Rs);
@@ -404,8 +182,9 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
   float* rb_s = reinterpret_cast<float*>(smem + L.rb);
   float* pp_s = reinterpret_cast<float*>(smem + L.pp);
   int* lens_s = reinterpret_cast<int*>(smem + L.lens);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar);  // [0,1] h buffers, [2,3] r.h buffers
-  __shared__ int flag_smem;
+  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  // cluster: [0,1] h buffers, [2,3] r.h buffers; grid: [0] staged rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar);
 
   const T* R = static_cast<const T*>(p.R);
   const T* Bias = static_cast<const T*>(p.Bias);
@@ -481,72 +260,97 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
       // H stay zero from here on (the grid kernel stages h and r.h alike in
       // its one chunk buffer hs)
       for (size_t e = tid; e < (size_t)NBC * KP; e += NT) hs[e] = 0.0f;
-      if (tid == 0) mbar_init(smem_u32(&bars[0]), 1);  // staged rows landed
+      if (tid == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);  // staged rows landed
+        fence_mbar_init_cluster();
+      }
       // the exchange buffer is written by ordinary stores and read by bulk copies
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
   }
 
-  unsigned nbar = 0;  // grid barriers passed so far
+  uint32_t stage_no = 0;  // grid: stagings of exchanged rows so far (each completes mbarrier bars[0] once)
   bool alive = true;
+  // grid: this CTA's new h (or r.h) is in the exchange buffer: one release add
+  // on the team's counter (after a barrier that orders the writing threads'
+  // stores and proxy fences before it)
+  auto publish = [&](unsigned* ctr) { asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory"); };
   if constexpr (GRID) {
-    alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
+    __syncthreads();
+    if (tid == 0) publish(ctr_h);
   }
 
-  // Stage the batch rows [c0, c0 + NBC) of a global exchange buffer (grid
-  // kernel): one bulk copy of H floats per row when rows are a whole number
-  // of 16 bytes (rows past the team's batch keep stale values whose sums no
-  // gate reads), else element loads.
+  // Grid kernel, staging warp: copy batch rows [c0, c0 + NBC) of an exchange
+  // buffer into hs, completing mbarrier bars[0].  With `ctr`, lane 0 first
+  // waits until the team's counter shows every CTA's publication number
+  // `want`.  Rows of a whole number of 16 bytes: one bulk copy per row.  Other
+  // rows: element loads by the whole warp.  A wait that gives up still
+  // completes the mbarrier (with a plain arrival) so that no reader waits on
+  // it, and returns false.  Rows past the team's batch keep stale values whose
+  // sums no gate reads; columns past H stay zero from the prologue.
   const bool bulk_rows = (H % 4) == 0;
-  uint32_t stage_phase = 0;
-  auto load_chunk = [&](const float* src, int c0) -> bool {
+  auto stage_rows = [&](const float* src, int c0, const unsigned* ctr, unsigned want) -> bool {
+    const int nr = min(NBC, nbt - c0);
+    const float* rows = src + ((size_t)d * p.N + b0 + c0) * KP;
+    const uint32_t bar = smem_u32(&bars[0]);
+    int rdy = 1;
+    if (lane == 0 && ctr != nullptr) rdy = counter_wait_bounded(ctr, (unsigned)C * want, p.timeout_ns) ? 1 : 0;
+    // also orders lane 0's acquire before the other lanes' loads
+    const bool ok = __shfl_sync(0xffffffffu, rdy, 0) != 0;
+    if (!ok) {
+      if (lane == 0) mbar_arrive(bar);
+      return false;
+    }
     if (bulk_rows) {
-      const int nrows = min(NBC, nbt - c0);
-      if (tid == 0) {
-        // the writers' ordinary stores, acquired by the team barrier, are
-        // read by the async proxy; this block's reads of the previous rows
-        // come before the async proxy rewrites them
+      if (lane == 0) {
+        // the writers' stores (made visible to the async proxy before their
+        // release) are read by the async proxy; this CTA's earlier reads of
+        // hs come before the async proxy rewrites it
         asm volatile("fence.proxy.async.global;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(smem_u32(&bars[0]), (uint32_t)nrows * (uint32_t)H * 4u);
-        for (int bl = 0; bl < nrows; ++bl)
-          bulk_copy_g2s(smem_u32(hs + (size_t)bl * KP), src + ((size_t)d * p.N + b0 + c0 + bl) * KP, (uint32_t)H * 4u,
-                        smem_u32(&bars[0]));
+        mbar_arrive_expect_tx(bar, (uint32_t)nr * (uint32_t)H * 4u);
+        for (int bl = 0; bl < nr; ++bl)
+          bulk_copy_g2s(smem_u32(hs + (size_t)bl * KP), rows + (size_t)bl * KP, (uint32_t)H * 4u, bar);
       }
-      const bool ok = mbar_wait_bounded(smem_u32(&bars[0]), stage_phase & 1u, p.timeout_ns);
-      ++stage_phase;
-      return ok;
+      return true;
     }
-    const int nk4 = KP / 4;
-    for (int e = tid; e < NBC * nk4; e += NT) {
-      const int bl = e / nk4, k = (e % nk4) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c0 + bl < nbt && k < H) {
-        const float* q = src + ((size_t)d * p.N + b0 + c0 + bl) * KP + k;
-        if (k + 3 < H) {
-          v = __ldcg(reinterpret_cast<const float4*>(q));
-        } else {
-          v.x = __ldcg(q);
-          if (k + 1 < H) v.y = __ldcg(q + 1);
-          if (k + 2 < H) v.z = __ldcg(q + 2);
-        }
-      }
-      *reinterpret_cast<float4*>(hs + (size_t)bl * KP + k) = v;
+    for (int e = lane; e < nr * H; e += 32) {
+      const int bl = e / H, k = e % H;
+      hs[(size_t)bl * KP + k] = __ldcg(rows + (size_t)bl * KP + k);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
     return true;
   };
 
   // Row sums for rows [row0, row0 + nrows) against the current h (or r.h).
-  auto products = [&](int row0, int nrows, const float* cluster_src, const float* global_src) {
+  // Cluster kernel: h is already in shared memory.  Grid kernel: per chunk of
+  // NBC batch rows the staging warp copies the rows (waiting for the team's
+  // counter on the first chunk; it starts while the other warps still do the
+  // previous phase's gate arithmetic) and the other warps multiply them once
+  // landed; a barrier of the whole CTA ends every chunk.  Returns false (grid
+  // kernel, every thread alike) when a wait gave up.
+  auto products = [&](int row0, int nrows, const float* cluster_src, const float* global_src, const unsigned* ctr,
+                      unsigned want) -> bool {
     if constexpr (!GRID) {
       matvec<RPW, NBC, T>(Rs, KP, row0, nrows, cluster_src, gs, NBC, 0, warp, nwarps, lane);
+      return true;
     } else {
       for (int c0 = 0; c0 < nbt; c0 += NBC) {
-        if (!load_chunk(global_src, c0) && tid == 0) atomicOr(p.status, 1);  // the barriers after it still pass
-        __syncthreads();
-        matvec<RPW, NBC, T>(Rs, KP, row0, nrows, hs, gs, nb_ld, c0, warp, nwarps, lane);
-        __syncthreads();
+        bool ok;
+        if (producer) {
+          ok = stage_rows(global_src, c0, c0 == 0 ? ctr : nullptr, want);
+        } else {
+          ok = mbar_wait_bounded(smem_u32(&bars[0]), stage_no & 1u, p.timeout_ns);
+          matvec<RPW, NBC, T>(Rs, KP, row0, nrows, hs, gs, nb_ld, c0, warp, nwarps - 1, lane);
+        }
+        ++stage_no;
+        if (__syncthreads_or(!ok)) {
+          if (tid == 0) atomicOr(p.status, 1);
+          return false;
+        }
       }
+      return true;
     }
   };
 
@@ -574,6 +378,23 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
   };
 
   const int npairs = Jc * nbt;
+  // The thread's first (unit, batch row) pair, whose indices every step
+  // reuses: unit fj, row fb, its Y index at t = 0 (Y advances by y_tstride
+  // per time step) and its index in an exchange buffer.
+  const int fj = tid_c < npairs ? tid_c % Jc : 0, fb = tid_c < npairs ? tid_c / Jc : 0;
+  const size_t fy0 = y_index(p, 0, d, b0 + fb, j0 + fj);
+  const size_t y_tstride = p.layout == 0 ? (size_t)p.D * p.N * H : (size_t)p.D * H;
+  const size_t fg0 = ((size_t)d * p.N + b0 + fb) * KP + j0 + fj;
+  const size_t hbuf = (size_t)p.D * p.N * KP;  // floats per exchange buffer
+  // the first pair's biases and peepholes, held in registers for the launch
+  float fwb[G], frb[G], fpp[3];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    fwb[g] = wb_s[g * Jp + fj];
+    frb[g] = rb_s[g * Jp + fj];
+  }
+#pragma unroll
+  for (int q = 0; q < 3; ++q) fpp[q] = pp_s[q * Jp + fj];
   const uint32_t h_bytes = (uint32_t)nbt * (uint32_t)H * 4u;
   // The cluster kernel's launch may overlap the projection that writes Xw
   // (programmatic dependent launch); wait for it before the first Xw read.
@@ -590,25 +411,37 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
         if (lbr0) mbar_arrive_expect_tx(smem_u32(&bars[2 + cur]), h_bytes);
       }
     }
-    // prefetch this thread's xw (first pair) before waiting on h
-    float xwv[G];
-    int pj = 0, pb = 0, pL = 0, pt = 0;
-    bool pact = false;
-    if (tid < npairs) {
-      pj = tid % Jc;
-      pb = tid / Jc;
-      pL = lens_s[pb];
-      pact = s < pL;
-      pt = pact ? (reverse ? pL - 1 - s : s) : s;
+    // prefetch this thread's xw (first pair) into shared memory before
+    // waiting on h: an asynchronous copy, which neither the compiler nor the
+    // assembler moves to the first use as they may a load into a register
+    float* xsv = xs + (size_t)tid_c * G;
+    if (tid_c < npairs) {
+      const int pL = lens_s[fb];
+      const bool pact = s < pL;
+      const int pt = pact ? (reverse ? pL - 1 - s : s) : s;
 #pragma unroll
-      for (int g = 0; g < G; ++g) xwv[g] = pact ? __ldcg(p.xw + xw_index(p, d, pt, b0 + pb, g, j0 + pj)) : 0.0f;
+      for (int g = 0; g < G; ++g) {
+        if (pact) {
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(xsv + g)),
+                       "l"(p.xw + xw_index(p, d, pt, b0 + fb, g, j0 + fj))
+                       : "memory");
+        } else {
+          xsv[g] = 0.0f;
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
     }
     bool timed_out = false;
     if constexpr (!GRID) {
       if (s >= 1) timed_out = !mbar_wait_bounded(smem_u32(&bars[cur]), (uint32_t)(((s - 1) >> 1) & 1), p.timeout_ns);
     }
-    // rec = R . h_prev for all gate rows (GRU lbr=0: z and r rows only)
-    products(0, lbr0 ? 2 * Jp : G * Jp, hs + (size_t)cur * NBC * KP, p.hglob + (size_t)cur * p.D * p.N * KP);
+    // rec = R . h_prev for all gate rows (GRU lbr=0: z and r rows only); the
+    // grid kernel's h_prev is publication s + 1 (the prologue's is the first)
+    if (!products(0, lbr0 ? 2 * Jp : G * Jp, hs + (size_t)cur * NBC * KP, p.hglob + (size_t)cur * p.D * p.N * KP,
+                  ctr_h, (unsigned)(s + 1))) {
+      alive = false;
+      break;
+    }
     if constexpr (!GRID) {
       if (__syncthreads_or(timed_out)) {
         if (tid == 0) atomicOr(p.status, 1);
@@ -619,36 +452,42 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
 
     if (lbr0) {
       // GRU, linear_before_reset = 0: z, r, then r (.) h_prev of every unit is exchanged
-      for (int idx = tid; idx < npairs; idx += NT) {
-        const int jl = idx % Jc, bl = idx / Jc;
+      for (int idx = tid_c; idx < npairs; idx += NTc) {
+        const bool first = idx == tid_c;
+        const int jl = first ? fj : idx % Jc, bl = first ? fb : idx / Jc;
         const int L = lens_s[bl];
         const bool active = s < L;
         const int t = active ? (reverse ? L - 1 - s : s) : s;
         float xz, xr;
-        if (idx == tid) {
-          xz = xwv[0];
-          xr = xwv[1];
+        if (first) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          xz = xsv[0];
+          xr = xsv[1];
         } else {
           xz = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, 0, j0 + jl)) : 0.0f;
           xr = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, 1, j0 + jl)) : 0.0f;
         }
         const float hp = hown[bl * J + jl];
-        const float pz = ((xz + gs[(size_t)(0 * Jp + jl) * nb_ld + bl]) + wb_s[0 * Jp + jl]) + rb_s[0 * Jp + jl];
-        const float pr = ((xr + gs[(size_t)(1 * Jp + jl) * nb_ld + bl]) + wb_s[1 * Jp + jl]) + rb_s[1 * Jp + jl];
-        const float z = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pz));
-        const float r = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pr));
+        const float wz = first ? fwb[0] : wb_s[0 * Jp + jl], rz = first ? frb[0] : rb_s[0 * Jp + jl];
+        const float wr = first ? fwb[1] : wb_s[1 * Jp + jl], rr = first ? frb[1] : rb_s[1 * Jp + jl];
+        const float pz = ((xz + gs[(size_t)(0 * Jp + jl) * nb_ld + bl]) + wz) + rz;
+        const float pr = ((xr + gs[(size_t)(1 * Jp + jl) * nb_ld + bl]) + wr) + rr;
+        const float z = act<GEN, 0>(af, clip_pre(p.clip, pz));
+        const float r = act<GEN, 0>(af, clip_pre(p.clip, pr));
         zs[bl * J + jl] = z;
         const float rh = r * hp;
         if constexpr (GRID) {
-          p.rhglob[((size_t)d * p.N + b0 + bl) * KP + j0 + jl] = rh;
+          p.rhglob[first ? fg0 : ((size_t)d * p.N + b0 + bl) * KP + j0 + jl] = rh;
         } else {
           rstage[bl * J + jl] = rh;
         }
       }
       if constexpr (GRID) {
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // r.h is read by bulk copies
-        alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
-        if (!alive) break;
+        if (!producer) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // r.h is read by bulk copies
+          asm volatile("bar.sync 1, %0;" ::"r"(NTc) : "memory");
+          if (tid == 0) publish(ctr_rh);
+        }
       } else {
         __syncthreads();
         push_slice(rstage, rhs + (size_t)cur * NBC * KP, &bars[2 + cur]);
@@ -659,48 +498,75 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
           break;
         }
       }
-      products(2 * Jp, Jp, rhs + (size_t)cur * NBC * KP, p.rhglob);
+      if (!products(2 * Jp, Jp, rhs + (size_t)cur * NBC * KP, p.rhglob, ctr_rh, (unsigned)(s + 1))) {
+        alive = false;
+        break;
+      }
       if constexpr (!GRID) __syncthreads();
     }
 
     // gate arithmetic and state update, one (unit, batch row) pair per thread
-    for (int idx = tid; idx < npairs; idx += NT) {
-      const int jl = idx % Jc, bl = idx / Jc;
+    for (int idx = tid_c; idx < npairs; idx += NTc) {
+      const bool first = idx == tid_c;
+      int jl, bl;
+      size_t y0, g0;
+      if (first) {
+        jl = fj;
+        bl = fb;
+        y0 = fy0;
+        g0 = fg0;
+      } else {
+        jl = idx % Jc;
+        bl = idx / Jc;
+        y0 = y_index(p, 0, d, b0 + bl, j0 + jl);
+        g0 = ((size_t)d * p.N + b0 + bl) * KP + j0 + jl;
+      }
       const int L = lens_s[bl];
       const bool active = s < L;
       const int t = active ? (reverse ? L - 1 - s : s) : s;
-      float xv[G];
+      // the pair's xw, biases and peepholes: the first pair's from the
+      // prefetch and registers, any other's from memory
+      float xv[G], wbv[G], rbv[G], ppv[3];
+      if (first) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (idx == tid) {
-          xv[g] = xwv[g];
-        } else {
-          xv[g] = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, g, j0 + jl)) : 0.0f;
+        for (int g = 0; g < G; ++g) {
+          xv[g] = xsv[g];
+          wbv[g] = fwb[g];
+          rbv[g] = frb[g];
         }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) ppv[q] = fpp[q];
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          xv[g] = active ? __ldcg(p.xw + xw_index(p, d, t, b0 + bl, g, j0 + jl)) : 0.0f;
+          wbv[g] = wb_s[g * Jp + jl];
+          rbv[g] = rb_s[g * Jp + jl];
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) ppv[q] = pp_s[q * Jp + jl];
       }
       const float hp = hown[bl * J + jl];
       float hn = hp;
       if (active) {
         float pre[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int lr = g * Jp + jl;
-          pre[g] = ((xv[g] + gs[(size_t)lr * nb_ld + bl]) + wb_s[lr]) + rb_s[lr];
-        }
+        for (int g = 0; g < G; ++g) pre[g] = ((xv[g] + gs[(size_t)(g * Jp + jl) * nb_ld + bl]) + wbv[g]) + rbv[g];
         if constexpr (CELL == 0) {
           const float cp = cs[bl * J + jl];
           float pi = pre[0], po = pre[1], pf = pre[2], pc = pre[3];
           if (has_p) {
-            pi = pi + pp_s[0 * Jp + jl] * cp;
-            pf = pf + pp_s[2 * Jp + jl] * cp;
+            pi = pi + ppv[0] * cp;
+            pf = pf + ppv[2] * cp;
           }
-          const float ig = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pi));
-          const float fg = p.input_forget ? 1.0f - ig : act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pf));
-          const float cg = act<GEN, 1>(p, d * A + 1, clip_pre(p.clip, pc));
+          const float ig = act<GEN, 0>(af, clip_pre(p.clip, pi));
+          const float fg = p.input_forget ? 1.0f - ig : act<GEN, 0>(af, clip_pre(p.clip, pf));
+          const float cg = act<GEN, 1>(ag, clip_pre(p.clip, pc));
           const float cn = fg * cp + ig * cg;
-          if (has_p) po = po + pp_s[1 * Jp + jl] * cn;
-          const float og = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, po));
-          hn = og * act<GEN, 1>(p, d * A + 2, cn);
+          if (has_p) po = po + ppv[1] * cn;
+          const float og = act<GEN, 0>(af, clip_pre(p.clip, po));
+          hn = og * act<GEN, 1>(ah, cn);
           cs[bl * J + jl] = cn;
         } else if constexpr (CELL == 1) {
           float z, ph;
@@ -708,33 +574,35 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC>::value, 1) step_kernel(co
             z = zs[bl * J + jl];
             ph = pre[2];  // ((xw_h + R_h.(r.h)) + Wb_h) + Rb_h
           } else {
-            z = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pre[0]));
-            const float r = act<GEN, 0>(p, d * A + 0, clip_pre(p.clip, pre[1]));
-            const int lr = 2 * Jp + jl;
-            ph = (xv[2] + r * (gs[(size_t)lr * nb_ld + bl] + rb_s[lr])) + wb_s[lr];
+            z = act<GEN, 0>(af, clip_pre(p.clip, pre[0]));
+            const float r = act<GEN, 0>(af, clip_pre(p.clip, pre[1]));
+            ph = (xv[2] + r * (gs[(size_t)(2 * Jp + jl) * nb_ld + bl] + rbv[2])) + wbv[2];
           }
-          const float hc = act<GEN, 1>(p, d * A + 1, clip_pre(p.clip, ph));
+          const float hc = act<GEN, 1>(ag, clip_pre(p.clip, ph));
           hn = (1.0f - z) * hc + z * hp;
         } else {
-          hn = act<GEN, 1>(p, d * A + 0, clip_pre(p.clip, pre[0]));
+          hn = act<GEN, 1>(af, clip_pre(p.clip, pre[0]));
         }
       }
       hown[bl * J + jl] = hn;
-      if (Y != nullptr) store_elem<T>(Y + y_index(p, t, d, b0 + bl, j0 + jl), active ? hn : 0.0f);
+      if (Y != nullptr) store_elem<T>(Y + y0 + (size_t)t * y_tstride, active ? hn : 0.0f);
       if constexpr (GRID) {
-        p.hglob[(size_t)nxt * p.D * p.N * KP + ((size_t)d * p.N + b0 + bl) * KP + j0 + jl] = hn;
+        p.hglob[(size_t)nxt * hbuf + g0] = hn;
       } else {
         stage[bl * J + jl] = hn;
       }
     }
-    if (s + 1 < p.T) {
-      if constexpr (GRID) {
+    if constexpr (GRID) {
+      // the computing threads are done with gs and have written h; the
+      // staging warp is already waiting for the next step's h
+      if (!producer) {
         asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read by bulk copies
-        alive = team_barrier(p.counters + team, (unsigned)C * (++nbar), p.timeout_ns, p.status, &flag_smem);
-      } else {
-        __syncthreads();
-        push_slice(stage, hs + (size_t)nxt * NBC * KP, &bars[nxt]);
+        asm volatile("bar.sync 1, %0;" ::"r"(NTc) : "memory");
+        if (tid == 0 && s + 1 < p.T) publish(ctr_h);
       }
+    } else if (s + 1 < p.T) {
+      __syncthreads();
+      push_slice(stage, hs + (size_t)nxt * NBC * KP, &bars[nxt]);
     }
   }
 

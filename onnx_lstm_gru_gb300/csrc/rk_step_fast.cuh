@@ -32,7 +32,7 @@
 // wait.
 #pragma once
 
-#include "rk_step.cuh"
+#include "rk_step_common.cuh"
 
 namespace rk {
 

@@ -11,7 +11,7 @@ namespace rk {
 template <int CELL, typename T, bool GEN, int RPW, int NBC, bool GRID>
 cudaError_t step_launch_one(const StepParams& p, const StepPlan& plan, cudaStream_t stream, int* resident_teams) {
   auto kern = step_kernel<CELL, T, GEN, RPW, NBC, GRID>;
-  if (plan.threads > MaxThreads<RPW, NBC>::value || plan.threads % 32 != 0) return cudaErrorInvalidConfiguration;
+  if (plan.threads > MaxThreads<RPW, NBC, GRID>::value || plan.threads % 32 != 0) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   if (!GRID && plan.team_ctas > 8) {

@@ -55,7 +55,7 @@
 #include <cstdint>
 
 #include "rk_proj_tc.cuh"
-#include "rk_step.cuh"
+#include "rk_step_common.cuh"
 
 namespace rk {
 

@@ -201,10 +201,14 @@ def test_operand_table_packing():
 def test_scratch_lengths():
     p = rk.Problem("lstm", seq=80, batch=1, input=256, hidden=256, direction="bidirectional")
     assert rk.rk_xw_length(p.to_c()) == 2 * 80 * 1 * 4 * 256
-    assert rk.rk_state_length(p.to_c()) == 256 + 2 * 2 * 1 * 256 + 2 * (1 + 128) * 256
+    # header, team counters (64 per direction and group of 64 batch rows),
+    # the double-buffered h, r.h or the 16-bit copies of h
+    assert rk.rk_state_length(p.to_c()) == 256 + 2 * 64 + 2 * 2 * 1 * 256 + 2 * (1 + 128) * 256
     g = rk.Problem("gru", seq=0, batch=8, input=5, hidden=100)
     assert rk.rk_xw_length(g.to_c()) == 0
-    assert rk.rk_state_length(g.to_c()) == 256 + 2 * 1 * 8 * 128 + 1 * (8 + 128) * 128
+    assert rk.rk_state_length(g.to_c()) == 256 + 64 + 2 * 1 * 8 * 128 + 1 * (8 + 128) * 128
+    w = rk.Problem("rnn", seq=3, batch=65, input=5, hidden=100)
+    assert rk.rk_state_length(w.to_c()) == 256 + 2 * 64 + 2 * 1 * 65 * 128 + 1 * (65 + 128) * 128
 
 
 def test_plans_without_device(handle):
