@@ -543,7 +543,7 @@ rk_status plan_step_uncached(rk_handle* h, const rk_problem* p, StepParams* sp, 
     pl.rows_pad = G * Jp;
     // computing warps (a warp per row group, up to the kernel's thread
     // budget) and one warp that stages the exchanged rows
-    const int max_threads = pl.shape == rk::kShapeR4B4 ? 512 : 640;
+    const int max_threads = pl.shape == rk::kShapeR4B4 ? 320 : 640;
     pl.threads = (int)std::min<int64_t>(max_threads - 32, std::max<int64_t>(256, 32 * (pl.rows_pad / rpw))) + 32;
     pl.grid = teams * pl.team_ctas;
     if (!finish(pl))

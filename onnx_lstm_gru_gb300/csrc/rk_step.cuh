@@ -47,7 +47,7 @@ namespace rk {
 
 // Row sums gs[(row0 + r) * gs_ld + col0 + b] = sum_k Rs[row0 + r][k] * hsrc[b][k]
 // for rows [row0, row0 + nrows) (nrows a multiple of RPW) and NBC batch rows.
-template <int RPW, int NBC, typename T>
+template <int RPW, int NBC, typename T, int UNROLL = 1>
 __device__ __forceinline__ void matvec(const T* __restrict__ Rs, int KP, int row0, int nrows,
                                        const float* __restrict__ hsrc, float* __restrict__ gs, int gs_ld,
                                        int col0, int warp, int nwarps, int lane) {
@@ -59,6 +59,7 @@ __device__ __forceinline__ void matvec(const T* __restrict__ Rs, int KP, int row
     float acc[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) acc[i] = 0.0f;
+#pragma unroll UNROLL
     for (int kc = 0; kc < nchunks; ++kc) {
       const int k = (kc * 32 + lane) * 4;
       float4 hv[NBC];
@@ -125,7 +126,7 @@ __host__ __device__ inline SmemLayout smem_layout(const StepParams& p, int rows_
 // staging warp's state without spilling the tile).
 template <int RPW, int NBC, bool GRID>
 struct MaxThreads {
-  static constexpr int value = (RPW * NBC >= 32) ? (GRID ? 640 : 768) : 512;
+  static constexpr int value = (RPW * NBC >= 32) ? (GRID ? 640 : 768) : (GRID ? 320 : 512);
 };
 
 template <int CELL, typename T, bool GEN, int RPW, int NBC, bool GRID>
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_ker
           ok = stage_rows(global_src, c0, c0 == 0 ? ctr : nullptr, want);
         } else {
           ok = mbar_wait_bounded(smem_u32(&bars[0]), stage_no & 1u, p.timeout_ns);
-          matvec<RPW, NBC, T>(Rs, KP, row0, nrows, hs, gs, nb_ld, c0, warp, nwarps - 1, lane);
+          matvec<RPW, NBC, T, (RPW * NBC >= 32) ? 1 : 2>(Rs, KP, row0, nrows, hs, gs, nb_ld, c0, warp, nwarps - 1, lane);
         }
         ++stage_no;
         if (__syncthreads_or(!ok)) {
@@ -556,15 +557,13 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_ker
         if constexpr (CELL == 0) {
           const float cp = cs[bl * J + jl];
           float pi = pre[0], po = pre[1], pf = pre[2], pc = pre[3];
-          if (has_p) {
-            pi = pi + ppv[0] * cp;
-            pf = pf + ppv[2] * cp;
-          }
+          pi = has_p ? pi + ppv[0] * cp : pi;
+          pf = has_p ? pf + ppv[2] * cp : pf;
           const float ig = act<GEN, 0>(af, clip_pre(p.clip, pi));
           const float fg = p.input_forget ? 1.0f - ig : act<GEN, 0>(af, clip_pre(p.clip, pf));
           const float cg = act<GEN, 1>(ag, clip_pre(p.clip, pc));
           const float cn = fg * cp + ig * cg;
-          if (has_p) po = po + ppv[1] * cn;
+          po = has_p ? po + ppv[1] * cn : po;
           const float og = act<GEN, 0>(af, clip_pre(p.clip, po));
           hn = og * act<GEN, 1>(ah, cn);
           cs[bl * J + jl] = cn;

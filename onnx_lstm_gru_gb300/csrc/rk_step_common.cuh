@@ -161,6 +161,34 @@ __device__ __forceinline__ float act_eval(int kind, float a, float b, float x) {
   return __int_as_float(0x7fffffff);
 }
 
+// The same activations with at most two branches (taken by the whole launch
+// alike) instead of one per kind: sigmoid, tanh and scaled tanh share one
+// exponential and one fast reciprocal; relu, affine, leaky relu,
+// thresholded relu, hard sigmoid and softsign are a few operations each,
+// chosen by selects, and never wait for the exponential; ELU and Softplus go
+// to act_eval.  Each kind's value comes from the same operations as in
+// act_eval (2 * r with r = __fdividef(1, y) equals __fdividef(2, y): the fast
+// division multiplies by an approximate reciprocal, and doubling is exact),
+// so the two give the same bits.
+__device__ __forceinline__ float act_eval_any(int kind, float a, float b, float x) {
+  if (kind == 0 || kind == 1 || kind == 6) {
+    const float u = kind == 6 ? b * x : x;
+    const float e = __expf(kind == 0 ? -u : 2.0f * u);
+    const float r = __fdividef(1.0f, 1.0f + e);  // sigmoid(x), or (1 - tanh(u)) / 2
+    const float th = 1.0f - 2.0f * r;
+    return kind == 0 ? r : (kind == 6 ? a * th : th);
+  }
+  if (kind < 2 || kind == 8 || kind > 9) return act_eval(kind, a, b, x);
+  const float hs = a * x + b;
+  float y = x / (1.0f + fabsf(x));  // softsign (9)
+  y = kind == 2 ? (x > 0.0f ? x : (x <= 0.0f ? 0.0f : x)) : y;
+  y = kind == 3 ? hs : y;
+  y = kind == 4 ? (x >= 0.0f ? x : (x < 0.0f ? a * x : x)) : y;
+  y = kind == 5 ? (x > a ? x : (x <= a ? 0.0f : x)) : y;
+  y = kind == 7 ? (hs < 0.0f ? 0.0f : (hs > 1.0f ? 1.0f : hs)) : y;
+  return y;
+}
+
 // Slot `slot` of direction d.  GEN = false compiles in the ONNX defaults.
 template <bool GEN, int DEFAULT_KIND>
 __device__ __forceinline__ float act(const StepParams& p, int idx, float x) {
@@ -176,18 +204,16 @@ __device__ __forceinline__ float act(const StepParams& p, int idx, float x) {
 template <bool GEN, int DEFAULT_KIND>
 __device__ __forceinline__ float act(const ActSlot& a, float x) {
   if constexpr (GEN) {
-    return act_eval(a.kind, a.alpha, a.beta, x);
+    return act_eval_any(a.kind, a.alpha, a.beta, x);
   } else {
     return act_eval(DEFAULT_KIND, 0.0f, 0.0f, x);
   }
 }
 
 __device__ __forceinline__ float clip_pre(float c, float x) {
-  if (c > 0.0f) {
-    if (x > c) return c;
-    if (x < -c) return -c;
-  }
-  return x;
+  // selects, not branches; NaN passes (every comparison with it is false)
+  const float y = x > c ? c : (x < -c ? -c : x);
+  return c > 0.0f ? y : x;
 }
 
 // ------------------------------------------------------------------ indexing
