@@ -507,6 +507,10 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_ker
     }
 
     // gate arithmetic and state update, one (unit, batch row) pair per thread
+    // (grid kernel: the first pair's Y element is stored after the team
+    // counter's release, which then waits only for the exchanged h)
+    float y_first = 0.0f;
+    size_t y_first_at = 0;
     for (int idx = tid_c; idx < npairs; idx += NTc) {
       const bool first = idx == tid_c;
       int jl, bl;
@@ -584,7 +588,12 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_ker
         }
       }
       hown[bl * J + jl] = hn;
-      if (Y != nullptr) store_elem<T>(Y + y0 + (size_t)t * y_tstride, active ? hn : 0.0f);
+      if (GRID && first) {
+        y_first = active ? hn : 0.0f;
+        y_first_at = y0 + (size_t)t * y_tstride;
+      } else if (Y != nullptr) {
+        store_elem<T>(Y + y0 + (size_t)t * y_tstride, active ? hn : 0.0f);
+      }
       if constexpr (GRID) {
         p.hglob[(size_t)nxt * hbuf + g0] = hn;
       } else {
@@ -598,6 +607,7 @@ __global__ void __launch_bounds__(MaxThreads<RPW, NBC, GRID>::value, 1) step_ker
         asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read by bulk copies
         asm volatile("bar.sync 1, %0;" ::"r"(NTc) : "memory");
         if (tid == 0 && s + 1 < p.T) publish(ctr_h);
+        if (Y != nullptr && tid_c < npairs) store_elem<T>(Y + y_first_at, y_first);
       }
     } else if (s + 1 < p.T) {
       __syncthreads();
