@@ -37,8 +37,16 @@
 // every product that read h_s is complete.  GRU with linear_before_reset
 // = 0 runs two rounds per step: the first product gives z and r, each warp
 // pushes its 16-bit r (.) h_prev the same way into a second pair of buffers,
-// and the second product's candidate rows give R_h . (r (.) h).  The
-// summation order is fixed (k in increasing 16-wide steps), so runs are
+// and the second product gives R_h . (r (.) h).  Neither round needs all
+// 128 rows of M, and an MMA costs the same whatever its rows, so the rounds
+// stack k ranges into the rows instead: round 1 holds the z and r rows of
+// the first and of the second half of k (4 x 32 rows) against the h rows of
+// both halves (N = 32), round 2 the candidate rows of the four quarters of
+// k (4 x 32 rows) against the r (.) h rows of the four quarters (N = 64);
+// only the blocks of a k range times the same k range are used, and each
+// gate sum is the sum of its ranges in increasing order.  H / 32 MMAs per
+// step instead of H / 8.  The summation order is fixed (k in increasing
+// 16-wide steps within a range, ranges in order), so runs are
 // bit-identical.  Every wait is bounded; on expiry the kernel sets the
 // status word, drains its MMAs, frees its TMEM and returns.
 #pragma once
@@ -52,14 +60,41 @@ constexpr int XN = 16;         // MMA N: a direction's batch rows, padded
 constexpr int XJ = 32;         // hidden units per CTA
 constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at most
 constexpr int XBLK_B = XN * 128;   // bytes of one 64-k block of h
-constexpr uint32_t XACC_COLS = 32;  // TMEM columns of the two accumulators (2 rounds x 16)
+constexpr uint32_t XACC_COLS = 32;  // TMEM columns of the accumulator (one round: 16, rounded up)
+// GRU with linear_before_reset = 0: k ranges stacked into the rows (F = 2
+// ranges in round 1, 4 in round 2); TMEM columns of the round-1 accumulator
+// (N = 32), the round-2 accumulator (N = 64) and the start of the gate rows
+constexpr uint32_t XS_ACC1 = 0, XS_ACC2 = 64, XS_ROWS = 128;
+
+// 64-k blocks per k range when the operand's k is cut into F ranges.
+__host__ __device__ constexpr int tcs_blocks_per_range(int KB, int F) { return (KB + F - 1) / F; }
 
 // TMEM columns the kernel allocates for hidden size H: the accumulators,
 // then the CTA's gate rows as the MMA's A operand (lane = gate row, one
-// column per two k), a power of two.
-__host__ __device__ inline uint32_t tcs_tmem_cols(int H) {
+// column per two k), a power of two.  Stacked (GRU lbr 0): the z and r rows
+// of two k halves, then the candidate rows of four k quarters.
+__host__ __device__ inline uint32_t tcs_tmem_cols(int H, bool stacked) {
   const int KB = (H + SK - 1) / SK;
+  if (stacked)
+    return tmem_cols_for(XS_ROWS + (uint32_t)(tcs_blocks_per_range(KB, 2) + tcs_blocks_per_range(KB, 4)) * (SK / 2));
   return tmem_cols_for(XACC_COLS + (uint32_t)KB * (SK / 2));
+}
+
+// Bytes of one operand buffer: room for KB blocks of 16 rows, for 2 ranges
+// of ceil(KB / 2) blocks of 32 rows and for 4 ranges of ceil(KB / 4)
+// blocks of 64 rows alike (a multiple of 1 KB, the swizzle atom).
+__host__ __device__ inline int tcs_buffer_bytes(int H) {
+  const int KB = (H + SK - 1) / SK;
+  return tcs_blocks_per_range(KB, 4) * 4 * XBLK_B;
+}
+
+// Byte offset of element (batch row b, k) in an operand buffer whose k is
+// cut into F ranges of KBF = ceil(KB / F) blocks: block j of range q holds
+// rows q * 16 + b of 64 consecutive k, 128-byte swizzled (F = 1: the plain
+// layout, block kb = k / 64 of 16 rows).
+__device__ __forceinline__ uint32_t tcs_operand_offset(int F, int KBF, int b, int k) {
+  const int kb = k / SK, q = kb / KBF, j = kb - q * KBF;
+  return (uint32_t)j * (uint32_t)(F * XBLK_B) + sw128_offset(q * XN + b, k % SK);
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes from 32 registers.
@@ -85,7 +120,7 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint
       : "memory");
 }
 
-// Shared memory: [operands: [h, r (.) h][2 buffers][KB x 2 KB]][staged
+// Shared memory: [operands: [h, r (.) h][2 buffers][tcs_buffer_bytes]][staged
 // products [4 gates][16 rows][32 units] floats][barriers][biases].  The gate
 // rows live in TMEM.
 struct XsSmem {
@@ -93,9 +128,8 @@ struct XsSmem {
 };
 __host__ __device__ inline XsSmem xs_layout(int G, int H) {
   XsSmem L{};
-  const int KB = (H + SK - 1) / SK;
   size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
-  L.h = o;    o += (size_t)2 * 2 * KB * XBLK_B;
+  L.h = o;    o += (size_t)2 * 2 * tcs_buffer_bytes(H);
   L.acc = o;  o += (size_t)4 * XJ * XN * 4;
   L.bar = o;  o += 256;
   L.bias = o; o += (size_t)2 * 4 * XJ * 4 + 3 * XJ * 4;
@@ -111,7 +145,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
   // accumulators (columns 0 .. 31), then the gate rows (A operand)
-  const uint32_t kTmemCols = tcs_tmem_cols(p.H);
+  const uint32_t kTmemCols = tcs_tmem_cols(p.H, LBR0);
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const XsSmem L = xs_layout(G, p.H);
@@ -159,12 +193,20 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   // operand buffers: zero all (the k columns past the last CTA's units and
   // the rows past the batch belong to nobody; R is zero there too, but a
   // stale Inf or NaN times zero would not be), then h_0 into buffer 0
-  const int KBB = KB * XBLK_B;  // bytes of one buffer
+  const int KBB = tcs_buffer_bytes(H);  // bytes of one buffer
+  // k ranges stacked into the rows of each operand (1: not stacked) and
+  // 64-k blocks per range
+  const int F0 = LBR0 ? 2 : 1, F1 = 4;
+  const int KB0 = tcs_blocks_per_range(KB, F0), KB1 = tcs_blocks_per_range(KB, F1);
   for (int e = tid; e < 4 * KBB / 16; e += blockDim.x)
     reinterpret_cast<uint4*>(sH)[e] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
+  // byte offset of element (batch row b, k) of operand `which` in its buffer
+  auto op_off = [&](int which, int b, int k) {
+    return which == 0 ? tcs_operand_offset(F0, KB0, b, k) : tcs_operand_offset(F1, KB1, b, k);
+  };
   auto sh_at = [&](int which, int buf, int b, int j) {
-    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + (size_t)(j / SK) * XBLK_B + sw128_offset(b, j % SK));
+    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + op_off(which, b, j));
   };
   for (int e = tid; e < N * H; e += blockDim.x) {
     const int b = e / H, j = e % H;
@@ -209,14 +251,18 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   // cost tracks its operand bytes at these small N); from TMEM only the 512
   // bytes of h are read.  Warp w stores the rows of lane quarter w % 4 and
   // the 64-k blocks kb with kb % 2 == w / 4, one block (32 columns) at a time.
+  // Stacked (GRU lbr 0): lane quarter Q holds from column XS_ROWS the z
+  // (Q even) or r (Q odd) rows of k half Q / 2, ceil(KB / 2) blocks, and
+  // after those the candidate rows of k quarter Q, ceil(KB / 4) blocks.
   if (warp < 8) {
     const int q = warp & 3;
-    const int g = q, u = lane;  // row 32 q + lane
-    const bool row_ok = g < G && j0 + u < H;
-    const E* rrow = R + ((size_t)d * GH + (size_t)(row_ok ? g : 0) * H + (row_ok ? j0 + u : 0)) * H;
     const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
-    const uint32_t trow = *tmem_slot + ((uint32_t)(32 * q) << 16) + XACC_COLS;
-    for (int kb = warp >> 2; kb < KB; kb += 2) {
+    const uint32_t tlane = *tmem_slot + ((uint32_t)(32 * q) << 16);
+    // 64 k of block kb of gate g's row of unit j0 + lane into 32 columns at col
+    auto put_block = [&](int g, int kb, uint32_t col) {
+      const int u = lane;
+      const bool row_ok = g < G && j0 + u < H && kb < KB;
+      const E* rrow = R + ((size_t)d * GH + (size_t)(row_ok ? g : 0) * H + (row_ok ? j0 + u : 0)) * H;
       uint32_t v[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -237,7 +283,14 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         v[4 * c + 2] = w.z;
         v[4 * c + 3] = w.w;
       }
-      tmem_st32(trow + (uint32_t)(kb * (SK / 2)), v);
+      tmem_st32(tlane + col, v);
+    };
+    if constexpr (LBR0) {
+      for (int j = warp >> 2; j < KB0; j += 2) put_block(q & 1, (q >> 1) * KB0 + j, XS_ROWS + (uint32_t)(j * (SK / 2)));
+      for (int j = warp >> 2; j < KB1; j += 2)
+        put_block(2, q * KB1 + j, XS_ROWS + (uint32_t)((KB0 + j) * (SK / 2)));
+    } else {
+      for (int kb = warp >> 2; kb < KB; kb += 2) put_block(q, kb, XACC_COLS + (uint32_t)(kb * (SK / 2)));
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   }
@@ -296,8 +349,8 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       const uint32_t hi = __shfl_sync(0xffffffffu, hv, 8 * c + 2 * i + 1);
       w[i] = lo | (hi << 16);
     }
-    const int k = j0 + 8 * c;  // first unit of the chunk
-    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB + (k / SK) * XBLK_B) + sw128_offset(b, k % SK);
+    const int k = j0 + 8 * c;  // first unit of the chunk (the 8 units lie in one 64-k block)
+    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB) + op_off(which, b, k);
     const uint32_t bar = full_bar(which, buf);
     const float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]), __uint_as_float(w[3]));
     for (int q = lane >> 2; q < C; q += 8) st_async_v4(map_to_rank(dst, (uint32_t)q), x, map_to_rank(bar, (uint32_t)q));
@@ -310,8 +363,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
 
   if (warp == 9) {
     // ---------------- MMA lane: acc_rd[128 gate rows x 16 batch] = R_rows . operand^T
+    // (stacked: acc_rd[128 rows of F k ranges x 16 F rows of the same F ranges])
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(XN) | Elem<E>::kMmaAB;
+      const uint32_t idesc_st[2] = {idesc_f16(XN * 2) | Elem<E>::kMmaAB, idesc_f16(XN * 4) | Elem<E>::kMmaAB};
       const uint32_t ta0 = tmem_acc + XACC_COLS;  // the gate rows: 8 columns per 16 k
       constexpr uint64_t kK16 = 32 >> 4;
       bool ok = true;
@@ -330,14 +385,31 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
             break;
           }
           tc_fence_after();
-          const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
-          uint32_t ta = ta0;
           uint64_t bd = desc_sw128(su32(sH) + (uint32_t)((rd * 2 + (s & 1)) * KBB));
-          for (int kb = 0; kb < KB; ++kb, ta += SK / 2, bd += XBLK_B >> 4) {
-            tc_mma_ts(tacc, ta, bd, idesc, kb != 0 ? 1u : 0u);
-            tc_mma_ts(tacc, ta + 8, bd + kK16, idesc, 1u);
-            tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idesc, 1u);
-            tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idesc, 1u);
+          if constexpr (LBR0) {
+            // round rd: F ranges of KBF blocks; block j of every range in one
+            // MMA per 16 k (rows of range q times operand rows of range q
+            // are the products used)
+            const int F = rd == 0 ? F0 : F1, KBF = rd == 0 ? KB0 : KB1;
+            const uint32_t tacc = tmem_acc + (rd == 0 ? XS_ACC1 : XS_ACC2);
+            const uint32_t idn = idesc_st[rd];
+            uint32_t ta = tmem_acc + XS_ROWS + (uint32_t)(rd == 0 ? 0 : KB0 * (SK / 2));
+            const uint64_t bstep = (uint64_t)(F * XBLK_B) >> 4;
+            for (int j = 0; j < KBF; ++j, ta += SK / 2, bd += bstep) {
+              tc_mma_ts(tacc, ta, bd, idn, j != 0 ? 1u : 0u);
+              tc_mma_ts(tacc, ta + 8, bd + kK16, idn, 1u);
+              tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idn, 1u);
+              tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idn, 1u);
+            }
+          } else {
+            const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
+            uint32_t ta = ta0;
+            for (int kb = 0; kb < KB; ++kb, ta += SK / 2, bd += XBLK_B >> 4) {
+              tc_mma_ts(tacc, ta, bd, idesc, kb != 0 ? 1u : 0u);
+              tc_mma_ts(tacc, ta + 8, bd + kK16, idesc, 1u);
+              tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idesc, 1u);
+              tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idesc, 1u);
+            }
           }
           tc_commit(rbar(rd, 0));  // accumulator rd of step s complete
         }
@@ -366,13 +438,17 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     };
     // wait for accumulator rd of step s, stage gates [g0, g1) of it (warp g
     // holds gate g of the 32 units, lane = unit) and make them visible to
-    // every gate warp
+    // every gate warp.  Stacked (GRU lbr 0): warp Q < 4 stages the sums of
+    // its lane quarter over its own k range (round 1: gate Q % 2, half
+    // Q / 2; round 2: the candidate gate, quarter Q) into slot Q.
     auto stage = [&](int rd, int s, int g0, int g1) -> bool {
       if (abort_flag || !bar_wait(rbar(rd, 0), (uint32_t)(s & 1), p.timeout_ns)) return false;
       tc_fence_after();
-      if (warp >= g0 && warp < g1) {
+      if (LBR0 ? warp < 4 : (warp >= g0 && warp < g1)) {
+        uint32_t col = (uint32_t)(rd * XN);
+        if constexpr (LBR0) col = rd == 0 ? XS_ACC1 + (uint32_t)((warp >> 1) * XN) : XS_ACC2 + (uint32_t)(warp * XN);
         uint32_t v[XN];
-        tmem_ld<XN>(tmem_acc + ((uint32_t)(warp * 32) << 16) + (uint32_t)(rd * XN), v);
+        tmem_ld<XN>(tmem_acc + ((uint32_t)(warp * 32) << 16) + col, v);
 #pragma unroll
         for (int b = 0; b < XN; ++b) sAcc[((size_t)warp * XN + b) * XJ + lane] = __uint_as_float(v[b]);
       }
@@ -401,8 +477,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           const int b = (tid + 256 * k) >> 5;
           float pre[2];
 #pragma unroll
-          for (int g = 0; g < 2; ++g)
-            pre[g] = ((xv[k][g] + sAcc[((size_t)g * XN + b) * XJ + pu]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
+          for (int g = 0; g < 2; ++g) {
+            // the two k halves of gate g's sum, in order
+            const float rec = sAcc[((size_t)g * XN + b) * XJ + pu] + sAcc[((size_t)(g + 2) * XN + b) * XJ + pu];
+            pre[g] = ((xv[k][g] + rec) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
+          }
           zr[k][0] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
           zr[k][1] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
           push_row(1, s & 1, b, pj < H ? zr[k][1] * hreg[k] : 0.0f);
@@ -423,7 +502,13 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         float rec[G], pre[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          rec[g] = (LBR0 && g < 2) ? 0.0f : sAcc[((size_t)g * XN + b) * XJ + pu];
+          if constexpr (LBR0) {
+            // the candidate's sum: its four k quarters, in order
+            const float* q0 = sAcc + (size_t)b * XJ + pu;
+            rec[g] = g < 2 ? 0.0f : ((q0[0] + q0[XN * XJ]) + q0[2 * XN * XJ]) + q0[3 * XN * XJ];
+          } else {
+            rec[g] = sAcc[((size_t)g * XN + b) * XJ + pu];
+          }
           pre[g] = ((xv[k][g] + rec[g]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
         }
         float hn = hreg[k];
