@@ -13,12 +13,11 @@
 // With a small batch the product is turned around: the MMA's M = 128 rows
 // are this CTA's gate rows (row g * 32 + u for gate g, unit u of its 32
 // units; rows past G * 32 are zero) held in TMEM as the MMA's A operand for
-// the whole layer, and its N = 16 columns are the direction's batch rows, so the
-// exchanged operand is only 16 rows of h (2 KB per 64 k).  A team is one
-// direction, one cluster of ceil(H / 32) CTAs.  Every CTA keeps the whole
-// 16-bit operand, double-buffered, in its own shared memory in the layout
-// the tensor cores read (H / 64 blocks of 16 rows x 64 k, 128-byte
-// swizzled).  Per step:
+// the whole layer, and its N = 16 columns are the direction's batch rows,
+// so the exchanged operand is only 16 rows of h (2 KB per 64 k).  A team is
+// one direction, one cluster of ceil(H / 32) CTAs.  Every CTA keeps the
+// whole 16-bit operand, double-buffered, in its own shared memory in the
+// layout the tensor cores read (128-byte swizzled rows of 64 k).  Per step:
 //   1. one lane issues the H / 16 MMAs (kind::f16, M = 128, N = 16,
 //      K = 16) on buffer s % 2 into one fp32 TMEM accumulator (lane = gate
 //      row, column = batch row) once that buffer's byte-counting mbarrier
@@ -34,21 +33,27 @@
 // A buffer is re-armed (expected bytes) before this CTA pushes the h that
 // lets its peers produce the next value for it, and a peer can only write
 // h_{s+2} into buffer s % 2 after it has every CTA's h_{s+1}, by which time
-// every product that read h_s is complete.  GRU with linear_before_reset
-// = 0 runs two rounds per step: the first product gives z and r, each warp
-// pushes its 16-bit r (.) h_prev the same way into a second pair of buffers,
-// and the second product gives R_h . (r (.) h).  Neither round needs all
-// 128 rows of M, and an MMA costs the same whatever its rows, so the rounds
-// stack k ranges into the rows instead: round 1 holds the z and r rows of
-// the first and of the second half of k (4 x 32 rows) against the h rows of
-// both halves (N = 32), round 2 the candidate rows of the four quarters of
-// k (4 x 32 rows) against the r (.) h rows of the four quarters (N = 64);
-// only the blocks of a k range times the same k range are used, and each
-// gate sum is the sum of its ranges in increasing order.  H / 32 MMAs per
-// step instead of H / 8.  The summation order is fixed (k in increasing
-// 16-wide steps within a range, ranges in order), so runs are
-// bit-identical.  Every wait is bounded; on expiry the kernel sets the
-// status word, drains its MMAs, frees its TMEM and returns.
+// every product that read h_s is complete.
+//
+// GRU with linear_before_reset = 0 needs r before it can exchange
+// r (.) h_prev, and the candidate's product only after that exchange, so
+// two products lie on each step's chain.  An MMA costs about the same
+// whatever its rows, so there the gates are multiplied one at a time with
+// k quarters stacked into the rows ("stacked"): the 32 rows of gate g for
+// k quarter q sit in TMEM lane quarter q, and the operand's rows for
+// quarter q are rows 16 q + b of a 64-row tile; one MMA per 16 k of a
+// quarter's blocks multiplies all four quarters at once into gate g's
+// accumulator (128 lanes x 64 columns), of which the blocks quarter q times
+// quarter q (lanes 32 q .., columns 16 q ..) are used, and a gate's sum is
+// its four quarters added in order.  r is multiplied first (H / 64 MMAs),
+// each warp pushes its 16-bit r (.) h_prev into a second pair of buffers
+// while z is multiplied, and the candidate's rows are multiplied against
+// that operand: 2 H / 64 MMAs on the chain instead of 2 H / 16.  (For the
+// other cells all gates are on the chain at once, and the plain single
+// product was measured faster than three stacked ones.)  The summation
+// order is fixed (k in increasing 16-wide steps, quarters in order), so
+// runs are bit-identical.  Every wait is bounded; on expiry the kernel sets
+// the status word, drains its MMAs, frees its TMEM and returns.
 #pragma once
 #include "rk_step_tc.cuh"
 
@@ -56,45 +61,38 @@ namespace rk {
 
 namespace {
 
-constexpr int XN = 16;         // MMA N: a direction's batch rows, padded
+constexpr int XN = 16;         // MMA N per k range: a direction's batch rows, padded
 constexpr int XJ = 32;         // hidden units per CTA
+constexpr int XQ = 4;          // k quarters stacked into the MMA's rows (GRU lbr 0)
 constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at most
-constexpr int XBLK_B = XN * 128;   // bytes of one 64-k block of h
-constexpr uint32_t XACC_COLS = 32;  // TMEM columns of the accumulator (one round: 16, rounded up)
-// GRU with linear_before_reset = 0: k ranges stacked into the rows (F = 2
-// ranges in round 1, 4 in round 2); TMEM columns of the round-1 accumulator
-// (N = 32), the round-2 accumulator (N = 64) and the start of the gate rows
-constexpr uint32_t XS_ACC1 = 0, XS_ACC2 = 64, XS_ROWS = 128;
+constexpr int XBLK_B = XN * 128;        // bytes of one 64-k block of the plain operand (16 rows)
+constexpr int XBLKQ_B = XQ * XBLK_B;    // bytes of one 64-k block of the stacked operand (64 rows)
+constexpr uint32_t XACC_COLS = 32;      // plain: TMEM columns of the accumulator (16, rounded up)
+constexpr uint32_t XACC = XQ * XN;      // stacked: TMEM columns of one gate's accumulator (N = 64)
 
-// 64-k blocks per k range when the operand's k is cut into F ranges.
-__host__ __device__ constexpr int tcs_blocks_per_range(int KB, int F) { return (KB + F - 1) / F; }
+// 64-k blocks per k quarter.
+__host__ __device__ constexpr int tcs_quarter_blocks(int H) { return ((H + SK - 1) / SK + XQ - 1) / XQ; }
 
-// TMEM columns the kernel allocates for hidden size H: the accumulators,
-// then the CTA's gate rows as the MMA's A operand (lane = gate row, one
-// column per two k), a power of two.  Stacked (GRU lbr 0): the z and r rows
-// of two k halves, then the candidate rows of four k quarters.
-__host__ __device__ inline uint32_t tcs_tmem_cols(int H, bool stacked) {
-  const int KB = (H + SK - 1) / SK;
-  if (stacked)
-    return tmem_cols_for(XS_ROWS + (uint32_t)(tcs_blocks_per_range(KB, 2) + tcs_blocks_per_range(KB, 4)) * (SK / 2));
-  return tmem_cols_for(XACC_COLS + (uint32_t)KB * (SK / 2));
+// TMEM columns the kernel allocates for hidden size H and G gates, a power
+// of two.  Plain: the accumulator, then the gate rows (lane = row g * 32 + u,
+// one column per two k).  Stacked: G accumulators of 64 columns, then gate
+// g's rows (lane = 32 q + u for k quarter q).
+__host__ __device__ inline uint32_t tcs_tmem_cols(int H, int G, bool stacked) {
+  if (stacked) return tmem_cols_for((uint32_t)G * (XACC + (uint32_t)tcs_quarter_blocks(H) * (SK / 2)));
+  return tmem_cols_for(XACC_COLS + (uint32_t)((H + SK - 1) / SK) * (SK / 2));
 }
 
-// Bytes of one operand buffer: room for KB blocks of 16 rows, for 2 ranges
-// of ceil(KB / 2) blocks of 32 rows and for 4 ranges of ceil(KB / 4)
-// blocks of 64 rows alike (a multiple of 1 KB, the swizzle atom).
-__host__ __device__ inline int tcs_buffer_bytes(int H) {
-  const int KB = (H + SK - 1) / SK;
-  return tcs_blocks_per_range(KB, 4) * 4 * XBLK_B;
-}
+// Bytes of one operand buffer, room for either layout (a multiple of 8 KB).
+__host__ __device__ inline int tcs_buffer_bytes(int H) { return tcs_quarter_blocks(H) * XBLKQ_B; }
 
-// Byte offset of element (batch row b, k) in an operand buffer whose k is
-// cut into F ranges of KBF = ceil(KB / F) blocks: block j of range q holds
-// rows q * 16 + b of 64 consecutive k, 128-byte swizzled (F = 1: the plain
-// layout, block kb = k / 64 of 16 rows).
-__device__ __forceinline__ uint32_t tcs_operand_offset(int F, int KBF, int b, int k) {
-  const int kb = k / SK, q = kb / KBF, j = kb - q * KBF;
-  return (uint32_t)j * (uint32_t)(F * XBLK_B) + sw128_offset(q * XN + b, k % SK);
+// Byte offset of element (batch row b, k) in an operand buffer, 128-byte
+// swizzled rows of 64 k.  Plain: block kb = k / 64 holds rows b.  Stacked:
+// block j of quarter q (KBQ blocks per quarter) holds rows 16 q + b.
+__device__ __forceinline__ uint32_t tcs_operand_offset(bool stacked, int KBQ, int b, int k) {
+  const int kb = k / SK;
+  if (!stacked) return (uint32_t)kb * (uint32_t)XBLK_B + sw128_offset(b, k % SK);
+  const int q = kb / KBQ, j = kb - q * KBQ;
+  return (uint32_t)j * (uint32_t)XBLKQ_B + sw128_offset(q * XN + b, k % SK);
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes from 32 registers.
@@ -121,8 +119,8 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint
 }
 
 // Shared memory: [operands: [h, r (.) h][2 buffers][tcs_buffer_bytes]][staged
-// products [4 gates][16 rows][32 units] floats][barriers][biases].  The gate
-// rows live in TMEM.
+// quarter sums [4 gates][4 quarters][16 rows][32 units] floats][barriers]
+// [biases].  The gate rows live in TMEM.
 struct XsSmem {
   size_t h, acc, bar, bias, total;
 };
@@ -130,7 +128,7 @@ __host__ __device__ inline XsSmem xs_layout(int G, int H) {
   XsSmem L{};
   size_t o = 1024;  // room to align the dynamic base up to 1024 bytes
   L.h = o;    o += (size_t)2 * 2 * tcs_buffer_bytes(H);
-  L.acc = o;  o += (size_t)4 * XJ * XN * 4;
+  L.acc = o;  o += (size_t)4 * XQ * XJ * XN * 4;
   L.bar = o;  o += 256;
   L.bias = o; o += (size_t)2 * 4 * XJ * 4 + 3 * XJ * 4;
   L.total = o;
@@ -140,23 +138,22 @@ __host__ __device__ inline XsSmem xs_layout(int G, int H) {
 
 template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
 __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams p) {
-  static_assert(!LBR0 || CELL == 1, "two rounds only for GRU with linear_before_reset = 0");
-  constexpr int NRND = LBR0 ? 2 : 1;  // products per step
+  static_assert(!LBR0 || CELL == 1, "r (.) h exchange only for GRU with linear_before_reset = 0");
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
-  // accumulators (columns 0 .. 31), then the gate rows (A operand)
-  const uint32_t kTmemCols = tcs_tmem_cols(p.H, LBR0);
+  // accumulators, then the gate rows (A operand): see tcs_tmem_cols
+  const uint32_t kTmemCols = tcs_tmem_cols(p.H, G, LBR0);
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const XsSmem L = xs_layout(G, p.H);
   unsigned char* sH = base + (L.h - 1024);
-  // staged products [g][b][u]: a gate thread's row b is warp-uniform and its
-  // unit is the lane, so its reads are 32 consecutive floats (the layout
-  // [g][u][b] had lanes 16 floats apart: 16-way bank conflicts)
+  // staged quarter sums [g][q][b][u]: a gate thread's row b is warp-uniform
+  // and its unit is the lane, so its reads are 32 consecutive floats (the
+  // layout [g][u][b] had lanes 16 floats apart: 16-way bank conflicts)
   float* sAcc = reinterpret_cast<float*>(base + (L.acc - 1024));
-  // operand arrived [round][buffer], drain, then per round: done, free, staged
+  // operand arrived [operand][buffer], drain, then per gate: done, free, staged
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + (L.bar - 1024));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   float* wb_s = reinterpret_cast<float*>(base + (L.bias - 1024));  // [g * XJ + u]
   float* rb_s = wb_s + 4 * XJ;
   float* pp_s = rb_s + 4 * XJ;                                     // [u * 3 + g]
@@ -194,19 +191,12 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   // the rows past the batch belong to nobody; R is zero there too, but a
   // stale Inf or NaN times zero would not be), then h_0 into buffer 0
   const int KBB = tcs_buffer_bytes(H);  // bytes of one buffer
-  // k ranges stacked into the rows of each operand (1: not stacked) and
-  // 64-k blocks per range
-  const int F0 = LBR0 ? 2 : 1, F1 = 4;
-  const int KB0 = tcs_blocks_per_range(KB, F0), KB1 = tcs_blocks_per_range(KB, F1);
+  const int KBQ = tcs_quarter_blocks(H);  // 64-k blocks per k quarter
   for (int e = tid; e < 4 * KBB / 16; e += blockDim.x)
     reinterpret_cast<uint4*>(sH)[e] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  // byte offset of element (batch row b, k) of operand `which` in its buffer
-  auto op_off = [&](int which, int b, int k) {
-    return which == 0 ? tcs_operand_offset(F0, KB0, b, k) : tcs_operand_offset(F1, KB1, b, k);
-  };
   auto sh_at = [&](int which, int buf, int b, int j) {
-    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + op_off(which, b, j));
+    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + tcs_operand_offset(LBR0, KBQ, b, j));
   };
   for (int e = tid; e < N * H; e += blockDim.x) {
     const int b = e / H, j = e % H;
@@ -216,10 +206,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   const uint32_t op_bytes = (uint32_t)C * (uint32_t)N * (uint32_t)(XJ * 2);
   auto full_bar = [&](int which, int buf) { return su32(&bars[which * 2 + buf]); };
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);  // operand [round][buffer] arrived
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[i]), 1);  // operand [h, r (.) h][buffer] arrived
     mbar_init(smem_u32(&bars[4]), 1);                                // final MMA drain
-    for (int rd = 0; rd < 2; ++rd) {
-      uint64_t* b3 = bars + 5 + 3 * rd;
+    for (int a = 0; a < G; ++a) {
+      uint64_t* b3 = bars + 5 + 3 * a;
       mbar_init(smem_u32(&b3[0]), 1);  // accumulator complete (MMA commit)
       mbar_init(smem_u32(&b3[1]), 8);  // accumulator read (8 gate warps)
       mbar_init(smem_u32(&b3[2]), 8);  // products staged (8 gate warps)
@@ -244,16 +234,15 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // The gate rows (row g * 32 + u for gate g, unit u; zero past G * 32
-  // rows, past H units and past H in k) go to TMEM once, as the MMA's A
-  // operand: lane = row, column XACC_COLS + k / 2 holding k and k + 1.
-  // From shared memory every MMA re-read its 4 KB of A there (the MMA's
-  // cost tracks its operand bytes at these small N); from TMEM only the 512
-  // bytes of h are read.  Warp w stores the rows of lane quarter w % 4 and
-  // the 64-k blocks kb with kb % 2 == w / 4, one block (32 columns) at a time.
-  // Stacked (GRU lbr 0): lane quarter Q holds from column XS_ROWS the z
-  // (Q even) or r (Q odd) rows of k half Q / 2, ceil(KB / 2) blocks, and
-  // after those the candidate rows of k quarter Q, ceil(KB / 4) blocks.
+  // The gate rows go to TMEM once, as the MMA's A operand (zero past H
+  // units, past G gates and past H in k), one column per two k.  From
+  // shared memory every MMA re-read its 4 KB of A there (the MMA's cost
+  // tracks its operand bytes at these small N); from TMEM only the operand
+  // is read.  Plain: row g * 32 + u in lane quarter g from column 32, warp w
+  // storing lane quarter w % 4 and the blocks kb with kb % 2 == w / 4.
+  // Stacked: gate g's rows of k quarter q in lanes 32 q + u from column
+  // G * 64 + g * KBQ * 32, warp w storing the blocks (g, j) with
+  // (g * KBQ + j) % 2 == w / 4; one block (32 columns) at a time.
   if (warp < 8) {
     const int q = warp & 3;
     const bool r_vec = (reinterpret_cast<uintptr_t>(R) & 15) == 0;
@@ -286,9 +275,10 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       tmem_st32(tlane + col, v);
     };
     if constexpr (LBR0) {
-      for (int j = warp >> 2; j < KB0; j += 2) put_block(q & 1, (q >> 1) * KB0 + j, XS_ROWS + (uint32_t)(j * (SK / 2)));
-      for (int j = warp >> 2; j < KB1; j += 2)
-        put_block(2, q * KB1 + j, XS_ROWS + (uint32_t)((KB0 + j) * (SK / 2)));
+      for (int i = warp >> 2; i < G * KBQ; i += 2) {
+        const int g = i / KBQ, j = i % KBQ;
+        put_block(g, q * KBQ + j, (uint32_t)(G * XACC) + (uint32_t)(i * (SK / 2)));
+      }
     } else {
       for (int kb = warp >> 2; kb < KB; kb += 2) put_block(q, kb, XACC_COLS + (uint32_t)(kb * (SK / 2)));
     }
@@ -333,8 +323,9 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   const uint32_t tmem_acc = *tmem_slot;
 
   const uint32_t bar_drain = su32(&bars[4]);
-  // round rd's barriers: done, free, staged
-  auto rbar = [&](int rd, int i) { return su32(&bars[5 + 3 * rd + i]); };
+  // gate g's barriers: accumulator complete (MMA commit), read (8 gate
+  // warps), quarter sums staged (8 gate warps)
+  auto gbar = [&](int g, int i) { return su32(&bars[5 + 3 * g + i]); };
   // push this warp's batch row b of operand `which` (lane = unit, value v)
   // into buffer buf of every CTA: lanes 8c .. 8c + 7 form the 16-byte
   // chunk c of the row, lane l sends chunk l % 4 to CTAs l / 4, l / 4 + 8
@@ -350,7 +341,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       w[i] = lo | (hi << 16);
     }
     const int k = j0 + 8 * c;  // first unit of the chunk (the 8 units lie in one 64-k block)
-    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB) + op_off(which, b, k);
+    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB) + tcs_operand_offset(LBR0, KBQ, b, k);
     const uint32_t bar = full_bar(which, buf);
     const float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]), __uint_as_float(w[3]));
     for (int q = lane >> 2; q < C; q += 8) st_async_v4(map_to_rank(dst, (uint32_t)q), x, map_to_rank(bar, (uint32_t)q));
@@ -362,56 +353,68 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
   const bool input_forget = !PLAIN && p.input_forget;
 
   if (warp == 9) {
-    // ---------------- MMA lane: acc_rd[128 gate rows x 16 batch] = R_rows . operand^T
-    // (stacked: acc_rd[128 rows of F k ranges x 16 F rows of the same F ranges])
+    // ---------------- MMA lane.  Stacked: per gate g, acc_g[128 rows of 4 k
+    // quarters x 64 operand rows of the same 4 quarters] = gate g's rows .
+    // operand^T
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(XN) | Elem<E>::kMmaAB;
-      const uint32_t idesc_st[2] = {idesc_f16(XN * 2) | Elem<E>::kMmaAB, idesc_f16(XN * 4) | Elem<E>::kMmaAB};
-      const uint32_t ta0 = tmem_acc + XACC_COLS;  // the gate rows: 8 columns per 16 k
+      const uint32_t idesc = idesc_f16(LBR0 ? (int)XACC : XN) | Elem<E>::kMmaAB;
       constexpr uint64_t kK16 = 32 >> 4;
+      constexpr uint64_t kBlk = (uint64_t)(LBR0 ? XBLKQ_B : XBLK_B) >> 4;
       bool ok = true;
       for (int s = 0; s < Tn && ok; ++s) {
-        for (int rd = 0; rd < NRND; ++rd) {
-          // operand rd of step s (buffer s % 2, its (s / 2)-th arrival)
-          if (abort_flag || !bar_wait(full_bar(rd, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
+        if constexpr (!LBR0) {
+          // plain: acc[128 gate rows x 16 batch rows] = R_rows . h^T over all of k
+          if (abort_flag || !bar_wait(full_bar(0, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
             ok = false;
             break;
           }
-          // the peers' st.async writes, acquired above, are read by the async proxy
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          // the gate warps must have read this accumulator of the previous step
-          if (s > 0 && !bar_wait(rbar(rd, 1), (uint32_t)((s - 1) & 1), p.timeout_ns)) {
+          if (s > 0 && !bar_wait(gbar(0, 1), (uint32_t)((s - 1) & 1), p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint64_t bd = desc_sw128(su32(sH) + (uint32_t)((rd * 2 + (s & 1)) * KBB));
-          if constexpr (LBR0) {
-            // round rd: F ranges of KBF blocks; block j of every range in one
-            // MMA per 16 k (rows of range q times operand rows of range q
-            // are the products used)
-            const int F = rd == 0 ? F0 : F1, KBF = rd == 0 ? KB0 : KB1;
-            const uint32_t tacc = tmem_acc + (rd == 0 ? XS_ACC1 : XS_ACC2);
-            const uint32_t idn = idesc_st[rd];
-            uint32_t ta = tmem_acc + XS_ROWS + (uint32_t)(rd == 0 ? 0 : KB0 * (SK / 2));
-            const uint64_t bstep = (uint64_t)(F * XBLK_B) >> 4;
-            for (int j = 0; j < KBF; ++j, ta += SK / 2, bd += bstep) {
-              tc_mma_ts(tacc, ta, bd, idn, j != 0 ? 1u : 0u);
-              tc_mma_ts(tacc, ta + 8, bd + kK16, idn, 1u);
-              tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idn, 1u);
-              tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idn, 1u);
+          uint32_t ta = tmem_acc + XACC_COLS;
+          uint64_t bd = desc_sw128(su32(sH) + (uint32_t)((s & 1) * KBB));
+          for (int kb = 0; kb < KB; ++kb, ta += SK / 2, bd += kBlk) {
+            tc_mma_ts(tmem_acc, ta, bd, idesc, kb != 0 ? 1u : 0u);
+            tc_mma_ts(tmem_acc, ta + 8, bd + kK16, idesc, 1u);
+            tc_mma_ts(tmem_acc, ta + 16, bd + 2 * kK16, idesc, 1u);
+            tc_mma_ts(tmem_acc, ta + 24, bd + 3 * kK16, idesc, 1u);
+          }
+          tc_commit(gbar(0, 0));  // accumulator of step s complete
+        } else {
+          // stacked: r first (its r (.) h goes out while z is multiplied),
+          // then z, then the candidate against r (.) h
+          for (int i = 0; i < G; ++i) {
+            const int g = i == 0 ? 1 : (i == 1 ? 0 : 2);
+            const int which = g == 2 ? 1 : 0;
+            if (i != 1) {
+              // operand `which` of step s (buffer s % 2, its (s / 2)-th arrival)
+              if (abort_flag || !bar_wait(full_bar(which, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              // the peers' st.async writes, acquired above, are read by the async proxy
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-          } else {
-            const uint32_t tacc = tmem_acc + (uint32_t)(rd * XN);
-            uint32_t ta = ta0;
-            for (int kb = 0; kb < KB; ++kb, ta += SK / 2, bd += XBLK_B >> 4) {
-              tc_mma_ts(tacc, ta, bd, idesc, kb != 0 ? 1u : 0u);
+            // the gate warps must have read this accumulator of the previous step
+            if (s > 0 && !bar_wait(gbar(g, 1), (uint32_t)((s - 1) & 1), p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t tacc = tmem_acc + (uint32_t)g * XACC;
+            uint32_t ta = tmem_acc + (uint32_t)(G * XACC) + (uint32_t)(g * KBQ * (SK / 2));
+            uint64_t bd = desc_sw128(su32(sH) + (uint32_t)((which * 2 + (s & 1)) * KBB));
+            for (int j = 0; j < KBQ; ++j, ta += SK / 2, bd += kBlk) {
+              tc_mma_ts(tacc, ta, bd, idesc, j != 0 ? 1u : 0u);
               tc_mma_ts(tacc, ta + 8, bd + kK16, idesc, 1u);
               tc_mma_ts(tacc, ta + 16, bd + 2 * kK16, idesc, 1u);
               tc_mma_ts(tacc, ta + 24, bd + 3 * kK16, idesc, 1u);
             }
+            tc_commit(gbar(g, 0));  // accumulator g of step s complete
           }
-          tc_commit(rbar(rd, 0));  // accumulator rd of step s complete
         }
       }
       if (!ok) {
@@ -436,38 +439,46 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         for (int g = 0; g < G; ++g) xv[k][g] = on ? __ldg(qx + (size_t)g * H) : 0.0f;
       }
     };
-    // wait for accumulator rd of step s, stage gates [g0, g1) of it (warp g
-    // holds gate g of the 32 units, lane = unit) and make them visible to
-    // every gate warp.  Stacked (GRU lbr 0): warp Q < 4 stages the sums of
-    // its lane quarter over its own k range (round 1: gate Q % 2, half
-    // Q / 2; round 2: the candidate gate, quarter Q) into slot Q.
-    auto stage = [&](int rd, int s, int g0, int g1) -> bool {
-      if (abort_flag || !bar_wait(rbar(rd, 0), (uint32_t)(s & 1), p.timeout_ns)) return false;
+    // Stacked: wait for gate g's accumulator of step s; the four warps of
+    // lane group g % 2 (warp w: lane quarter w % 4, i.e. k quarter q) stage
+    // the sums of their quarter (unit = lane) in shared memory.  Plain (g =
+    // 0, the one accumulator): warp w < G stages gate w (its lane quarter).
+    // Every gate warp then marks the accumulator read and the sums staged.
+    auto stage = [&](int g, int s) -> bool {
+      if (abort_flag || !bar_wait(gbar(g, 0), (uint32_t)(s & 1), p.timeout_ns)) return false;
       tc_fence_after();
-      if (LBR0 ? warp < 4 : (warp >= g0 && warp < g1)) {
-        uint32_t col = (uint32_t)(rd * XN);
-        if constexpr (LBR0) col = rd == 0 ? XS_ACC1 + (uint32_t)((warp >> 1) * XN) : XS_ACC2 + (uint32_t)(warp * XN);
+      if (LBR0 ? (warp >> 2) == (g & 1) : warp < G) {
+        const int q = warp & 3;
+        const int sg = LBR0 ? g : warp, sq = LBR0 ? q : 0;  // the slot: gate, quarter
         uint32_t v[XN];
-        tmem_ld<XN>(tmem_acc + ((uint32_t)(warp * 32) << 16) + col, v);
+        tmem_ld<XN>(tmem_acc + ((uint32_t)(q * 32) << 16) + (LBR0 ? (uint32_t)g * XACC + (uint32_t)(q * XN) : 0u), v);
+        float* dst = sAcc + (size_t)(sg * XQ + sq) * XN * XJ + lane;
 #pragma unroll
-        for (int b = 0; b < XN; ++b) sAcc[((size_t)warp * XN + b) * XJ + lane] = __uint_as_float(v[b]);
+        for (int b = 0; b < XN; ++b) dst[(size_t)b * XJ] = __uint_as_float(v[b]);
       }
       // the accumulator may be overwritten by the next step's product
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(rbar(rd, 1)) : "memory");
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(rbar(rd, 2)) : "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gbar(g, 1)) : "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gbar(g, 2)) : "memory");
       }
-      return bar_wait(rbar(rd, 2), (uint32_t)(s & 1), p.timeout_ns);
+      return true;
     };
-    float zr[XPAIRS][2];  // GRU linear_before_reset = 0: z and r between the rounds
+    auto staged = [&](int g, int s) { return bar_wait(gbar(g, 2), (uint32_t)(s & 1), p.timeout_ns); };
+    // gate g's sum for batch row b and this thread's unit (stacked: its four
+    // k quarters added in order)
+    auto gsum = [&](int g, int b) {
+      const float* q0 = sAcc + ((size_t)g * XQ * XN + b) * XJ + pu;
+      if constexpr (!LBR0) return q0[0];
+      return ((q0[0] + q0[XN * XJ]) + q0[2 * XN * XJ]) + q0[3 * XN * XJ];
+    };
     load_xw(0);
     bool ok = true;
     for (int s = 0; s < Tn; ++s) {
       if constexpr (LBR0) {
-        // round 0: z and r; push r (.) h_prev
-        if (!stage(0, s, 0, 2)) {
+        // r first; push r (.) h_prev; then z and the candidate (against r (.) h)
+        if (!stage(1, s) || !staged(1, s)) {
           ok = false;
           break;
         }
@@ -475,21 +486,15 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         for (int k = 0; k < XPAIRS; ++k) {
           if (!pv[k]) continue;  // the same for the whole warp
           const int b = (tid + 256 * k) >> 5;
-          float pre[2];
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            // the two k halves of gate g's sum, in order
-            const float rec = sAcc[((size_t)g * XN + b) * XJ + pu] + sAcc[((size_t)(g + 2) * XN + b) * XJ + pu];
-            pre[g] = ((xv[k][g] + rec) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
-          }
-          zr[k][0] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
-          zr[k][1] = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[1]));
-          push_row(1, s & 1, b, pj < H ? zr[k][1] * hreg[k] : 0.0f);
+          const float pr = ((xv[k][1] + gsum(1, b)) + wb_s[1 * XJ + pu]) + rb_s[1 * XJ + pu];
+          const float r = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pr));
+          push_row(1, s & 1, b, pj < H ? r * hreg[k] : 0.0f);
         }
-      }
-      // the last (or only) round: the remaining gate arithmetic
-      constexpr int RL = NRND - 1;
-      if (!stage(RL, s, LBR0 ? 2 : 0, G)) {
+        if (!stage(0, s) || !stage(2, s) || !staged(0, s) || !staged(2, s)) {
+          ok = false;
+          break;
+        }
+      } else if (!stage(0, s) || !staged(0, s)) {
         ok = false;
         break;
       }
@@ -502,13 +507,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
         float rec[G], pre[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          if constexpr (LBR0) {
-            // the candidate's sum: its four k quarters, in order
-            const float* q0 = sAcc + (size_t)b * XJ + pu;
-            rec[g] = g < 2 ? 0.0f : ((q0[0] + q0[XN * XJ]) + q0[2 * XN * XJ]) + q0[3 * XN * XJ];
-          } else {
-            rec[g] = sAcc[((size_t)g * XN + b) * XJ + pu];
-          }
+          rec[g] = (LBR0 && g == 1) ? 0.0f : gsum(g, b);  // r was done above
           pre[g] = ((xv[k][g] + rec[g]) + wb_s[g * XJ + pu]) + rb_s[g * XJ + pu];
         }
         float hn = hreg[k];
@@ -533,7 +532,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           float z, hc;
           if constexpr (LBR0) {
             // h~ = g(((xw_h + R_h . (r (.) h_prev)) + Wb_h) + Rb_h)
-            z = zr[k][0];
+            z = act<GEN, 0>(p, d * A + 0, clip_pre(clip, pre[0]));
             hc = act<GEN, 1>(p, d * A + 1, clip_pre(clip, pre[2]));
           } else {
             // linear_before_reset = 1: h~ = g((xw_h + r*(rec_h + Rb_h)) + Wb_h)
