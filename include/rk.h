@@ -229,16 +229,20 @@ rk_status rk_encode(rk_handle* h, const rk_problem* p, const rk_operands* ops,
                     const rk_scratch* scratch, void* stream);
 
 /* Same layer with HOST operand pointers (no counterpart on the pages, whose
- * tensors are always device buffers): copies the inputs to device buffers
- * owned by the handle (grown on demand), encodes on `stream`, copies the
- * requested outputs back and synchronises the stream before returning.  X
- * and W are copied on `stream`; the operands only the step kernel reads (R,
- * B, sequence_lens, initial states, P) on a second stream owned by the
- * handle, which starts after the work already on `stream` and joins it
- * before the step kernel, so those copies overlap the projection.  When it
- * returns, success or error, every copy it issued has completed (the host
- * buffers may be reused at once).  Host memory that is page-locked copies
- * asynchronously; other host memory is staged by the CUDA runtime. */
+ * tensors are always device buffers): encodes on `stream` and synchronises
+ * the stream before returning.  X and W are always copied to device buffers
+ * owned by the handle (grown on demand): W on `stream`, X on a second stream
+ * owned by the handle (started after the work already on `stream`, joined
+ * before the projection), so the two copies overlap.  Every other operand
+ * (R, B, sequence_lens, initial states, P; the outputs Y, Y_h, Y_c) that
+ * lies in page-locked host memory (cudaHostAlloc, cudaHostRegister, e.g. a
+ * pinned torch tensor) is not copied: the step kernel reads or writes it in
+ * place through the device's mapping of that memory, each element once.
+ * Operands in other host memory are copied: inputs on the second stream,
+ * joined just before the step kernel (they land while the projection
+ * runs), outputs back on `stream` after it.  When it returns, success or
+ * error, every copy and kernel it issued has completed (the host buffers may
+ * be reused at once). */
 rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* host_ops,
                          void* stream);
 

@@ -47,7 +47,9 @@ struct rk_handle {
   // rk_encode_host: a second stream copies the operands only the step kernel
   // reads while the first copies X and W and runs the projection
   cudaStream_t copy_stream = nullptr;
-  cudaEvent_t copy_ev[2] = {nullptr, nullptr};  // fork from the caller's stream, join before the step
+  // fork from the caller's stream; join before the step; X copied (join before the projection)
+  cudaEvent_t copy_ev[3] = {nullptr, nullptr, nullptr};
+  bool can_map_host = false;  // the device can address page-locked host memory
   // Plans of the last problems encoded (the planner's occupancy queries cost
   // more host time than a small layer takes on the GPU)
   struct PlanEntry {
@@ -224,6 +226,9 @@ rk_status ensure_device(rk_handle* h) {
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+  int map = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&map, cudaDevAttrCanMapHostMemory, h->device);
+  h->can_map_host = map != 0;
   if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
   if (e != cudaSuccess) return fail(h, RK_ERR_CUDA, "recurrent: device setup failed: %s", cudaGetErrorName(e));
@@ -1033,26 +1038,50 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
     rk_tensor* dst;
     int64_t bytes;
     bool input;
+    bool direct_ok;  // read or written by the kernels with plain loads and stores only
   };
   rk_operands dev = {};
+  // X and W feed the projection, which reads them with asynchronous copies
+  // (cp.async, TMA): always copied to device memory
   Item items[11] = {
-      {&host_ops->X, &dev.X, ex.X * eb, true},
-      {&host_ops->W, &dev.W, ex.W * eb, true},
-      {&host_ops->R, &dev.R, ex.R * eb, true},
-      {&host_ops->B, &dev.B, ex.B * eb, true},
-      {&host_ops->sequence_lens, &dev.sequence_lens, ex.lens * 4, true},
-      {&host_ops->initial_h, &dev.initial_h, ex.state * eb, true},
-      {&host_ops->initial_c, &dev.initial_c, ex.state * eb, true},
-      {&host_ops->P, &dev.P, ex.P * eb, true},
-      {&host_ops->Y, &dev.Y, ex.Y * eb, false},
-      {&host_ops->Y_h, &dev.Y_h, ex.state * eb, false},
-      {&host_ops->Y_c, &dev.Y_c, ex.state * eb, false},
+      {&host_ops->X, &dev.X, ex.X * eb, true, false},
+      {&host_ops->W, &dev.W, ex.W * eb, true, false},
+      {&host_ops->R, &dev.R, ex.R * eb, true, true},
+      {&host_ops->B, &dev.B, ex.B * eb, true, true},
+      {&host_ops->sequence_lens, &dev.sequence_lens, ex.lens * 4, true, true},
+      {&host_ops->initial_h, &dev.initial_h, ex.state * eb, true, true},
+      {&host_ops->initial_c, &dev.initial_c, ex.state * eb, true, true},
+      {&host_ops->P, &dev.P, ex.P * eb, true, true},
+      {&host_ops->Y, &dev.Y, ex.Y * eb, false, true},
+      {&host_ops->Y_h, &dev.Y_h, ex.state * eb, false, true},
+      {&host_ops->Y_c, &dev.Y_c, ex.state * eb, false, true},
   };
+  // Page-locked host memory is mapped into the device's address space, so
+  // the step kernel reads R, B, the lengths, the initial states and P and
+  // writes Y, Y_h, Y_c there directly (over the CPU-GPU link, each byte once)
+  // instead of through a copy: a copy costs several microseconds of fixed
+  // latency before the first byte moves, which is more than a small layer's
+  // whole transfer.  Other host memory is copied.
+  void* direct[11] = {};
+  if (h->can_map_host) {
+    for (int i = 2; i < 11; ++i) {
+      const rk_tensor& t = *items[i].src;
+      if (!items[i].direct_ok || !t.ptr || items[i].bytes == 0) continue;
+      const int elem = (i == 4) ? 4 : eb;
+      const char* hp = static_cast<const char*>(t.ptr) + t.offset * elem;
+      cudaPointerAttributes a{};
+      if (cudaPointerGetAttributes(&a, hp) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) direct[i] = a.devicePointer;
+    }
+  }
   size_t total = 0;
   size_t offs[11];
   for (int i = 0; i < 11; ++i) {
     offs[i] = total;
-    if (items[i].src->ptr) total += (size_t)round_up(std::max<int64_t>(items[i].bytes, 1), 256);
+    if (items[i].src->ptr && !direct[i]) total += (size_t)round_up(std::max<int64_t>(items[i].bytes, 1), 256);
   }
   if (h->host_arena_cap < total) {
     if (h->host_arena) {
@@ -1070,28 +1099,39 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
   }
   if (h->copy_stream == nullptr) {
     cudaError_t e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&h->copy_ev[i], cudaEventDisableTiming);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&h->copy_ev[i], cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(h, p, "copy stream set-up", e);
   }
-  // X and W (the projection's operands) on the caller's stream; R, B, the
-  // lengths, initial states and P on the copy stream, forked after the
-  // caller's earlier work and joined just before the step kernel, so they
-  // land while the projection runs
+  // W on the caller's stream; X first on the copy stream (forked after the
+  // caller's earlier work, joined before the projection), so the two copies
+  // overlap; then the other copied operands, joined just before the step
+  // kernel, so they land while the projection runs
   cudaError_t e = cudaEventRecord(h->copy_ev[0], stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->copy_stream, h->copy_ev[0], 0);
   if (e != cudaSuccess) return cuda_fail(h, p, "copy stream fork", e);
-  for (int i = 0; i < 11; ++i) {
+  for (int i = 0; i < 8; ++i) {
     if (!items[i].src->ptr) continue;
     const int elem = (i == 4) ? 4 : eb;
-    items[i].dst->ptr = h->host_arena + offs[i];
     items[i].dst->offset = 0;
     items[i].dst->length = items[i].bytes / elem;
-    if (items[i].input && items[i].bytes > 0) {
+    if (direct[i]) {
+      items[i].dst->ptr = direct[i];
+      continue;
+    }
+    items[i].dst->ptr = h->host_arena + offs[i];
+    if (items[i].bytes > 0) {
       const char* src = static_cast<const char*>(items[i].src->ptr) + items[i].src->offset * elem;
       e = cudaMemcpyAsync(items[i].dst->ptr, src, (size_t)items[i].bytes, cudaMemcpyHostToDevice,
-                          i < 2 ? stream : h->copy_stream);
+                          i == 1 ? stream : h->copy_stream);
       if (e != cudaSuccess) break;
     }
+    if (i == 0 && e == cudaSuccess) e = cudaEventRecord(h->copy_ev[2], h->copy_stream);  // X landed
+  }
+  for (int i = 8; i < 11; ++i) {
+    if (!items[i].src->ptr) continue;
+    items[i].dst->offset = 0;
+    items[i].dst->length = items[i].bytes / eb;
+    items[i].dst->ptr = direct[i] ? direct[i] : h->host_arena + offs[i];
   }
   // on an error past this point the copies already issued are waited for,
   // so that the caller may reuse its host buffers at once
@@ -1106,13 +1146,20 @@ rk_status rk_encode_host(rk_handle* h, const rk_problem* p, const rk_operands* h
     return cuda_fail(h, p, "host-to-device copy", e != cudaSuccess ? e : j);
   }
   st = validate_all(h, p, &dev);
+  if (st == RK_OK && host_ops->X.ptr) {
+    e = cudaStreamWaitEvent(stream, h->copy_ev[2], 0);
+    if (e != cudaSuccess) {
+      drain();
+      return cuda_fail(h, p, "wait for the copy of X", e);
+    }
+  }
   if (st == RK_OK) st = encode_validated(h, p, &dev, nullptr, stream, h->copy_ev[1]);
   if (st != RK_OK) {
     drain();
     return st;
   }
   for (int i = 8; i < 11; ++i) {
-    if (!items[i].src->ptr || items[i].bytes == 0) continue;
+    if (!items[i].src->ptr || items[i].bytes == 0 || direct[i]) continue;
     char* dstp = static_cast<char*>(items[i].src->ptr) + items[i].src->offset * eb;
     e = cudaMemcpyAsync(dstp, items[i].dst->ptr, (size_t)items[i].bytes, cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) {

@@ -551,6 +551,47 @@ def test_host_buffer_entry_bfloat16():
         assert torch.equal(t.reshape(-1), dev[n + "_raw"].cpu()), n
 
 
+@pytest.mark.parametrize("name,flags", [("bilstm_s80_b1_i256_h256_f32", 0),
+                                        ("revlstm_peep_clip_s200_b4_i128_h1024_f32", 0),
+                                        ("bilstm_s48_b8_i192_h96_f16", 0),
+                                        ("bilstm_s48_b8_i192_h96_bf16", TC),
+                                        ("bigru_s128_b8_i512_h512_f16_lbr0", 0)])
+@pytest.mark.parametrize("mode", ["pinned", "pageable", "mixed"])
+def test_host_entry_pinned_buffers_in_place(name, flags, mode):
+    """The host entry reads page-locked inputs other than X and W, and
+    writes page-locked outputs, in place through the device's mapping of
+    that memory, and copies the rest: all pinned, all pageable and a mix give
+    the device entry's bits on the register-resident, grid, small-batch and
+    row-team tensor-core kernels, and the kernels' writes stay inside each
+    output (sentinels around it)."""
+    w = workloads.WORKLOADS[name]
+    pr = w.problem
+    inp = workloads.make_inputs(w)
+    dt = torch_dtype(pr)
+    want = run_gpu(pr, inp, flags=flags)
+
+    def place(t, i):
+        pinned = mode == "pinned" or (mode == "mixed" and i % 2 == 0)
+        return t.pin_memory() if pinned else t
+
+    ins = {k: place(torch.from_numpy(v) if k == "sequence_lens" else torch.from_numpy(v).to(dt), i)
+           for i, (k, v) in enumerate(sorted(inp.items()))}
+    shp = pr.shapes()
+    names = [n for n in ("Y", "Y_h", "Y_c") if not (n == "Y_c" and pr.cell != "lstm")]
+    bufs, outs = {}, {}
+    for i, n in enumerate(names):
+        m = int(np.prod(shp[n]))
+        bufs[n] = place(torch.full((m + 16,), SENTINEL, dtype=dt), i + 1)
+        outs[n] = bufs[n][8:8 + m]
+    for _ in range(2):
+        layer(flags).encode_host(pr, **ins, **outs)
+        for n in names:
+            b = bufs[n]
+            assert torch.all(b[:8] == SENTINEL) and torch.all(b[-8:] == SENTINEL), f"{n}: sentinel overwritten"
+            assert torch.equal(b[8:-8], want[n + "_raw"].cpu()), n
+    layer(flags).poll()
+
+
 def test_host_entry_planner_memory_round_robin():
     """One handle encodes six different layers twice in turn through the host
     entry (more problems than the handle remembers plans for, so plans are
