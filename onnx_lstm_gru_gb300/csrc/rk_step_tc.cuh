@@ -186,6 +186,14 @@ __device__ __forceinline__ void store_halves(E* dst, const E (&v)[UH]) {
   if constexpr (UH == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(v);
   else *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(v);
 }
+// The same with the streaming cache hint (st.global.cs): for Y, written once
+// and not read in the launch, so that its lines leave L2 first and do not
+// push out what the launch still reads there (the Xw ring, the exchanged h).
+template <int UH, typename E>
+__device__ __forceinline__ void store_halves_streaming(E* dst, const E (&v)[UH]) {
+  if constexpr (UH == 8) __stcs(reinterpret_cast<uint4*>(dst), *reinterpret_cast<const uint4*>(v));
+  else __stcs(reinterpret_cast<uint2*>(dst), *reinterpret_cast<const uint2*>(v));
+}
 
 
 // Shared memory: [R slice: KB blocks of (16 G rows x 64 k) E][ring: stages x 16 KB][barriers][biases]
@@ -868,7 +876,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tc_kernel(const StepParams p
       if (grow && Y != nullptr) {
         E* ydst = Y + y_index(p, t, d, bg, jb);
         if (jb + UH <= H && (reinterpret_cast<uintptr_t>(ydst) % (2 * UH)) == 0) {
-          store_halves<UH>(ydst, yv);
+          store_halves_streaming<UH>(ydst, yv);
         } else {
           for (int u = 0; u < UH; ++u)
             if (jb + u < H) ydst[u] = yv[u];
