@@ -424,7 +424,7 @@ rk_status plan_step_uncached(rk_handle* h, const rk_problem* p, StepParams* sp, 
       pl.threads = 320;
       pl.grid = D * Cc;
       pl.stages = 1;
-      pl.smem = rk::step_tcs_smem(G, H, p->cell == RK_GRU && !p->linear_before_reset);
+      pl.smem = rk::step_tcs_smem(G, H, (p->cell == RK_GRU && !p->linear_before_reset) || p->cell == RK_RNN);
       if ((int)pl.smem <= smem_cap && (!check || resident(pl) >= 1)) {
         sp->team_ctas = pl.team_ctas;
         sp->J = pl.J;

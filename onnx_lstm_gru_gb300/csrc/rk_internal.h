@@ -154,7 +154,7 @@ size_t step_tc_smem(int G, int H, int stages, int units);
 // ceil(H / 32) CTAs per direction; plans it with nbc = 16): dynamic shared
 // memory and the launch, same contract as step_tc_entry (its exchanged h
 // stays in the CTAs' shared memory: h16 is not used).
-size_t step_tcs_smem(int G, int H, bool lbr0);
+size_t step_tcs_smem(int G, int H, bool stacked);
 cudaError_t step_tcs_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16);
 int step_tc_stages(int G, int H, int units, size_t smem_cap);
 cudaError_t step_tc_entry(const StepParams& p, const StepPlan& plan, cudaStream_t s, int* resident, void* h16,

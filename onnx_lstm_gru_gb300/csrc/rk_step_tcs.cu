@@ -8,9 +8,9 @@ namespace rk {
 // share an SM than their TMEM allocations fit at once.  A CTA beyond that
 // would wait in tcgen05.alloc for another to free its columns, and within a
 // cluster the others may be waiting for it.
-size_t step_tcs_smem(int G, int H, bool lbr0) {
+size_t step_tcs_smem(int G, int H, bool stacked) {
   const size_t need = xs_layout(G, H).total;
-  const int per_sm = (int)(512u / tcs_tmem_cols(H, G, lbr0));  // allocations that fit an SM's 512 columns
+  const int per_sm = (int)(512u / tcs_tmem_cols(H, G, stacked));  // allocations that fit an SM's 512 columns
   int dev = 0, sm_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || sm_smem <= 0) {

@@ -48,9 +48,11 @@
 // its four quarters added in order.  r is multiplied first (H / 64 MMAs),
 // each warp pushes its 16-bit r (.) h_prev into a second pair of buffers
 // while z is multiplied, and the candidate's rows are multiplied against
-// that operand: 2 H / 64 MMAs on the chain instead of 2 H / 16.  (For the
-// other cells all gates are on the chain at once, and the plain single
-// product was measured faster than three stacked ones.)  The summation
+// that operand: 2 H / 64 MMAs on the chain instead of 2 H / 16.  An RNN's
+// one gate fills only 32 of the 128 rows, so it is stacked the same way:
+// H / 64 MMAs per step instead of H / 16.  (For LSTM and GRU with
+// linear_before_reset = 1 all gates are on the chain at once, and the plain
+// single product was measured faster than three stacked ones.)  The summation
 // order is fixed (k in increasing 16-wide steps, quarters in order), so
 // runs are bit-identical.  Every wait is bounded; on expiry the kernel sets
 // the status word, drains its MMAs, frees its TMEM and returns.
@@ -63,7 +65,7 @@ namespace {
 
 constexpr int XN = 16;         // MMA N per k range: a direction's batch rows, padded
 constexpr int XJ = 32;         // hidden units per CTA
-constexpr int XQ = 4;          // k quarters stacked into the MMA's rows (GRU lbr 0)
+constexpr int XQ = 4;          // k quarters stacked into the MMA rows (GRU lbr 0, RNN)
 constexpr int XPAIRS = 2;      // (unit, batch row) pairs per gate thread at most
 constexpr int XBLK_B = XN * 128;        // bytes of one 64-k block of the plain operand (16 rows)
 constexpr int XBLKQ_B = XQ * XBLK_B;    // bytes of one 64-k block of the stacked operand (64 rows)
@@ -139,10 +141,13 @@ __host__ __device__ inline XsSmem xs_layout(int G, int H) {
 template <int CELL, bool GEN, bool PLAIN, bool LBR0, typename E>
 __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams p) {
   static_assert(!LBR0 || CELL == 1, "r (.) h exchange only for GRU with linear_before_reset = 0");
+  // k quarters stacked into the MMA rows: GRU lbr 0 (three gates, one at a
+  // time) and RNN (its one gate fills only 32 rows)
+  constexpr bool STK = LBR0 || CELL == 2;
   constexpr int G = CellInfo<CELL>::G;
   constexpr int A = CellInfo<CELL>::A;
   // accumulators, then the gate rows (A operand): see tcs_tmem_cols
-  const uint32_t kTmemCols = tcs_tmem_cols(p.H, G, LBR0);
+  const uint32_t kTmemCols = tcs_tmem_cols(p.H, G, STK);
   extern __shared__ unsigned char tsm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~(uintptr_t)1023);
   const XsSmem L = xs_layout(G, p.H);
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     reinterpret_cast<uint4*>(sH)[e] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   auto sh_at = [&](int which, int buf, int b, int j) {
-    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + tcs_operand_offset(LBR0, KBQ, b, j));
+    return reinterpret_cast<E*>(sH + (size_t)(which * 2 + buf) * KBB + tcs_operand_offset(STK, KBQ, b, j));
   };
   for (int e = tid; e < N * H; e += blockDim.x) {
     const int b = e / H, j = e % H;
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       }
       tmem_st32(tlane + col, v);
     };
-    if constexpr (LBR0) {
+    if constexpr (STK) {
       for (int i = warp >> 2; i < G * KBQ; i += 2) {
         const int g = i / KBQ, j = i % KBQ;
         put_block(g, q * KBQ + j, (uint32_t)(G * XACC) + (uint32_t)(i * (SK / 2)));
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
       w[i] = lo | (hi << 16);
     }
     const int k = j0 + 8 * c;  // first unit of the chunk (the 8 units lie in one 64-k block)
-    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB) + tcs_operand_offset(LBR0, KBQ, b, k);
+    const uint32_t dst = su32(sH) + (uint32_t)((which * 2 + buf) * KBB) + tcs_operand_offset(STK, KBQ, b, k);
     const uint32_t bar = full_bar(which, buf);
     const float4 x = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]), __uint_as_float(w[3]));
     for (int q = lane >> 2; q < C; q += 8) st_async_v4(map_to_rank(dst, (uint32_t)q), x, map_to_rank(bar, (uint32_t)q));
@@ -357,12 +362,12 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     // quarters x 64 operand rows of the same 4 quarters] = gate g's rows .
     // operand^T
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(LBR0 ? (int)XACC : XN) | Elem<E>::kMmaAB;
+      const uint32_t idesc = idesc_f16(STK ? (int)XACC : XN) | Elem<E>::kMmaAB;
       constexpr uint64_t kK16 = 32 >> 4;
-      constexpr uint64_t kBlk = (uint64_t)(LBR0 ? XBLKQ_B : XBLK_B) >> 4;
+      constexpr uint64_t kBlk = (uint64_t)(STK ? XBLKQ_B : XBLK_B) >> 4;
       bool ok = true;
       for (int s = 0; s < Tn && ok; ++s) {
-        if constexpr (!LBR0) {
+        if constexpr (!STK) {
           // plain: acc[128 gate rows x 16 batch rows] = R_rows . h^T over all of k
           if (abort_flag || !bar_wait(full_bar(0, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
             ok = false;
@@ -384,12 +389,13 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
           }
           tc_commit(gbar(0, 0));  // accumulator of step s complete
         } else {
-          // stacked: r first (its r (.) h goes out while z is multiplied),
-          // then z, then the candidate against r (.) h
+          // stacked.  GRU lbr 0: r first (its r (.) h goes out while z is
+          // multiplied), then z, then the candidate against r (.) h.  RNN:
+          // its one gate against h.
           for (int i = 0; i < G; ++i) {
-            const int g = i == 0 ? 1 : (i == 1 ? 0 : 2);
-            const int which = g == 2 ? 1 : 0;
-            if (i != 1) {
+            const int g = LBR0 ? (i == 0 ? 1 : (i == 1 ? 0 : 2)) : i;
+            const int which = (LBR0 && g == 2) ? 1 : 0;
+            if (i == 0 || which == 1) {
               // operand `which` of step s (buffer s % 2, its (s / 2)-th arrival)
               if (abort_flag || !bar_wait(full_bar(which, s & 1), (uint32_t)((s >> 1) & 1), p.timeout_ns)) {
                 ok = false;
@@ -447,11 +453,11 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     auto stage = [&](int g, int s) -> bool {
       if (abort_flag || !bar_wait(gbar(g, 0), (uint32_t)(s & 1), p.timeout_ns)) return false;
       tc_fence_after();
-      if (LBR0 ? (warp >> 2) == (g & 1) : warp < G) {
+      if (STK ? (warp >> 2) == (g & 1) : warp < G) {
         const int q = warp & 3;
-        const int sg = LBR0 ? g : warp, sq = LBR0 ? q : 0;  // the slot: gate, quarter
+        const int sg = STK ? g : warp, sq = STK ? q : 0;  // the slot: gate, quarter
         uint32_t v[XN];
-        tmem_ld<XN>(tmem_acc + ((uint32_t)(q * 32) << 16) + (LBR0 ? (uint32_t)g * XACC + (uint32_t)(q * XN) : 0u), v);
+        tmem_ld<XN>(tmem_acc + ((uint32_t)(q * 32) << 16) + (STK ? (uint32_t)g * XACC + (uint32_t)(q * XN) : 0u), v);
         float* dst = sAcc + (size_t)(sg * XQ + sq) * XN * XJ + lane;
 #pragma unroll
         for (int b = 0; b < XN; ++b) dst[(size_t)b * XJ] = __uint_as_float(v[b]);
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(STHREADS, 1) step_tcs_kernel(const StepParams 
     // k quarters added in order)
     auto gsum = [&](int g, int b) {
       const float* q0 = sAcc + ((size_t)g * XQ * XN + b) * XJ + pu;
-      if constexpr (!LBR0) return q0[0];
+      if constexpr (!STK) return q0[0];
       return ((q0[0] + q0[XN * XJ]) + q0[2 * XN * XJ]) + q0[3 * XN * XJ];
     };
     load_xw(0);

@@ -503,6 +503,35 @@ def test_tensor_core_gru_lbr0(H, N, direction, layout, opts, dtype):
             assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
 
 
+@pytest.mark.parametrize("H,N,direction,layout,opts", [(40, 4, "bidirectional", 0, "plain"),
+                                                     (200, 9, "reverse", 1, "full"),
+                                                     (512, 16, "bidirectional", 0, "full"),
+                                                     (512, 8, "forward", 1, "plain")])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tensor_core_rnn_stacked_quarters(H, N, direction, layout, opts, dtype):
+    """RNN on the small-batch tensor-core kernel, whose one gate is multiplied
+    with its four k quarters stacked into the MMA rows (whole and partly
+    empty quarters): matches the oracle within the type's tolerance and the
+    SIMT cluster kernel, and two runs give the same bits."""
+    kw = dict(clip=1.5) if opts == "full" else {}
+    if opts == "full":
+        D = 2 if direction == "bidirectional" else 1
+        kw["activations"] = [("softsign", 0, 0)] * D
+    pr = rk.Problem("rnn", seq=9, batch=N, input=24, hidden=H, direction=direction, dtype=dtype, layout=layout, **kw)
+    plan = layer(TC).plan(pr)
+    assert "variant=small" in plan, plan
+    lens = list(np.random.default_rng(H + N).integers(0, 10, N))
+    inp = rand_inputs(pr, seed=H + 5 * N, lens=lens, scale=0.2)
+    got = run_gpu(pr, inp, flags=TC)
+    compare(pr, got, run_oracle(pr, inp), lens)
+    simt = run_gpu(pr, inp, flags=rk.RK_FORCE_SIMT_STEP)
+    compare(pr, got, {k: v for k, v in simt.items() if not k.endswith("_raw")}, lens)
+    again = run_gpu(pr, inp, flags=TC)
+    for k in got:
+        if k.endswith("_raw"):
+            assert torch.equal(got[k], again[k]), f"{k}: two runs differ"
+
+
 @pytest.mark.parametrize("H,N", [(40, 5), (96, 130)])
 def test_tensor_core_step_ignores_stale_scratch(H, N):
     """The tensor-core step kernel reads its Half h copies in whole 64-wide k
