@@ -726,7 +726,9 @@ def run_gb300(args):
         "kernels_ms": {"projection": main.proj_ms, "step": main.step_ms},
         "roofline": roofline, "layer_roofline": layer_roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_gflops, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_s * 1e3},
+                "ms_per_step": e2e_s * 1e3,
+                "transfer": "pinned host buffers through rk_encode_host: X and W copied, the other inputs read "
+                            "and the outputs written in place by the step kernel over the CPU-GPU link"},
         "clocks": main.clocks, "gpu_launches": main.launches,
         "peaks": peaks_rec,
         # the other configurations of the benchmark list, measured in this run
