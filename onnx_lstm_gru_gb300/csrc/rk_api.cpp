@@ -44,8 +44,8 @@ struct rk_handle {
   bool profiling = false;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // proj start/end, step start/end
   bool ev_proj = false, ev_step = false;
-  // rk_encode_host: a second stream copies the operands only the step kernel
-  // reads while the first copies X and W and runs the projection
+  // rk_encode_host: a second stream copies X and the (pageable) operands only
+  // the step kernel reads while the first copies W and runs the projection
   cudaStream_t copy_stream = nullptr;
   // fork from the caller's stream; join before the step; X copied (join before the projection)
   cudaEvent_t copy_ev[3] = {nullptr, nullptr, nullptr};
